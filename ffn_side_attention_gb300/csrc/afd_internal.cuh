@@ -1,0 +1,275 @@
+// afd_internal.cuh -- internal structures, launch declarations and inline-PTX
+// helpers (mbarrier, TMA, tcgen05/TMEM) shared by the kernels of libafd_ffn.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/afd_ffn.h"
+
+namespace afd {
+
+// ---------------------------------------------------------------- constants
+constexpr int kWarp = 32;
+constexpr int kRouterTokTile = 16;  // tokens per router CTA
+constexpr int kRouterExpTile = 32;  // experts per router CTA
+constexpr int kGemmBN = 256;        // max tokens per GEMM tile (MMA N)
+constexpr int kGemmBM = 128;        // weight rows per MMA (MMA M)
+constexpr int kMaxExperts = 257;    // routed + shared
+
+// device error word bits
+constexpr int kErrTimeout = 1;
+constexpr int kErrRange = 2;
+
+// ---------------------------------------------------------------- batch table
+// The M source/output buffers of one forward, passed by value to kernels.
+// Token t lives in buffer m with row0[m] <= t < row0[m+1], row t - row0[m].
+struct SrcTable {
+  const void* src[AFD_MAX_SOURCES];
+  void* out[AFD_MAX_SOURCES];
+  int row0[AFD_MAX_SOURCES + 1];
+  int M;
+  int T;
+};
+
+__device__ __forceinline__ int src_of_token(const SrcTable& s, int t) {
+  int lo = 0, hi = s.M - 1;  // last m with row0[m] <= t
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (s.row0[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// ---------------------------------------------------------------- workspace
+struct Workspace {
+  int32_t* topk_idx = nullptr;  // [maxT*k]
+  float* topk_w = nullptr;      // [maxT*k]
+  float* logits = nullptr;      // [maxT*E]
+  int32_t* tile_counter = nullptr;  // [ceil(maxT/kRouterTokTile)]
+  int32_t* counts = nullptr;    // [E+S]
+  int32_t* offsets = nullptr;   // [E+S+1]
+  int32_t* tile_base = nullptr; // [E+S+1], prefix of ceil(counts/kGemmBN)
+  int32_t* perm = nullptr;      // [max_rows] token of each packed row
+  int32_t* pos = nullptr;       // [maxT*k]  packed row of each (t, j)
+  float* row_w = nullptr;       // [max_rows] routing weight of each packed row
+  void* P = nullptr;            // [max_rows, H] packed activations
+  float* P_scale = nullptr;     // [max_rows, H/128] (fp8)
+  void* Hb = nullptr;           // [max_rows, I] SwiGLU output
+  float* H_scale = nullptr;     // [max_rows, I/128] (fp8)
+  void* Y = nullptr;            // [max_rows, H] weighted expert outputs
+  int* err = nullptr;           // device error word
+  void* stage = nullptr;        // forward_host staging: [maxT, H] in + [maxT, H] out
+  int last_T = 0;
+  CUtensorMap tm_P, tm_H;       // B operands of the two GEMMs
+  bool ready = false;
+};
+
+// ---------------------------------------------------------------- launchers
+struct LayerDims {
+  int H, I, E, k, S, dtype;  // dtype: afd_dtype
+};
+
+cudaError_t launch_router(const SrcTable& st, const void* wrT, const float* bias, const LayerDims& d,
+                          Workspace& ws, cudaStream_t s);
+cudaError_t launch_routing(const LayerDims& d, int T, Workspace& ws, cudaStream_t s);
+cudaError_t launch_pack(const SrcTable& st, const LayerDims& d, int T, Workspace& ws, int num_sms,
+                        cudaStream_t s);
+cudaError_t launch_combine(const SrcTable& st, const LayerDims& d, int T, Workspace& ws, int num_sms,
+                           cudaStream_t s);
+cudaError_t launch_gemm_simt(const LayerDims& d, int T, const float* wg, const float* wu, const float* wd,
+                             Workspace& ws, cudaStream_t s);
+
+struct TcWeights {
+  const CUtensorMap* tm_wg;  // [(E+S)*I, H] K-major
+  const CUtensorMap* tm_wu;
+  const CUtensorMap* tm_wd;  // [(E+S)*H, I] K-major
+  const float* sg;           // fp8: [(E+S), I/128, H/128]  (m-block major)
+  const float* su;
+  const float* sd;           // fp8: [(E+S), H/128, I/128]
+};
+cudaError_t launch_gemm_tc(const LayerDims& d, int T, const TcWeights& w, Workspace& ws, int num_sms,
+                           cudaStream_t s);
+cudaError_t gemm_tc_setup();  // opt-in shared memory sizes (once per process)
+
+cudaError_t launch_transpose(const void* src, void* dst, int batch, int rows, int cols, int elem_bytes,
+                             cudaStream_t s);
+cudaError_t launch_transpose_f32(const float* src, float* dst, int batch, int rows, int cols,
+                                 cudaStream_t s);
+
+// ---------------------------------------------------------------- device helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// --- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of `bar`, giving up after `limit_ns` or as soon as
+// another thread of the CTA raised `*abort`.  On a timeout the CTA abort flag
+// and the kTimeout bit of the device error word are set.  Returns false when
+// the caller must abandon its work.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err,
+                                          uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > limit_ns) {
+        *abort = 1;
+        atomicOr(err, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// --- TMA (tiled, 2D) global -> shared, completion on an mbarrier
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// --- tcgen05 / TMEM
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Arrive once on `bar` when all tcgen05.mma issued so far by this thread complete.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16 (bf16 inputs, fp32 accumulate)
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Same for e4m3 x e4m3 (kind::f8f6f4), fp32 accumulate.
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns: thread i of the warp gets row
+// (lane base + i), columns [col, col+32).
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+        "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+        "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor for a K-major operand tile written by TMA
+// with 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+// The tile must start on a 1024-byte boundary.
+__device__ __forceinline__ uint64_t sw128_desc(const void* tile) {
+  uint64_t a = smem_u32(tile);
+  uint64_t d = 0;
+  d |= (a >> 4) & 0x3fffull;          // start address (16-byte units)
+  d |= 1ull << 16;                    // leading byte offset (unused when swizzled)
+  d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset: next 8-row group
+  d |= 1ull << 46;                    // descriptor version
+  d |= 2ull << 61;                    // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: fp32 accumulate, both operands K-major, M x N.
+// ab_fmt: kind::f16 -> 1 = bf16; kind::f8f6f4 -> 0 = e4m3.
+__device__ __forceinline__ uint32_t mma_idesc(uint32_t ab_fmt, int M, int N) {
+  return (1u << 4) | (ab_fmt << 7) | (ab_fmt << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+}  // namespace afd

@@ -1,0 +1,331 @@
+// gemm_tc.cu -- R4/R5: grouped expert GEMMs on the 5th-generation tensor
+// cores (tcgen05.mma, accumulators in TMEM, operands staged by TMA).
+//
+// The expert FFN of the layer is SwiGLU (gate/up projections, SiLU-gated
+// product, down projection).  "MoE系统与AFD架构概述", section 2.1, counts
+// its work as 6*B*H*I FLOPs per expert pass; section 3.3 fuses the activation
+// into the expert kernel.  Both GEMMs are grouped over experts: the rows of
+// expert e are the packed rows offsets[e] .. offsets[e+1]-1.
+//
+// Swap-AB: decode batches give an expert few tokens (1..~250), so the weight
+// matrix is the MMA's M side (128 weight rows per MMA) and the expert's tokens
+// are the N side (16..256, padded to 16).  Weights are stored K-major
+// ([rows][K]) at create time so both operands are K-major tiles.
+//   gate/up:  D0 = Wg^T[e][i0:i0+128, :] * P[rows]^T, D1 = Wu^T[...] * P^T;
+//             h[row, i] = silu(D0) * D1 -> bf16   (one CTA item = 128 channels)
+//   down:     D0 = Wd^T[e][o0:o0+128, :] * h^T,   D1 = rows o0+128..o0+256
+//             Y[row, o] = D -> bf16                (one CTA item = 256 columns)
+// Two accumulators of up to 256 fp32 columns fill the 512 TMEM columns.
+//
+// Work list: item = (group g, m tile, token tile) in that order, enumerated on
+// the device from tile_base (no host sync); items of one (g, m tile) are
+// adjacent so concurrently running CTAs share the weight tile in L2.  The
+// kernel is persistent: grid = SM count, CTA c takes items c, c+grid, ...
+//
+// Warp roles (192 threads): warp 0 lane 0 issues TMA into a 3-stage ring
+// (weights with an L2 evict-first hint, activations evict-last); warp 1
+// owns TMEM and lane 0 issues tcgen05.mma; warps 2-5 are the epilogue
+// (warp w reads TMEM lanes 32*(w%4) .. +31).  Every mbarrier wait is bounded:
+// on a timeout the CTA raises its abort flag and the device error word, every
+// role stops, issued copies and MMAs are drained, TMEM is freed and the kernel
+// returns.
+#include <cuda_bf16.h>
+
+#include "afd_internal.cuh"
+
+namespace afd {
+namespace {
+
+constexpr int kStages = 3;
+constexpr int kRowBytes = 128;                    // one 128-byte swizzle row of K
+constexpr int kATile = kGemmBM * kRowBytes;       // 16 KB
+constexpr int kBTile = kGemmBN * kRowBytes;       // 32 KB
+constexpr int kBBoxRows = 32;                     // rows per TMA box of B
+constexpr int kStageBytes = 2 * kATile + kBTile;  // 64 KB
+constexpr int kDynSmem = kStages * kStageBytes + 1024;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kDrainLimitNs = 200000000ull;
+
+struct TcArgs {
+  const int32_t* counts;
+  const int32_t* offsets;
+  const int32_t* tile_base;
+  int G;                 // groups: routed experts + shared
+  int num_kb;            // K / 64
+  int MT;                // m tiles per group
+  int a_rows_per_group;  // A rows per group (I for gate/up, H for down)
+  int a_mt_stride;       // A rows per m tile (128 gate/up, 256 down)
+  int a1_offset;         // A1 rows relative to A0 (0: other map; 128: same map)
+  uint16_t* out;         // bf16 [rows, ld_out]
+  int ld_out;
+  int mode;              // 0: SwiGLU(D0, D1) ; 1: D0 | D1 as two column blocks
+  int* err;
+};
+
+struct Item {
+  int g, mt, row0, nrows;
+};
+
+__device__ __forceinline__ Item decode_item(int item, int MT, int G, const int* tb, const int* off,
+                                            const int* cnt) {
+  int lo = 0, hi = G - 1;  // last g with MT * tb[g] <= item
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (MT * tb[mid] <= item) lo = mid; else hi = mid - 1;
+  }
+  Item it;
+  it.g = lo;
+  const int nt_g = tb[lo + 1] - tb[lo];
+  const int local = item - MT * tb[lo];
+  it.mt = local / nt_g;
+  const int nt = local - it.mt * nt_g;
+  it.row0 = off[lo] + nt * kGemmBN;
+  it.nrows = min(kGemmBN, cnt[lo] - nt * kGemmBN);
+  return it;
+}
+
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  return true;
+}
+
+__device__ __forceinline__ uint16_t f2bf(float v) {
+  __nv_bfloat16 b = __float2bfloat16_rn(v);
+  return *reinterpret_cast<uint16_t*>(&b);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                     const __grid_constant__ CUtensorMap tmB, const TcArgs args) {
+  extern __shared__ uint8_t dyn_smem[];
+  uint8_t* smem = dyn_smem + ((1024u - (smem_u32(dyn_smem) & 1023u)) & 1023u);
+
+  __shared__ __align__(8) uint64_t bars[2 * kStages + 3];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int s_tb[kMaxExperts + 1], s_off[kMaxExperts + 1], s_cnt[kMaxExperts];
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* tfull = bars + 2 * kStages;
+  uint64_t* tempty = tfull + 1;
+  uint64_t* drain = tfull + 2;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = args.G;
+  for (int g = threadIdx.x; g <= G; g += kThreads) {
+    s_tb[g] = args.tile_base[g];
+    s_off[g] = args.offsets[g];
+    if (g < G) s_cnt[g] = args.counts[g];
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, 4);
+    mbar_init(drain, 1);
+    s_abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA0);
+    tma_prefetch_desc(&tmA1);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const int total = args.MT * s_tb[G];
+  volatile int* abort = &s_abort;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_b = l2_policy_evict_last();
+      int s = 0;
+      uint32_t ph = 0, filled = 0, fill_ph = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
+        const Item it = decode_item(item, args.MT, G, s_tb, s_off, s_cnt);
+        const int a0 = it.g * args.a_rows_per_group + it.mt * args.a_mt_stride;
+        const int a1 = a0 + args.a1_offset;
+        const int nbox = (it.nrows + kBBoxRows - 1) / kBBoxRows;
+        const uint32_t bytes = 2 * kATile + nbox * kBBoxRows * kRowBytes;
+        for (int kb = 0; kb < args.num_kb; ++kb) {
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort, args.err)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + s * kStageBytes;
+          mbar_arrive_expect_tx(&full[s], bytes);
+          tma_load_2d_hint(st, &tmA0, &full[s], kb * 64, a0, pol_w);
+          tma_load_2d_hint(st + kATile, &tmA1, &full[s], kb * 64, a1, pol_w);
+          for (int b = 0; b < nbox; ++b)
+            tma_load_2d_hint(st + 2 * kATile + b * kBBoxRows * kRowBytes, &tmB, &full[s], kb * 64,
+                             it.row0 + b * kBBoxRows, pol_b);
+          filled |= 1u << s;
+          fill_ph = (fill_ph & ~(1u << s)) | (ph << s);
+          if (++s == kStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (!ok)  // let the copies already issued land before the CTA exits
+        for (int q = 0; q < kStages; ++q)
+          if ((filled >> q) & 1u) mbar_wait_limit(&full[q], (fill_ph >> q) & 1u, kDrainLimitNs);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      int s = 0;
+      uint32_t ph = 0, tph = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
+        const Item it = decode_item(item, args.MT, G, s_tb, s_off, s_cnt);
+        const int N = (it.nrows + 15) & ~15;
+        const uint32_t idesc = mma_idesc(1u, kGemmBM, N);
+        if (!mbar_wait(tempty, tph ^ 1u, abort, args.err)) break;
+        tph ^= 1u;
+        tc_fence_after();
+        for (int kb = 0; kb < args.num_kb; ++kb) {
+          if (!mbar_wait(&full[s], ph, abort, args.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint8_t* st = smem + s * kStageBytes;
+          const uint64_t da0 = sw128_desc(st);
+          const uint64_t da1 = sw128_desc(st + kATile);
+          const uint64_t db = sw128_desc(st + 2 * kATile);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {  // 4 x K=16 per 128-byte row
+            const uint32_t acc = (kb | kk) ? 1u : 0u;
+            mma_f16(tmem, da0 + 2 * kk, db + 2 * kk, idesc, acc);
+            mma_f16(tmem + kGemmBN, da1 + 2 * kk, db + 2 * kk, idesc, acc);
+          }
+          tc_commit(&empty[s]);
+          if (++s == kStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(tfull);
+      }
+      tc_commit(drain);  // all MMAs issued above complete before TMEM is freed
+      mbar_wait_limit(drain, 0, kDrainLimitNs);
+    }
+  } else {
+    // ---------------- epilogue: warps 2..5
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // row of the 128-row MMA tile
+    const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
+    uint32_t tph = 0;
+    for (int item = blockIdx.x; item < total; item += gridDim.x) {
+      const Item it = decode_item(item, args.MT, G, s_tb, s_off, s_cnt);
+      if (!mbar_wait(tfull, tph, abort, args.err)) break;
+      tph ^= 1u;
+      tc_fence_after();
+      for (int c = 0; c < it.nrows; c += 32) {
+        float d0[32], d1[32];
+        tmem_ld_32x32b_x32(t_lane + (uint32_t)c, d0);
+        tmem_ld_32x32b_x32(t_lane + (uint32_t)(kGemmBN + c), d1);
+        tmem_ld_wait();
+        const int nn = min(32, it.nrows - c);
+        uint16_t* o = args.out + (size_t)(it.row0 + c) * args.ld_out;
+        if (args.mode == 0) {
+          const int col = it.mt * kGemmBM + r;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (j < nn) {
+              const float g = d0[j];
+              const float hv = g / (1.0f + expf(-g)) * d1[j];
+              o[(size_t)j * args.ld_out + col] = f2bf(hv);
+            }
+          }
+        } else {
+          const int col = it.mt * 2 * kGemmBM + r;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (j < nn) {
+              o[(size_t)j * args.ld_out + col] = f2bf(d0[j]);
+              o[(size_t)j * args.ld_out + col + kGemmBM] = f2bf(d1[j]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t gemm_tc_setup() {
+  return cudaFuncSetAttribute(gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
+}
+
+cudaError_t launch_gemm_tc(const LayerDims& d, int T, const TcWeights& w, Workspace& ws, int num_sms,
+                           cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  if (d.dtype != AFD_BF16) return cudaErrorNotSupported;
+  const int G = d.E + d.S;
+  const long rows = (long)T * (d.k + d.S);
+  const long tiles_ub = rows / kGemmBN + G + 1;
+
+  TcArgs a{};
+  a.counts = ws.counts;
+  a.offsets = ws.offsets;
+  a.tile_base = ws.tile_base;
+  a.G = G;
+  a.err = ws.err;
+
+  // gate/up + SwiGLU: K = H, items of 128 intermediate channels
+  a.num_kb = d.H / 64;
+  a.MT = d.I / kGemmBM;
+  a.a_rows_per_group = d.I;
+  a.a_mt_stride = kGemmBM;
+  a.a1_offset = 0;
+  a.out = static_cast<uint16_t*>(ws.Hb);
+  a.ld_out = d.I;
+  a.mode = 0;
+  long items_ub = tiles_ub * a.MT;
+  int grid = (int)(items_ub < num_sms ? items_ub : num_sms);
+  gemm_bf16_kernel<<<grid, kThreads, kDynSmem, s>>>(*w.tm_wg, *w.tm_wu, ws.tm_P, a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  // down: K = I, items of 256 output columns (two 128-row MMAs)
+  a.num_kb = d.I / 64;
+  a.MT = d.H / (2 * kGemmBM);
+  a.a_rows_per_group = d.H;
+  a.a_mt_stride = 2 * kGemmBM;
+  a.a1_offset = kGemmBM;
+  a.out = static_cast<uint16_t*>(ws.Y);
+  a.ld_out = d.H;
+  a.mode = 1;
+  items_ub = tiles_ub * a.MT;
+  grid = (int)(items_ub < num_sms ? items_ub : num_sms);
+  gemm_bf16_kernel<<<grid, kThreads, kDynSmem, s>>>(*w.tm_wd, *w.tm_wd, ws.tm_H, a);
+  return cudaGetLastError();
+}
+
+}  // namespace afd

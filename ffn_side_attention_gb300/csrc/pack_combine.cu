@@ -1,0 +1,183 @@
+// pack_combine.cu -- R3 pack and R6 combine.
+//
+// Pack: "MoE 大规模分布式推理工程实战", section 2.2 (the pack kernel gathers
+// each item's token row into a destination-contiguous buffer using the
+// prefix-sum offsets); here rows are gathered straight from the M
+// attention-instance buffers into expert-contiguous order.  For the fp8 layer
+// the pack also quantises ("MoE系统与AFD架构概述", section 3.3, FP8
+// activations): per row, per 128 channels, scale = amax / 448 (IEEE fp32
+// division), code = e4m3(x / scale) rounded to nearest even with saturation;
+// an all-zero block gets scale 1.
+//
+// Combine: same page, section 1.1 (combine brings the k processed copies of a
+// token back).  out[t] = sum_j w[t,j] * Y[pos[t,j]] in slot order (+ the
+// shared expert's row), accumulated in fp32 and rounded once; written to the
+// token's own output buffer.  No atomics: the result is run-to-run identical.
+//
+// Both are HBM/L2-bound row copies: one warp per row, 16-byte vector accesses.
+#include "afd_internal.cuh"
+
+namespace afd {
+namespace {
+
+__device__ __forceinline__ const uint8_t* src_row(const SrcTable& st, int t, size_t row_bytes) {
+  int m = src_of_token(st, t);
+  return reinterpret_cast<const uint8_t*>(st.src[m]) + (size_t)(t - st.row0[m]) * row_bytes;
+}
+
+__device__ __forceinline__ uint8_t* out_row(const SrcTable& st, int t, size_t row_bytes) {
+  int m = src_of_token(st, t);
+  return reinterpret_cast<uint8_t*>(st.out[m]) + (size_t)(t - st.row0[m]) * row_bytes;
+}
+
+// row copy (bf16 or fp32 layers): P[row] = x[perm[row]]
+__global__ void __launch_bounds__(256) pack_copy_kernel(SrcTable st, const int32_t* __restrict__ perm, int rows,
+                                                        int row_bytes, uint8_t* __restrict__ P) {
+  const int lane = threadIdx.x & 31;
+  const int nvec = row_bytes >> 4;
+  for (int row = blockIdx.x * 8 + (threadIdx.x >> 5); row < rows; row += gridDim.x * 8) {
+    int t = __ldg(perm + row);
+    const uint4* s = reinterpret_cast<const uint4*>(src_row(st, t, row_bytes));
+    uint4* d = reinterpret_cast<uint4*>(P + (size_t)row * row_bytes);
+    for (int v = lane; v < nvec; v += 32) d[v] = __ldg(s + v);
+  }
+}
+
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// fp8 layer: P[row] = e4m3 codes of x[perm[row]], P_scale[row][b] per 128 channels.
+// A 128-channel block is 16 lanes x 8 channels; one 16-byte load per lane.
+__global__ void __launch_bounds__(256) pack_fp8_kernel(SrcTable st, const int32_t* __restrict__ perm, int rows,
+                                                       int H, uint8_t* __restrict__ P, float* __restrict__ P_scale) {
+  const int lane = threadIdx.x & 31;
+  const int nblk = H >> 7;
+  for (int row = blockIdx.x * 8 + (threadIdx.x >> 5); row < rows; row += gridDim.x * 8) {
+    int t = __ldg(perm + row);
+    const uint4* s = reinterpret_cast<const uint4*>(src_row(st, t, (size_t)H * 2));
+    uint2* d = reinterpret_cast<uint2*>(P + (size_t)row * H);
+    for (int v = lane; v < (H >> 3); v += 32) {  // H % 256 == 0: whole warp active
+      uint4 u = __ldg(s + v);
+      float x[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
+                    bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
+      float amax = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(x[q]));
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      float scale = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+      uint32_t q01, q23, q45, q67;
+      if (amax == 0.0f) {
+        q01 = q23 = q45 = q67 = 0;
+      } else {
+        q01 = cvt_e4m3x2(__fdiv_rn(x[1], scale), __fdiv_rn(x[0], scale));
+        q23 = cvt_e4m3x2(__fdiv_rn(x[3], scale), __fdiv_rn(x[2], scale));
+        q45 = cvt_e4m3x2(__fdiv_rn(x[5], scale), __fdiv_rn(x[4], scale));
+        q67 = cvt_e4m3x2(__fdiv_rn(x[7], scale), __fdiv_rn(x[6], scale));
+      }
+      d[v] = make_uint2(q01 | (q23 << 16), q45 | (q67 << 16));
+      if ((lane & 15) == 0) P_scale[(size_t)row * nblk + (v >> 4)] = scale;
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+
+// bf16 Y (bf16 / fp8 layers): one warp per token, 8 channels per lane step.
+__global__ void __launch_bounds__(256) combine_bf16_kernel(SrcTable st, const int32_t* __restrict__ pos,
+                                                           const float* __restrict__ topk_w,
+                                                           const uint16_t* __restrict__ Y, int T, int k, int S,
+                                                           int H) {
+  const int lane = threadIdx.x & 31;
+  for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < T; t += gridDim.x * 8) {
+    uint4* o = reinterpret_cast<uint4*>(out_row(st, t, (size_t)H * 2));
+    for (int v = lane; v < (H >> 3); v += 32) {
+      float acc[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+      for (int j = 0; j < k; ++j) {
+        int r = __ldg(pos + (size_t)t * k + j);
+        float w = __ldg(topk_w + (size_t)t * k + j);
+        uint4 u = __ldg(reinterpret_cast<const uint4*>(Y + (size_t)r * H) + v);
+        acc[0] = fmaf(w, bf16_lo(u.x), acc[0]); acc[1] = fmaf(w, bf16_hi(u.x), acc[1]);
+        acc[2] = fmaf(w, bf16_lo(u.y), acc[2]); acc[3] = fmaf(w, bf16_hi(u.y), acc[3]);
+        acc[4] = fmaf(w, bf16_lo(u.z), acc[4]); acc[5] = fmaf(w, bf16_hi(u.z), acc[5]);
+        acc[6] = fmaf(w, bf16_lo(u.w), acc[6]); acc[7] = fmaf(w, bf16_hi(u.w), acc[7]);
+      }
+      if (S) {
+        uint4 u = __ldg(reinterpret_cast<const uint4*>(Y + (size_t)(T * k + t) * H) + v);
+        acc[0] += bf16_lo(u.x); acc[1] += bf16_hi(u.x); acc[2] += bf16_lo(u.y); acc[3] += bf16_hi(u.y);
+        acc[4] += bf16_lo(u.z); acc[5] += bf16_hi(u.z); acc[6] += bf16_lo(u.w); acc[7] += bf16_hi(u.w);
+      }
+      o[v] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                        pack_bf16x2(acc[6], acc[7]));
+    }
+  }
+}
+
+// fp32 layer: 4 channels per lane step.
+__global__ void __launch_bounds__(256) combine_f32_kernel(SrcTable st, const int32_t* __restrict__ pos,
+                                                          const float* __restrict__ topk_w,
+                                                          const float* __restrict__ Y, int T, int k, int S, int H) {
+  const int lane = threadIdx.x & 31;
+  for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < T; t += gridDim.x * 8) {
+    float4* o = reinterpret_cast<float4*>(out_row(st, t, (size_t)H * 4));
+    for (int v = lane; v < (H >> 2); v += 32) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < k; ++j) {
+        int r = __ldg(pos + (size_t)t * k + j);
+        float w = __ldg(topk_w + (size_t)t * k + j);
+        float4 y = __ldg(reinterpret_cast<const float4*>(Y + (size_t)r * H) + v);
+        acc.x = fmaf(w, y.x, acc.x); acc.y = fmaf(w, y.y, acc.y);
+        acc.z = fmaf(w, y.z, acc.z); acc.w = fmaf(w, y.w, acc.w);
+      }
+      if (S) {
+        float4 y = __ldg(reinterpret_cast<const float4*>(Y + (size_t)(T * k + t) * H) + v);
+        acc.x += y.x; acc.y += y.y; acc.z += y.z; acc.w += y.w;
+      }
+      o[v] = acc;
+    }
+  }
+}
+
+inline int grid_for(int rows_per_block_units, int units, int num_sms) {
+  int want = (units + rows_per_block_units - 1) / rows_per_block_units;
+  int cap = num_sms * 8;
+  return want < cap ? (want > 0 ? want : 1) : cap;
+}
+
+}  // namespace
+
+cudaError_t launch_pack(const SrcTable& st, const LayerDims& d, int T, Workspace& ws, int num_sms,
+                        cudaStream_t s) {
+  const int rows = T * (d.k + d.S);
+  if (rows == 0) return cudaSuccess;
+  const int grid = grid_for(8, rows, num_sms);
+  if (d.dtype == AFD_FP8_E4M3)
+    pack_fp8_kernel<<<grid, 256, 0, s>>>(st, ws.perm, rows, d.H, static_cast<uint8_t*>(ws.P), ws.P_scale);
+  else
+    pack_copy_kernel<<<grid, 256, 0, s>>>(st, ws.perm, rows, d.H * (d.dtype == AFD_FP32 ? 4 : 2),
+                                          static_cast<uint8_t*>(ws.P));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const SrcTable& st, const LayerDims& d, int T, Workspace& ws, int num_sms,
+                           cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int grid = grid_for(8, T, num_sms);
+  if (d.dtype == AFD_FP32)
+    combine_f32_kernel<<<grid, 256, 0, s>>>(st, ws.pos, ws.topk_w, static_cast<const float*>(ws.Y), T, d.k, d.S,
+                                            d.H);
+  else
+    combine_bf16_kernel<<<grid, 256, 0, s>>>(st, ws.pos, ws.topk_w, static_cast<const uint16_t*>(ws.Y), T, d.k,
+                                             d.S, d.H);
+  return cudaGetLastError();
+}
+
+}  // namespace afd

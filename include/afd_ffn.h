@@ -1,0 +1,180 @@
+/*
+ * afd_ffn.h -- C ABI of libafd_ffn.so: the FFN-server side of
+ * Attention-FFN Disaggregation (AFD) on one GB300 (sm_103a).
+ *
+ * One aggregated decode batch of hidden states, gathered from M
+ * attention-instance buffers, runs through one MoE layer:
+ *   router (logits, top-k, softmax over the selected) -> per-expert
+ *   histogram / exclusive prefix sum / stable expert-contiguous order ->
+ *   pack (optionally e4m3 quantisation) -> grouped gate/up GEMM + SwiGLU ->
+ *   grouped down GEMM x routing weight -> weighted combine back into the M
+ *   output buffers.
+ *
+ * Sources for the operation:
+ *   - "大模型推理的内存与计算解耦：AFD 架构解析与性能验证" (FastAFD blog),
+ *     section 2 benefit one (several attention instances feed one FFN server,
+ *     e.g. 4 x 128 -> 512 tokens) and section 3 (the FFN service is a daemon:
+ *     receive activations -> gate routing + expert compute -> return;
+ *     batch shape travels as control-plane metadata, tensors as data plane).
+ *   - "MoE 大规模分布式推理工程实战", section 4.1 (router: linear gate,
+ *     optional bias on the logits, top-k on logits, softmax over the top-k),
+ *     section 2.2 (per-destination counts, prefix-sum offsets, pack kernel)
+ *     and section 1.1 (dispatch / combine of k copies per token).
+ *   - "MoE系统与AFD架构概述", section 2.1 (6*B*H*I FLOPs per expert layer),
+ *     section 3.3 (pre-sorting routing results, FP8 activations, fused
+ *     expert kernels) and section 1 (three-buffer overlap, 3BO).
+ *
+ * Conventions (all entry points):
+ *   - Return 0 on success, a negative AFD_E* code on failure; nothing throws.
+ *     afd_ffn_last_error() gives a one-line description of the last failure
+ *     on a handle.
+ *   - Pointers named *_dev are device pointers (cudaMalloc'd or torch
+ *     tensors on the same device); pointers named *_host are host memory.
+ *     All matrices are dense row-major.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Asynchronous calls only enqueue work: they never synchronise
+ *     the host, and their device-side failures show up in afd_ffn_check().
+ *   - The caller owns every buffer it passes in; the library owns its copies
+ *     of the weights and its workspaces, freed by afd_ffn_destroy().
+ *   - One handle runs one forward at a time: calls on one handle must not
+ *     overlap on the GPU (use afd_ffn_forward_pipelined for concurrency).
+ */
+#ifndef AFD_FFN_H_
+#define AFD_FFN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define AFD_MAX_SOURCES 64 /* attention-instance buffers per forward */
+#define AFD_MAX_MICRO 4    /* micro-batches of afd_ffn_forward_pipelined */
+
+/* status codes */
+#define AFD_OK 0
+#define AFD_EINVAL -1      /* bad argument (null, size, alignment, config) */
+#define AFD_ECUDA -2       /* a CUDA runtime/driver call failed */
+#define AFD_ECAPACITY -3   /* batch larger than max_tokens / max_sources */
+#define AFD_EUNSUPPORTED -4 /* configuration not supported by this build */
+#define AFD_EDEVICE -5     /* afd_ffn_check: the device error word was set */
+
+typedef enum {
+  AFD_FP32 = 0,     /* fp32 activations, weights, output (fp32 SIMT path) */
+  AFD_BF16 = 1,     /* bf16 activations, weights, output; fp32 accumulate */
+  AFD_FP8_E4M3 = 2, /* bf16 activations in/out; e4m3 weights (fp32 scale per
+                       128x128 block); activations quantised to e4m3 per
+                       token per 128 channels inside the layer */
+} afd_dtype;
+
+/* Layer shape and capacity.
+ *   H hidden size; I expert intermediate size; E routed experts; k top-k
+ *   (1 <= k <= E <= 256); n_shared 0 or 1 always-on shared expert of the
+ *   same shape, added with weight 1; max_sources bound on M per forward
+ *   (<= AFD_MAX_SOURCES); max_tokens bound on T = sum of src_counts.
+ *   bf16/fp8 need H % 256 == 0 and I % 128 == 0; fp32 needs H % 8 == 0. */
+typedef struct {
+  int H, I, E, k, n_shared, max_sources, max_tokens;
+  afd_dtype dtype;
+} afd_ffn_config;
+
+/* Weights (device pointers, row-major; read once by afd_ffn_create, which
+ * copies and re-lays them out -- the caller may free them afterwards).
+ *   w_router   [H, E]  fp32 for AFD_FP32, bf16 otherwise
+ *   router_bias [E] fp32, added to the logits before selection, or NULL
+ *   w_gate, w_up [E, H, I]; w_down [E, I, H]   (fp32 / bf16 / e4m3 codes)
+ *   s_gate, s_up [E, H/128, I/128]; s_down [E, I/128, H/128]  fp32 block
+ *              scales, AFD_FP8_E4M3 only (weight = e4m3 value * scale)
+ *   sh_*       shared expert, [H, I], [H, I], [I, H] (+ scales), when
+ *              n_shared == 1; NULL otherwise */
+typedef struct {
+  const void* w_router;
+  const float* router_bias;
+  const void* w_gate;
+  const void* w_up;
+  const void* w_down;
+  const float* s_gate;
+  const float* s_up;
+  const float* s_down;
+  const void* sh_gate;
+  const void* sh_up;
+  const void* sh_down;
+  const float* sh_s_gate;
+  const float* sh_s_up;
+  const float* sh_s_down;
+} afd_ffn_weights;
+
+typedef struct afd_ffn* afd_ffn_t;
+
+/* Create a layer on the current CUDA device.  Validates the config, copies
+ * the weights into kernel layout (K-major for the tensor-core GEMMs) and
+ * sizes one workspace for max_tokens.  Synchronous.  On failure *out is
+ * NULL and the return code says why (use afd_ffn_create_error() for text). */
+int afd_ffn_create(const afd_ffn_config* cfg, const afd_ffn_weights* w, afd_ffn_t* out);
+
+/* Text of the last afd_ffn_create failure in this thread. */
+const char* afd_ffn_create_error(void);
+
+/* One forward over M source buffers (the FFN daemon's loop body in the
+ * FastAFD blog, section 3).
+ *   src_ptrs_dev[m]  device pointer to [src_counts_host[m], H] activations
+ *                    (fp32 for AFD_FP32, bf16 otherwise), 16-byte aligned
+ *   src_counts_host  host array of M row counts (>= 0; 0 allowed); this is
+ *                    the control-plane batch metadata; tokens are numbered
+ *                    in (m, row) order, T = sum of the counts <= max_tokens
+ *   out_ptrs_dev[m]  device pointer to [src_counts_host[m], H] outputs
+ *                    (fp32 for AFD_FP32, bf16 otherwise), 16-byte aligned;
+ *                    must not alias the sources
+ * Enqueues the whole layer on `stream`; T == 0 enqueues nothing. */
+int afd_ffn_forward(afd_ffn_t h, void* stream, const void* const* src_ptrs_dev,
+                    const int* src_counts_host, int M, void* const* out_ptrs_dev);
+
+/* Same layer with the batch split into n_micro (1..AFD_MAX_MICRO) contiguous
+ * token ranges (sizes differ by at most one, earlier ones larger), each run on
+ * its own library stream and workspace; the ranges fork from and join back
+ * to `stream` with events.  This is the one-GPU stand-in for the three-buffer
+ * overlap ("MoE系统与AFD架构概述", section 1 and section 2.3).  Outputs are
+ * identical to afd_ffn_forward. */
+int afd_ffn_forward_pipelined(afd_ffn_t h, void* stream, int n_micro, const void* const* src_ptrs_dev,
+                              const int* src_counts_host, int M, void* const* out_ptrs_dev);
+
+/* End-to-end call with HOST buffers: copies each source to the device
+ * (one cudaMemcpyAsync per buffer), runs afd_ffn_forward, copies each output
+ * back, and synchronises `stream` before returning.  Pinned host memory makes
+ * the copies asynchronous DMA; pageable memory works but is slower.  The
+ * staging buffers are part of the handle's workspace. */
+int afd_ffn_forward_host(afd_ffn_t h, void* stream, const void* const* src_ptrs_host,
+                         const int* src_counts_host, int M, void* const* out_ptrs_host);
+
+/* Copy the routing of the last forward (workspace 0) into caller device
+ * buffers, each may be NULL to skip:
+ *   topk_idx [T*k] int32, topk_w [T*k] fp32 (slot order: descending logit,
+ *   ties to the lower expert id), counts [E] int32, offsets [E+1] int32
+ *   (exclusive prefix sum, offsets[E] = T*k), perm_token [T*k] int32 (token of
+ *   each packed row; rows of an expert in ascending token order), pos [T*k]
+ *   int32 (packed row of each (token, slot)), logits [T*E] fp32.
+ * Enqueued on `stream`; T is the token count of that forward. */
+int afd_ffn_debug_routing(afd_ffn_t h, void* stream, int* topk_idx, float* topk_w, int* counts, int* offsets,
+                          int* perm_token, int* pos, float* logits);
+
+/* Synchronise `stream`, then read and clear the device error word of every
+ * workspace.  Returns 0, or AFD_EDEVICE with the word's bits in
+ * afd_ffn_last_error(): 1 = a kernel's bounded wait ran out (the kernel
+ * abandoned its work and returned), 2 = a routing value out of range. */
+int afd_ffn_check(afd_ffn_t h, void* stream);
+
+/* Last error text of the handle ("" if none). */
+const char* afd_ffn_last_error(afd_ffn_t h);
+
+/* Bytes of device memory the handle holds (weights + workspaces). */
+size_t afd_ffn_device_bytes(afd_ffn_t h);
+
+/* Free everything the handle owns.  Synchronises the device first.
+ * NULL is a no-op. */
+void afd_ffn_destroy(afd_ffn_t h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* AFD_FFN_H_ */

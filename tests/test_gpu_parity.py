@@ -1,0 +1,136 @@
+"""GPU parity: the CUDA layer (through the C ABI) against the CPU oracle on
+the same seeded inputs.  Routing is compared bit for bit; outputs within the
+dtype's tolerance (tests/gpu_helpers.py)."""
+import numpy as np
+import pytest
+import torch
+
+from ffn_side_attention_gb300 import afd, synth
+
+from gpu_helpers import (assert_close, assert_routing_exact, make_layer, out_to_f64, ref_to_f64, run_case)
+
+pytestmark = pytest.mark.gpu
+
+
+def _small(dtype="bf16", H=256, I=256, E=16, k=4, S=0, zipf=0.0):
+    return synth.LayerConfig("small", H=H, I=I, E=E, k=k, S=S, dtype=dtype, B=0, M=0, zipf_s=zipf)
+
+
+def test_tiny_fp32_layer():
+    c = synth.CONFIGS["tiny_fp32"]
+    layer, srcs, outs, r, ref = run_case(c, [c.B] * c.M)
+    assert_routing_exact(c, r, ref, c.T)
+    assert_close(c, out_to_f64(outs), ref_to_f64(c, ref["out"]))
+
+
+@pytest.mark.parametrize("shape,counts", [
+    (dict(), [17, 0, 40]),                                   # ragged, an empty buffer
+    (dict(S=1), [1]),                                        # single token + shared expert
+    (dict(E=4, k=2, H=512, I=384), [300, 301]),              # experts with > 256 rows: several N tiles
+    (dict(E=64, k=8, H=768, I=640, S=1), [5, 3, 0, 9]),      # many experts, few tokens
+    (dict(E=8, k=8, H=256, I=128), [33]),                    # k = E: every expert on every token
+])
+def test_bf16_shapes(shape, counts):
+    c = _small(**shape)
+    T = sum(counts)
+    layer, srcs, outs, r, ref = run_case(c, counts)
+    assert_routing_exact(c, r, ref, T)
+    assert_close(c, out_to_f64(outs), ref_to_f64(c, ref["out"]))
+
+
+def test_bf16_zipf_bias_imbalance():
+    """Zipf(1.2) log-bias on the logits: a few experts take most tokens."""
+    c = _small(E=64, k=8, H=512, I=256, zipf=1.2)
+    counts = [100, 100, 100]
+    layer, srcs, outs, r, ref = run_case(c, counts)
+    assert_routing_exact(c, r, ref, 300)
+    assert r["counts"].max().item() > 256  # the hot expert spans two token tiles
+    assert_close(c, out_to_f64(outs), ref_to_f64(c, ref["out"]))
+
+
+@pytest.mark.parametrize("B,M", [(6, 1), (48, 4)])
+def test_qwen3_bf16_small_batches_full_output(B, M):
+    c = synth.CONFIGS["qwen3_bf16"].with_batch(B, M)
+    layer, srcs, outs, r, ref = run_case(c, [B] * M)
+    assert_routing_exact(c, r, ref, c.T)
+    assert_close(c, out_to_f64(outs), ref_to_f64(c, ref["out"]))
+
+
+def test_qwen3_bf16_full_size_sampled():
+    """T = 8 x 395 = 3160 (the largest aggregated batch): routing bit-exact on
+    every token, outputs checked on sampled tokens (buffer edges + random)."""
+    c = synth.CONFIGS["qwen3_bf16"]
+    T = c.T
+    rng = np.random.default_rng(11)
+    edges = sorted({0, T - 1} | {m * c.B for m in range(c.M)} | {m * c.B - 1 for m in range(1, c.M)})
+    tokens = sorted(set(edges) | set(rng.choice(T, 16, replace=False).tolist()))
+    layer, srcs, outs, r, ref = run_case(c, [c.B] * c.M, tokens=tokens)
+    assert_routing_exact(c, r, ref, T)
+    got = out_to_f64(outs)[tokens]
+    assert_close(c, got, ref_to_f64(c, ref["out"]))
+
+
+def test_pipelined_equals_single_and_deterministic():
+    c = _small(E=16, k=4, S=1, H=512, I=256)
+    counts = [50, 0, 77, 12]
+    srcs = synth.make_sources(c, "cuda", counts=counts)
+    w = synth.make_weights(c, "cuda")
+    layer = make_layer(c, w, max_tokens=200, max_sources=8)
+    a = [o.clone() for o in layer.forward(srcs)]
+    b = [o.clone() for o in layer.forward(srcs)]
+    for n in (2, 3, 4):
+        p = layer.forward(srcs, n_micro=n)
+        torch.cuda.synchronize()
+        for x, y in zip(a, p):
+            assert torch.equal(x, y), f"pipelined n_micro={n} differs"
+    for x, y in zip(a, b):
+        assert torch.equal(x, y), "two forwards differ"
+    layer.check()
+
+
+def test_forward_host_equals_device():
+    c = _small(E=16, k=4, H=256, I=256)
+    counts = [20, 9]
+    srcs = synth.make_sources(c, "cuda", counts=counts)
+    w = synth.make_weights(c, "cuda")
+    layer = make_layer(c, w, max_tokens=64, max_sources=4)
+    dev = layer.forward(srcs)
+    torch.cuda.synchronize()
+    hs = [s.cpu().pin_memory() for s in srcs]
+    ho = [torch.empty_like(s).pin_memory() for s in hs]
+    layer.forward_host(hs, ho)
+    for x, y in zip(dev, ho):
+        assert torch.equal(x.cpu(), y)
+
+
+def test_empty_batch_is_noop():
+    c = _small()
+    w = synth.make_weights(c, "cuda")
+    layer = make_layer(c, w, max_tokens=8, max_sources=4)
+    srcs = [torch.empty(0, c.H, dtype=torch.bfloat16, device="cuda")] * 3
+    outs = layer.forward(srcs)
+    layer.check()
+    assert all(o.shape[0] == 0 for o in outs)
+
+
+def test_argument_errors():
+    c = _small()
+    w = synth.make_weights(c, "cuda")
+    layer = make_layer(c, w, max_tokens=8, max_sources=2)
+    x = synth.make_sources(c, "cuda", counts=[9])
+    with pytest.raises(afd.AfdError) as e:
+        layer.forward(x)
+    assert e.value.code == afd.AFD_ECAPACITY
+    x = synth.make_sources(c, "cuda", counts=[1, 1, 1])
+    with pytest.raises(afd.AfdError) as e:
+        layer.forward(x)
+    assert e.value.code == afd.AFD_ECAPACITY
+    big = torch.zeros(3 * c.H + 8, dtype=torch.bfloat16, device="cuda")
+    mis = big[1:1 + 2 * c.H].view(2, c.H)  # 2-byte offset: not 16-byte aligned
+    with pytest.raises(afd.AfdError) as e:
+        layer.forward([mis])
+    assert e.value.code == afd.AFD_EINVAL
+    with pytest.raises(afd.AfdError) as e:
+        layer.forward(x[:1], n_micro=9)
+    assert e.value.code == afd.AFD_EINVAL
+    layer.check()
