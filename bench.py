@@ -1,0 +1,398 @@
+"""Benchmark of the FFN-server MoE layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config qwen3_bf16] [--B 395] [--M 8] [--n-micro 1]
+
+One step = one pass of the whole layer (router -> routing tables -> pack ->
+gate/up GEMM -> down GEMM -> combine) over one aggregated batch of T = B*M
+tokens from M source buffers, inputs already resident in HBM.  The default
+workload is the Qwen3-235B-A22B-shaped bf16 layer at its largest aggregated
+decode batch (B=395 per attention instance, M=8 instances, T=3160).
+
+Prints ONE JSON line (rank 0).  ``value`` is whole-job tokens/s; ``tflops``
+and ``layer_roofline`` give TFLOPS and the fraction of the layer roofline
+(slower of FLOPs at the measured bf16 tensor peak and algorithmic bytes at
+the measured HBM bandwidth); ``roofline`` is the dominant kernel's (the
+grouped gate/up GEMM) achieved HBM bandwidth against the measured peak.
+``e2e`` is the same metric through afd_ffn_forward_host with pinned host
+buffers (copies in the timed region).  ``cpu_baseline`` is the CPU oracle on
+a bounded sample of the same workload.
+
+``--impl reference`` times the CPU oracle itself (the reference of this
+build) on a bounded sample of the workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from ffn_side_attention_gb300 import roofline, synth  # noqa: E402
+
+METRIC = "MoE-FFN tokens/s and TFLOPS on 1 GB300; fraction of roofline per batch size"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def recorded_traffic(kernel_file: str):
+    """dram bytes per launch of the gate/up GEMM from the committed ncu summary,
+    or None when the kernel source changed since that capture."""
+    import hashlib
+
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "ffn_side_attention_gb300", "csrc", kernel_file)
+    if not (os.path.exists(p) and os.path.exists(src)):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    with open(src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()
+    if rec.get("source_sha256") != h:
+        return None
+    return rec
+
+
+def tc_peak(peaks, dtype):
+    """Dense tensor peak for the layer's dtype, TFLOP/s (fp8 = 2x the bf16 measurement, the nominal ratio)."""
+    bf16 = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    return bf16 * (2.0 if dtype == "fp8" else 1.0)
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        uuid = getattr(torch.cuda.get_device_properties(device_index), "uuid", None)
+        if uuid is not None:
+            u = str(uuid)
+            cmd.insert(1, f"--id={u if u.startswith('GPU-') else 'GPU-' + u}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, pw, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in out.strip().splitlines():
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+                pw.append(float(p[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        # samples under load: power above the midpoint of the observed range
+        thr = (min(pw) + max(pw)) / 2 if pw else 0
+        load = [s for s, w in zip(sm, pw) if w >= thr] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm), "samples_under_load": len(load), "power_w_max": max(pw)}
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+def barrier_max(world, seconds: float) -> float:
+    if world == 1:
+        return seconds
+    import torch.distributed as dist
+
+    t = torch.tensor([seconds], device="cuda", dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+def oracle_sample(cfg, srcs_dev, weights_dev, n_tokens):
+    """Oracle (all host cores) on the first n_tokens of the workload, whole
+    layer (routing + experts + combine).  -> (seconds, tokens, cores)"""
+    import oracle
+
+    oracle.build()
+    x = torch.cat([s for s in srcs_dev])[:n_tokens]
+    src = [synth.to_numpy_bits(x)]
+    w = synth.weights_numpy(weights_dev)
+    c = dict(H=cfg.H, I=cfg.I, E=cfg.E, k=cfg.k, S=cfg.S, dtype=cfg.dtype)
+    t0 = time.perf_counter()
+    oracle.moe_forward(c, src, w)
+    dt = time.perf_counter() - t0
+    return dt, n_tokens, oracle.num_threads(), w, c, src
+
+
+def default_sample_tokens(cfg):
+    # about 10-20 s of oracle work on 16 host cores
+    per_tok = 6.0 * (cfg.k + cfg.S) * cfg.H * cfg.I  # FLOPs per token
+    return max(8, min(cfg.T, int(16 * 12 * 0.75e9 / per_tok)))
+
+
+# ------------------------------------------------------------------ main legs
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    cfg = synth.CONFIGS[args.config].with_batch(args.B, args.M)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    srcs = synth.make_sources(cfg, dev)
+    w = synth.make_weights(cfg, dev)
+    import oracle
+
+    oracle.build()
+    wn = synth.weights_numpy(w)
+    c = dict(H=cfg.H, I=cfg.I, E=cfg.E, k=cfg.k, S=cfg.S, dtype=cfg.dtype)
+    xall = torch.cat(srcs)
+    if args.cpu_sample:
+        n = args.cpu_sample
+    else:
+        # size each step so that warmup + steps take about two minutes (at most 2 s a step)
+        n0 = min(8, cfg.T)
+        t0 = time.perf_counter()
+        oracle.moe_forward(c, [synth.to_numpy_bits(xall[:n0])], wn)
+        per_tok = (time.perf_counter() - t0) / n0
+        budget = min(2.0, 120.0 / max(args.steps + args.warmup, 1))
+        n = int(max(1, min(cfg.T, budget / max(per_tok, 1e-9))))
+    src = [synth.to_numpy_bits(xall[:n])]
+    for _ in range(args.warmup):
+        oracle.moe_forward(c, src, wn)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.moe_forward(c, src, wn)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    value = n / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{cfg.name} B={cfg.B} M={cfg.M} T={cfg.T}", "sample_tokens": n,
+                   "H": cfg.H, "I": cfg.I, "E": cfg.E, "k": cfg.k, "S": cfg.S, "layer_dtype": cfg.dtype},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"first {n} tokens of the workload, whole layer, per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    from ffn_side_attention_gb300 import afd
+
+    torch.cuda.set_device(local)
+    cfg = synth.CONFIGS[args.config].with_batch(args.B, args.M)
+    T = cfg.T
+    peaks, peak_src = load_peaks()
+    w = synth.make_weights(cfg, "cuda")
+    n_sets = 4  # rotating input sets
+    inputs = [synth.make_sources(cfg, "cuda", seed=s) for s in range(n_sets)]
+    outs = [[torch.empty_like(x) for x in srcs] for srcs in inputs]
+    layer = afd.MoELayer(cfg.H, cfg.I, cfg.E, cfg.k, cfg.dtype, w, n_shared=cfg.S, max_tokens=T,
+                         max_sources=max(cfg.M, 1))
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        layer.forward(inputs[i % n_sets], outs[i % n_sets], stream=stream, n_micro=args.n_micro)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    layer.check()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler is not None:
+        time.sleep(0.3)
+    # a short spin-up so the clock samples see the load
+    t_spin = time.perf_counter()
+    i = 0
+    while time.perf_counter() - t_spin < 0.5:
+        step(i)
+        i += 1
+        if i % 16 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    elapsed = barrier_max(world, ev0.elapsed_time(ev1) / 1e3)
+    clocks = sampler.stop() if sampler is not None else None
+    layer.check()
+    ms_step = elapsed / max(args.steps, 1) * 1e3
+
+    # per-kernel times (separate instrumented pass, same workload)
+    n_prof = min(args.steps, 50)
+    layer.profile_begin()
+    for i in range(n_prof):
+        step(i)
+    kms, nf = layer.profile_end()
+    k_avg = {k: v / max(nf, 1) for k, v in kms.items()}
+
+    # routing statistics of input set 0 (touched experts)
+    layer.forward(inputs[0], outs[0], stream=stream)
+    r = layer.routing(T)
+    counts = r["counts"].cpu()
+    touched = int((counts > 0).sum().item())
+
+    flops = roofline.layer_flops(cfg, T)
+    lbytes = roofline.layer_bytes(cfg, T, touched)
+    ptc = tc_peak(peaks, cfg.dtype)
+    t_roof, bound = roofline.t_roof(flops, lbytes, ptc, peaks["hbm_gbs"])
+    step_s = ms_step / 1e3
+    gu_bytes = roofline.gateup_bytes(cfg, T, touched)
+    gu_s = k_avg["gemm_gateup"] / 1e3
+    dn_bytes = roofline.down_bytes(cfg, T, touched)
+    dn_s = k_avg["gemm_down"] / 1e3
+    gemm_roof, _ = roofline.t_roof(flops, gu_bytes + dn_bytes, ptc, peaks["hbm_gbs"])
+    achieved = gu_bytes / gu_s / 1e9 if gu_s > 0 else None
+    rec = recorded_traffic("gemm_tc.cu")
+    traffic = None
+    if args.traffic is not None:
+        traffic = args.traffic
+    elif rec and rec.get("workload") == cfg.name and rec.get("T") == T:
+        traffic = rec.get("dram_bytes_per_launch")
+    elif rec and rec.get("dram_bytes_per_touched_expert"):
+        # capture on a smaller case, scaled by the touched experts (traffic is weight-dominated)
+        traffic = rec["dram_bytes_per_touched_expert"] * (touched + cfg.S)
+
+    # end to end through the host-buffer entry point (pinned memory)
+    h_in = [x.cpu().pin_memory() for x in inputs[0]]
+    h_out = [torch.empty_like(x).pin_memory() for x in h_in]
+    for _ in range(max(2, args.warmup // 2)):
+        layer.forward_host(h_in, h_out, stream=stream)
+    e2e_steps = max(3, min(args.steps, 50))
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        layer.forward_host(h_in, h_out, stream=stream)
+    e2e_s = barrier_max(world, time.perf_counter() - t0) / e2e_steps
+    io_bytes = T * cfg.H * (4 if cfg.dtype == "fp32" else 2)
+
+    line = {
+        "metric": METRIC, "value": world * T / step_s, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": {"fp32": "f32", "bf16": "bf16", "fp8": "e4m3"}[cfg.dtype], "data": "synthetic",
+        "config": {"workload": f"{cfg.name} B={cfg.B} M={cfg.M} T={T}", "H": cfg.H, "I": cfg.I, "E": cfg.E,
+                   "k": cfg.k, "S": cfg.S, "n_micro": args.n_micro,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs > L2: expert weights streamed every step; 4 rotating input sets"},
+        "tflops": flops / step_s / 1e12,
+        "layer_roofline": {"t_roof_ms": t_roof * 1e3, "bound": bound, "frac": t_roof / step_s,
+                           "flops": flops, "bytes": lbytes, "touched_experts": touched,
+                           "peak_tflops": ptc, "peak_gbs": peaks["hbm_gbs"], "peaks": peak_src},
+        "gemm_roofline": {"t_roof_ms": gemm_roof * 1e3, "t_ms": (gu_s + dn_s) * 1e3,
+                          "frac": gemm_roof / (gu_s + dn_s) if gu_s + dn_s > 0 else None},
+        "roofline": {"kernel": "gemm_gateup", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"] if achieved else None,
+                     "traffic": traffic, "peak_src": peak_src},
+        "kernel_ms": k_avg,
+        "e2e": {"value": world * T / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": io_bytes,
+                "d2h_bytes_per_step": io_bytes, "api": "afd_ffn_forward_host"},
+        "gpu_launches": args.steps * layer.launches_per_forward * args.n_micro,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n = args.cpu_sample or default_sample_tokens(cfg)
+        dt, n, cores, *_ = oracle_sample(cfg, inputs[0], w, n)
+        line["cpu_baseline"] = {"value": n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": f"first {n} of {T} tokens, whole layer (routing + experts + combine)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    layer.close()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="qwen3_bf16", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--B", type=int, default=None)
+    ap.add_argument("--M", type=int, default=None)
+    ap.add_argument("--n-micro", type=int, default=None)
+    ap.add_argument("--E", type=int, default=None, help="override the expert count (small profiling cases)")
+    ap.add_argument("--cpu-sample", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu dram bytes per gate/up launch, when taken for the current kernel")
+    args = ap.parse_args()
+    base = synth.CONFIGS[args.config]
+    if args.E is not None:
+        import dataclasses
+
+        synth.CONFIGS[args.config] = base = dataclasses.replace(base, E=args.E, name=f"{base.name}_E{args.E}")
+    args.B = args.B if args.B is not None else base.B
+    args.M = args.M if args.M is not None else base.M
+    args.n_micro = args.n_micro if args.n_micro is not None else base.n_micro
+    args.warmup = max(args.warmup, 3)
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

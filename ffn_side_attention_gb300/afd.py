@@ -18,8 +18,12 @@ DTYPE_CODES = {"fp32": AFD_FP32, "bf16": AFD_BF16, "fp8": AFD_FP8_E4M3}
 AFD_OK, AFD_EINVAL, AFD_ECUDA, AFD_ECAPACITY, AFD_EUNSUPPORTED, AFD_EDEVICE = 0, -1, -2, -3, -4, -5
 AFD_MAX_SOURCES, AFD_MAX_MICRO = 64, 4
 
+AFD_NUM_KERNELS = 6
+KERNEL_NAMES = ["router", "routing", "pack", "gemm_gateup", "gemm_down", "combine"]
+
 EXPORTS = ["afd_ffn_create", "afd_ffn_create_error", "afd_ffn_forward", "afd_ffn_forward_pipelined",
            "afd_ffn_forward_host", "afd_ffn_debug_routing", "afd_ffn_check", "afd_ffn_last_error",
+           "afd_ffn_profile_begin", "afd_ffn_profile_end", "afd_ffn_launches_per_forward",
            "afd_ffn_device_bytes", "afd_ffn_destroy"]
 
 
@@ -66,6 +70,12 @@ def lib():
         L.afd_ffn_check.restype = ip
         L.afd_ffn_last_error.argtypes = [vp]
         L.afd_ffn_last_error.restype = C.c_char_p
+        L.afd_ffn_profile_begin.argtypes = [vp]
+        L.afd_ffn_profile_begin.restype = ip
+        L.afd_ffn_profile_end.argtypes = [vp, vp, vp]
+        L.afd_ffn_profile_end.restype = ip
+        L.afd_ffn_launches_per_forward.argtypes = [vp]
+        L.afd_ffn_launches_per_forward.restype = ip
         L.afd_ffn_device_bytes.argtypes = [vp]
         L.afd_ffn_device_bytes.restype = C.c_size_t
         L.afd_ffn_destroy.argtypes = [vp]
@@ -124,6 +134,22 @@ def afd_ffn_check(h, stream):
 
 def afd_ffn_last_error(h) -> str:
     return (lib().afd_ffn_last_error(h) or b"").decode()
+
+
+def afd_ffn_profile_begin(h):
+    return _check(lib().afd_ffn_profile_begin(h), h)
+
+
+def afd_ffn_profile_end(h):
+    """-> (list of summed ms per kernel, number of recorded forwards)"""
+    ms = (C.c_double * AFD_NUM_KERNELS)()
+    n = C.c_int(0)
+    _check(lib().afd_ffn_profile_end(h, ms, C.byref(n)), h)
+    return list(ms), n.value
+
+
+def afd_ffn_launches_per_forward(h) -> int:
+    return int(lib().afd_ffn_launches_per_forward(h))
 
 
 def afd_ffn_device_bytes(h) -> int:
@@ -214,6 +240,18 @@ class MoELayer:
 
     def check(self, stream=None):
         return afd_ffn_check(self.handle, self._stream(stream))
+
+    def profile_begin(self):
+        afd_ffn_profile_begin(self.handle)
+
+    def profile_end(self):
+        """-> (dict kernel name -> summed ms, number of recorded forwards)"""
+        ms, n = afd_ffn_profile_end(self.handle)
+        return dict(zip(KERNEL_NAMES, ms)), n
+
+    @property
+    def launches_per_forward(self):
+        return afd_ffn_launches_per_forward(self.handle)
 
     @property
     def device_bytes(self):

@@ -13,6 +13,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "afd_internal.cuh"
 
@@ -44,6 +45,10 @@ struct afd_ffn {
   cudaStream_t mstream[AFD_MAX_MICRO] = {};
   cudaEvent_t ev_fork = nullptr;
   cudaEvent_t ev_join[AFD_MAX_MICRO] = {};
+  // per-kernel timing: AFD_NUM_KERNELS + 1 events per recorded forward
+  bool prof_on = false;
+  std::vector<cudaEvent_t> prof_events;
+  size_t prof_used = 0;
   std::string err;
 };
 
@@ -211,23 +216,46 @@ SrcTable make_table(const void* const* src, const int* counts, int M, void* cons
   return st;
 }
 
+// Profiling: record the i-th event of the current forward (i = 0 before the
+// first kernel, i = n after kernel n).
+int prof_mark(afd_ffn* h, int i, cudaStream_t s) {
+  if (!h->prof_on) return AFD_OK;
+  if (i == 0 && h->prof_used + AFD_NUM_KERNELS + 1 > h->prof_events.size()) {
+    for (int q = 0; q <= AFD_NUM_KERNELS; ++q) {
+      cudaEvent_t e;
+      CUDA_TRY(h, cudaEventCreate(&e));
+      h->prof_events.push_back(e);
+    }
+  }
+  CUDA_TRY(h, cudaEventRecord(h->prof_events[h->prof_used + i], s));
+  if (i == AFD_NUM_KERNELS) h->prof_used += AFD_NUM_KERNELS + 1;
+  return AFD_OK;
+}
+
 // The launch sequence of one forward on one workspace.
 int run_layer(afd_ffn* h, const SrcTable& st, Workspace& ws, cudaStream_t s) {
   const LayerDims& d = h->dims;
   const int T = st.T;
   ws.last_T = T;
   if (T == 0) return AFD_OK;
+  int rc;
+  afd::TcWeights w{&h->tm_wg, &h->tm_wu, &h->tm_wd, h->sgT, h->suT, h->sdT};
+  if ((rc = prof_mark(h, 0, s))) return rc;
   CUDA_TRY(h, afd::launch_router(st, h->wrT, h->bias, d, ws, s));
+  if ((rc = prof_mark(h, 1, s))) return rc;
   CUDA_TRY(h, afd::launch_routing(d, T, ws, s));
+  if ((rc = prof_mark(h, 2, s))) return rc;
   CUDA_TRY(h, afd::launch_pack(st, d, T, ws, h->num_sms, s));
-  if (d.dtype == AFD_FP32) {
-    CUDA_TRY(h, afd::launch_gemm_simt(d, T, h->wg32, h->wu32, h->wd32, ws, s));
-  } else {
-    afd::TcWeights w{&h->tm_wg, &h->tm_wu, &h->tm_wd, h->sgT, h->suT, h->sdT};
-    CUDA_TRY(h, afd::launch_gemm_tc(d, T, w, ws, h->num_sms, s));
+  if ((rc = prof_mark(h, 3, s))) return rc;
+  for (int which = 0; which < 2; ++which) {
+    if (d.dtype == AFD_FP32)
+      CUDA_TRY(h, afd::launch_gemm_simt(d, T, h->wg32, h->wu32, h->wd32, ws, s, which));
+    else
+      CUDA_TRY(h, afd::launch_gemm_tc(d, T, w, ws, h->num_sms, s, which));
+    if ((rc = prof_mark(h, 4 + which, s))) return rc;
   }
   CUDA_TRY(h, afd::launch_combine(st, d, T, ws, h->num_sms, s));
-  return AFD_OK;
+  return prof_mark(h, 6, s);
 }
 
 int create_impl(const afd_ffn_config* cfg, const afd_ffn_weights* w, afd_ffn* h) {
@@ -465,6 +493,33 @@ int afd_ffn_check(afd_ffn_t h, void* stream) {
   return AFD_OK;
 }
 
+int afd_ffn_profile_begin(afd_ffn_t h) {
+  if (!h) return AFD_EINVAL;
+  h->prof_on = true;
+  h->prof_used = 0;
+  return AFD_OK;
+}
+
+int afd_ffn_profile_end(afd_ffn_t h, double* ms_per_kernel, int* n_forwards) {
+  if (!h || !ms_per_kernel) return AFD_EINVAL;
+  CUDA_TRY(h, cudaDeviceSynchronize());
+  for (int q = 0; q < AFD_NUM_KERNELS; ++q) ms_per_kernel[q] = 0.0;
+  const size_t nf = h->prof_used / (AFD_NUM_KERNELS + 1);
+  for (size_t f = 0; f < nf; ++f)
+    for (int q = 0; q < AFD_NUM_KERNELS; ++q) {
+      float ms = 0.f;
+      CUDA_TRY(h, cudaEventElapsedTime(&ms, h->prof_events[f * (AFD_NUM_KERNELS + 1) + q],
+                                       h->prof_events[f * (AFD_NUM_KERNELS + 1) + q + 1]));
+      ms_per_kernel[q] += ms;
+    }
+  if (n_forwards) *n_forwards = (int)nf;
+  h->prof_on = false;
+  h->prof_used = 0;
+  return AFD_OK;
+}
+
+int afd_ffn_launches_per_forward(afd_ffn_t h) { return h ? AFD_NUM_KERNELS : AFD_EINVAL; }
+
 const char* afd_ffn_last_error(afd_ffn_t h) { return h ? h->err.c_str() : "handle is NULL"; }
 
 size_t afd_ffn_device_bytes(afd_ffn_t h) { return h ? h->bytes : 0; }
@@ -481,6 +536,7 @@ void afd_ffn_destroy(afd_ffn_t h) {
   for (auto e : h->ev_join)
     if (e) cudaEventDestroy(e);
   if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  for (auto e : h->prof_events) cudaEventDestroy(e);
   delete h;
 }
 

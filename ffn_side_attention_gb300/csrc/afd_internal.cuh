@@ -80,7 +80,7 @@ cudaError_t launch_pack(const SrcTable& st, const LayerDims& d, int T, Workspace
 cudaError_t launch_combine(const SrcTable& st, const LayerDims& d, int T, Workspace& ws, int num_sms,
                            cudaStream_t s);
 cudaError_t launch_gemm_simt(const LayerDims& d, int T, const float* wg, const float* wu, const float* wd,
-                             Workspace& ws, cudaStream_t s);
+                             Workspace& ws, cudaStream_t s, int which);  // which: 0 gate/up, 1 down
 
 struct TcWeights {
   const CUtensorMap* tm_wg;  // [(E+S)*I, H] K-major
@@ -91,7 +91,7 @@ struct TcWeights {
   const float* sd;           // fp8: [(E+S), H/128, I/128]
 };
 cudaError_t launch_gemm_tc(const LayerDims& d, int T, const TcWeights& w, Workspace& ws, int num_sms,
-                           cudaStream_t s);
+                           cudaStream_t s, int which);  // which: 0 gate/up + SwiGLU, 1 down
 cudaError_t gemm_tc_setup();  // opt-in shared memory sizes (once per process)
 
 cudaError_t launch_transpose(const void* src, void* dst, int batch, int rows, int cols, int elem_bytes,

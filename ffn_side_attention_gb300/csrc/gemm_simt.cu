@@ -77,14 +77,15 @@ __global__ void transpose_kernel(const Elem* __restrict__ src, Elem* __restrict_
 }  // namespace
 
 cudaError_t launch_gemm_simt(const LayerDims& d, int T, const float* wg, const float* wu, const float* wd,
-                             Workspace& ws, cudaStream_t s) {
+                             Workspace& ws, cudaStream_t s, int which) {
   const int rows = T * (d.k + d.S);
   if (rows == 0) return cudaSuccess;
   const int G = d.E + d.S;
-  simt_gateup_kernel<<<dim3(rows, (d.I + 127) / 128), 128, 0, s>>>(static_cast<const float*>(ws.P), ws.offsets, G,
-                                                                   d.H, d.I, wg, wu, static_cast<float*>(ws.Hb));
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (which == 0) {
+    simt_gateup_kernel<<<dim3(rows, (d.I + 127) / 128), 128, 0, s>>>(static_cast<const float*>(ws.P), ws.offsets,
+                                                                     G, d.H, d.I, wg, wu, static_cast<float*>(ws.Hb));
+    return cudaGetLastError();
+  }
   simt_down_kernel<<<dim3(rows, (d.H + 127) / 128), 128, 0, s>>>(static_cast<const float*>(ws.Hb), ws.offsets, G,
                                                                  d.H, d.I, wd, static_cast<float*>(ws.Y));
   return cudaGetLastError();

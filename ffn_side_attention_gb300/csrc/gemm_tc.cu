@@ -284,7 +284,7 @@ cudaError_t gemm_tc_setup() {
 }
 
 cudaError_t launch_gemm_tc(const LayerDims& d, int T, const TcWeights& w, Workspace& ws, int num_sms,
-                           cudaStream_t s) {
+                           cudaStream_t s, int which) {
   if (T == 0) return cudaSuccess;
   if (d.dtype != AFD_BF16) return cudaErrorNotSupported;
   const int G = d.E + d.S;
@@ -298,6 +298,7 @@ cudaError_t launch_gemm_tc(const LayerDims& d, int T, const TcWeights& w, Worksp
   a.G = G;
   a.err = ws.err;
 
+  if (which == 0) {
   // gate/up + SwiGLU: K = H, items of 128 intermediate channels
   a.num_kb = d.H / 64;
   a.MT = d.I / kGemmBM;
@@ -307,11 +308,11 @@ cudaError_t launch_gemm_tc(const LayerDims& d, int T, const TcWeights& w, Worksp
   a.out = static_cast<uint16_t*>(ws.Hb);
   a.ld_out = d.I;
   a.mode = 0;
-  long items_ub = tiles_ub * a.MT;
-  int grid = (int)(items_ub < num_sms ? items_ub : num_sms);
+  const long items_ub = tiles_ub * a.MT;
+  const int grid = (int)(items_ub < num_sms ? items_ub : num_sms);
   gemm_bf16_kernel<<<grid, kThreads, kDynSmem, s>>>(*w.tm_wg, *w.tm_wu, ws.tm_P, a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+  }
 
   // down: K = I, items of 256 output columns (two 128-row MMAs)
   a.num_kb = d.I / 64;
@@ -322,9 +323,9 @@ cudaError_t launch_gemm_tc(const LayerDims& d, int T, const TcWeights& w, Worksp
   a.out = static_cast<uint16_t*>(ws.Y);
   a.ld_out = d.H;
   a.mode = 1;
-  items_ub = tiles_ub * a.MT;
-  grid = (int)(items_ub < num_sms ? items_ub : num_sms);
-  gemm_bf16_kernel<<<grid, kThreads, kDynSmem, s>>>(*w.tm_wd, *w.tm_wd, ws.tm_H, a);
+  const long items_ub2 = tiles_ub * a.MT;
+  const int grid2 = (int)(items_ub2 < num_sms ? items_ub2 : num_sms);
+  gemm_bf16_kernel<<<grid2, kThreads, kDynSmem, s>>>(*w.tm_wd, *w.tm_wd, ws.tm_H, a);
   return cudaGetLastError();
 }
 

@@ -180,8 +180,3 @@ def to_numpy_bits(t: torch.Tensor):
 def weights_numpy(w: dict) -> dict:
     return {k: to_numpy_bits(v) for k, v in w.items()}
 
-
-def flops(cfg: LayerConfig, T: int) -> int:
-    """Expert-FFN floating-point operations: 2 per multiply-add, three H x I
-    matrices per (token, expert) pair, k routed experts plus S shared."""
-    return 6 * T * (cfg.k + cfg.S) * cfg.H * cfg.I

@@ -167,6 +167,20 @@ int afd_ffn_check(afd_ffn_t h, void* stream);
 /* Last error text of the handle ("" if none). */
 const char* afd_ffn_last_error(afd_ffn_t h);
 
+/* Per-kernel timing (benchmark aid).  afd_ffn_profile_begin() makes every
+ * following forward record CUDA events on its stream around each of its
+ * AFD_NUM_KERNELS kernels (router, routing tables, pack, gate/up GEMM, down
+ * GEMM, combine).  afd_ffn_profile_end() synchronises the device, writes the
+ * summed milliseconds per kernel over the recorded forwards into
+ * ms_per_kernel[AFD_NUM_KERNELS] and their number into *n_forwards, and turns
+ * recording off.  Recording adds one event per kernel launch. */
+#define AFD_NUM_KERNELS 6
+int afd_ffn_profile_begin(afd_ffn_t h);
+int afd_ffn_profile_end(afd_ffn_t h, double* ms_per_kernel, int* n_forwards);
+
+/* Number of kernel launches one afd_ffn_forward of T > 0 tokens enqueues. */
+int afd_ffn_launches_per_forward(afd_ffn_t h);
+
 /* Bytes of device memory the handle holds (weights + workspaces). */
 size_t afd_ffn_device_bytes(afd_ffn_t h);
 
