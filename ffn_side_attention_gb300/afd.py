@@ -24,7 +24,7 @@ KERNEL_NAMES = ["router", "routing", "pack", "gemm_gateup", "gemm_down", "combin
 EXPORTS = ["afd_ffn_create", "afd_ffn_create_error", "afd_ffn_forward", "afd_ffn_forward_pipelined",
            "afd_ffn_forward_host", "afd_ffn_debug_routing", "afd_ffn_check", "afd_ffn_last_error",
            "afd_ffn_profile_begin", "afd_ffn_profile_end", "afd_ffn_launches_per_forward",
-           "afd_ffn_device_bytes", "afd_ffn_destroy"]
+           "afd_ffn_device_bytes", "afd_ffn_router_noalloc", "afd_ffn_destroy"]
 
 
 class AfdConfig(C.Structure):
@@ -78,6 +78,8 @@ def lib():
         L.afd_ffn_launches_per_forward.restype = ip
         L.afd_ffn_device_bytes.argtypes = [vp]
         L.afd_ffn_device_bytes.restype = C.c_size_t
+        L.afd_ffn_router_noalloc.argtypes = [vp, vp, vp, ip, ip, ip, ip, ip, vp, vp, vp, vp]
+        L.afd_ffn_router_noalloc.restype = ip
         L.afd_ffn_destroy.argtypes = [vp]
         L.afd_ffn_destroy.restype = None
         _lib = L
@@ -154,6 +156,15 @@ def afd_ffn_launches_per_forward(h) -> int:
 
 def afd_ffn_device_bytes(h) -> int:
     return int(lib().afd_ffn_device_bytes(h))
+
+
+def afd_ffn_router_noalloc(stream, src_ptrs, src_counts, H, E, k, dtype, w_router, router_bias, topk_idx,
+                           topk_w) -> int:
+    """Routing (top-k indices and weights) with no device allocation; returns
+    the status code (0 = ok).  Pointers are device addresses (ints)."""
+    return int(lib().afd_ffn_router_noalloc(stream, _ptr_array(src_ptrs), _int_array(src_counts), len(src_counts),
+                                            H, E, k, DTYPE_CODES[dtype] if isinstance(dtype, str) else dtype,
+                                            w_router, router_bias, topk_idx, topk_w))
 
 
 def afd_ffn_destroy(h):

@@ -184,6 +184,35 @@ int afd_ffn_launches_per_forward(afd_ffn_t h);
 /* Bytes of device memory the handle holds (weights + workspaces). */
 size_t afd_ffn_device_bytes(afd_ffn_t h);
 
+/* Router top-k with no device allocation (the pages have no counterpart:
+ * this serves callers that cannot allocate).  A caller that has handed all
+ * of its device memory to its own pool (e.g. an attention-side server that
+ * reserves HBM for its KV cache) cannot cudaMalloc, and one inside a
+ * latency-critical decode loop must not make an allocation call, which can
+ * block or synchronise the device.  This computes exactly the routing of
+ * afd_ffn_forward (same logits bit for bit, same top-k slots, same weights)
+ * without a handle and without allocating.
+ *   src_ptrs_dev[m], src_counts_host[m], M  as afd_ffn_forward (16-byte
+ *                    aligned rows of H activations, fp32 for AFD_FP32, bf16
+ *                    for AFD_BF16 and AFD_FP8_E4M3)
+ *   w_router_dev     [H, E] router weights in the same dtype, row-major,
+ *                    16-byte aligned; router_bias_dev [E] fp32 or NULL
+ *   topk_idx_dev     [T, k] int32 output; topk_w_dev [T, k] fp32 output
+ * Limits: T <= 4096 tokens, E <= 256 with E % 8 == 0, k <= 16, H % 8 == 0,
+ * M <= AFD_MAX_SOURCES.  Sizes beyond a limit return AFD_ECAPACITY; bad
+ * pointers or shapes return AFD_EINVAL; a failed CUDA call AFD_ECUDA.
+ * Scratch: one file-scope device array of 4 MiB + 1 KiB (logits and
+ * completion tickets), held by every GPU that loads the library until the
+ * process exits.  The first call on a device (with it current) looks up the
+ * array's address with cudaGetSymbolAddress; make that first call before any
+ * stream capture begins.  All calls share the array: calls whose work
+ * overlaps on the GPU race and must be serialised by the caller.  Each call
+ * clears the tickets with cudaMemsetAsync on `stream`, then launches one
+ * kernel; nothing is allocated or freed. */
+int afd_ffn_router_noalloc(void* stream, const void* const* src_ptrs_dev, const int* src_counts_host, int M,
+                           int H, int E, int k, afd_dtype dtype, const void* w_router_dev,
+                           const float* router_bias_dev, int* topk_idx_dev, float* topk_w_dev);
+
 /* Free everything the handle owns.  Synchronises the device first.
  * NULL is a no-op. */
 void afd_ffn_destroy(afd_ffn_t h);
