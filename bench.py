@@ -276,40 +276,63 @@ def run_ours(args, world, rank, local):
     layer.check()
     ms_step = elapsed / max(args.steps, 1) * 1e3
 
-    # per-kernel times (separate instrumented pass, same workload)
+
+    # routing statistics of input set 0 (touched experts), per micro-batch:
+    # each micro-batch is its own forward and streams its own experts' weights
+    ptc = tc_peak(peaks, cfg.dtype)
+    n_mb = max(args.n_micro, 1)
+    q, rem = divmod(T, n_mb)
+    sizes = [q + (1 if i < rem else 0) for i in range(n_mb)]
+    xall = torch.cat(inputs[0])
+    flops = lbytes = t_roof = 0.0
+    touched_list = []
+    bound = "hbm"
+    t0_ = 0
+    for sz in sizes:
+        sub = [xall[t0_:t0_ + sz]]
+        layer.forward(sub, [torch.empty_like(sub[0])], stream=stream)
+        r = layer.routing(sz)
+        tch = int((r["counts"].cpu() > 0).sum().item())
+        touched_list.append(tch)
+        f_i = roofline.layer_flops(cfg, sz)
+        b_i = roofline.layer_bytes(cfg, sz, tch)
+        tr_i, bound = roofline.t_roof(f_i, b_i, ptc, peaks["hbm_gbs"])
+        flops += f_i
+        lbytes += b_i
+        t_roof += tr_i
+        t0_ += sz
+    touched = touched_list[0] if n_mb == 1 else touched_list
+
+    # per-kernel times (separate instrumented pass on one stream; with micro-
+    # batches, the first micro-batch run alone, so each kernel is timed unshared)
     n_prof = min(args.steps, 50)
+    prof_in = [xall[:sizes[0]]]
+    prof_out = [torch.empty_like(prof_in[0])]
     layer.profile_begin()
     for i in range(n_prof):
-        step(i)
+        if n_mb == 1:
+            step(i)
+        else:
+            layer.forward(prof_in, prof_out, stream=stream)
     kms, nf = layer.profile_end()
     k_avg = {k: v / max(nf, 1) for k, v in kms.items()}
-
-    # routing statistics of input set 0 (touched experts)
-    layer.forward(inputs[0], outs[0], stream=stream)
-    r = layer.routing(T)
-    counts = r["counts"].cpu()
-    touched = int((counts > 0).sum().item())
-
-    flops = roofline.layer_flops(cfg, T)
-    lbytes = roofline.layer_bytes(cfg, T, touched)
-    ptc = tc_peak(peaks, cfg.dtype)
-    t_roof, bound = roofline.t_roof(flops, lbytes, ptc, peaks["hbm_gbs"])
     step_s = ms_step / 1e3
-    gu_bytes = roofline.gateup_bytes(cfg, T, touched)
+    gu_bytes = roofline.gateup_bytes(cfg, sizes[0], touched_list[0])  # the profiled launch
     gu_s = k_avg["gemm_gateup"] / 1e3
-    dn_bytes = roofline.down_bytes(cfg, T, touched)
+    dn_bytes = roofline.down_bytes(cfg, sizes[0], touched_list[0])
     dn_s = k_avg["gemm_down"] / 1e3
-    gemm_roof, _ = roofline.t_roof(flops, gu_bytes + dn_bytes, ptc, peaks["hbm_gbs"])
+    gemm_roof, _ = roofline.t_roof(roofline.layer_flops(cfg, sizes[0]), gu_bytes + dn_bytes, ptc,
+                                   peaks["hbm_gbs"])
     achieved = gu_bytes / gu_s / 1e9 if gu_s > 0 else None
     rec = recorded_traffic("gemm_tc.cu")
     traffic = None
     if args.traffic is not None:
         traffic = args.traffic
-    elif rec and rec.get("workload") == cfg.name and rec.get("T") == T:
+    elif rec and rec.get("workload") == cfg.name and rec.get("T") == sizes[0]:
         traffic = rec.get("dram_bytes_per_launch")
     elif rec and rec.get("dram_bytes_per_touched_expert"):
         # capture on a smaller case, scaled by the touched experts (traffic is weight-dominated)
-        traffic = rec["dram_bytes_per_touched_expert"] * (touched + cfg.S)
+        traffic = rec["dram_bytes_per_touched_expert"] * (touched_list[0] + cfg.S)
 
     # end to end through the host-buffer entry point (pinned memory)
     h_in = [x.cpu().pin_memory() for x in inputs[0]]
@@ -369,16 +392,19 @@ def main():
     ap.add_argument("--M", type=int, default=None)
     ap.add_argument("--n-micro", type=int, default=None)
     ap.add_argument("--E", type=int, default=None, help="override the expert count (small profiling cases)")
+    ap.add_argument("--I", type=int, default=None, help="override the expert intermediate size (profiling cases)")
     ap.add_argument("--cpu-sample", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per gate/up launch, when taken for the current kernel")
     args = ap.parse_args()
     base = synth.CONFIGS[args.config]
-    if args.E is not None:
+    if args.E is not None or args.I is not None:
         import dataclasses
 
-        synth.CONFIGS[args.config] = base = dataclasses.replace(base, E=args.E, name=f"{base.name}_E{args.E}")
+        E = args.E if args.E is not None else base.E
+        I = args.I if args.I is not None else base.I
+        synth.CONFIGS[args.config] = base = dataclasses.replace(base, E=E, I=I, name=f"{base.name}_E{E}_I{I}")
     args.B = args.B if args.B is not None else base.B
     args.M = args.M if args.M is not None else base.M
     args.n_micro = args.n_micro if args.n_micro is not None else base.n_micro

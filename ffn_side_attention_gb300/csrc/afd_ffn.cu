@@ -250,6 +250,8 @@ int run_layer(afd_ffn* h, const SrcTable& st, Workspace& ws, cudaStream_t s) {
   for (int which = 0; which < 2; ++which) {
     if (d.dtype == AFD_FP32)
       CUDA_TRY(h, afd::launch_gemm_simt(d, T, h->wg32, h->wu32, h->wd32, ws, s, which));
+    else if (d.dtype == AFD_FP8_E4M3)
+      CUDA_TRY(h, afd::launch_gemm_fp8(d, T, w, ws, h->num_sms, s, which));
     else
       CUDA_TRY(h, afd::launch_gemm_tc(d, T, w, ws, h->num_sms, s, which));
     if ((rc = prof_mark(h, 4 + which, s))) return rc;
@@ -265,6 +267,7 @@ int create_impl(const afd_ffn_config* cfg, const afd_ffn_weights* w, afd_ffn* h)
   h->max_rows = (size_t)c.max_tokens * (c.k + c.n_shared);
   CUDA_TRY(h, cudaGetDevice(&h->device));
   CUDA_TRY(h, cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device));
+  CUDA_TRY(h, afd::router_setup());
   if (c.dtype != AFD_FP32) {
     int major = 0, minor = 0;
     CUDA_TRY(h, cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, h->device));
@@ -273,8 +276,8 @@ int create_impl(const afd_ffn_config* cfg, const afd_ffn_weights* w, afd_ffn* h)
       return fail(h, AFD_EUNSUPPORTED, "tensor-core path is built for sm_103a; device is sm_%d%d", major, minor);
     if (!get_encoder()) return fail(h, AFD_ECUDA, "cuTensorMapEncodeTiled entry point unavailable");
     CUDA_TRY(h, afd::gemm_tc_setup());
+    CUDA_TRY(h, afd::gemm_fp8_setup());
   }
-  if (c.dtype == AFD_FP8_E4M3) return fail(h, AFD_EUNSUPPORTED, "fp8 expert GEMMs are not built yet");
 
   const size_t H = c.H, I = c.I, E = c.E, S = c.n_shared, G = E + S;
   const size_t ab = act_bytes(c), wb = wt_bytes(c);
@@ -317,6 +320,21 @@ int create_impl(const afd_ffn_config* cfg, const afd_ffn_weights* w, afd_ffn* h)
       CUDA_TRY(h, afd::launch_transpose(w->sh_down, d8 + E * H * I * wb, 1, (int)I, (int)H, (int)wb, s));
     }
     const bool fp8 = c.dtype == AFD_FP8_E4M3;
+    if (fp8) {
+      // block scales, m-block major: gate/up [(E+S)][I/128][H/128], down [(E+S)][H/128][I/128]
+      const size_t hb = H / 128, ib = I / 128;
+      if ((rc = dmalloc_t(h, &h->sgT, G * ib * hb)) || (rc = dmalloc_t(h, &h->suT, G * ib * hb)) ||
+          (rc = dmalloc_t(h, &h->sdT, G * hb * ib)))
+        return rc;
+      CUDA_TRY(h, afd::launch_transpose_f32(w->s_gate, h->sgT, (int)E, (int)hb, (int)ib, s));
+      CUDA_TRY(h, afd::launch_transpose_f32(w->s_up, h->suT, (int)E, (int)hb, (int)ib, s));
+      CUDA_TRY(h, afd::launch_transpose_f32(w->s_down, h->sdT, (int)E, (int)ib, (int)hb, s));
+      if (S) {
+        CUDA_TRY(h, afd::launch_transpose_f32(w->sh_s_gate, h->sgT + E * ib * hb, 1, (int)hb, (int)ib, s));
+        CUDA_TRY(h, afd::launch_transpose_f32(w->sh_s_up, h->suT + E * ib * hb, 1, (int)hb, (int)ib, s));
+        CUDA_TRY(h, afd::launch_transpose_f32(w->sh_s_down, h->sdT + E * hb * ib, 1, (int)ib, (int)hb, s));
+      }
+    }
     if (!make_map(&h->tm_wg, h->wgT, fp8, H, G * I, 128) || !make_map(&h->tm_wu, h->wuT, fp8, H, G * I, 128) ||
         !make_map(&h->tm_wd, h->wdT, fp8, I, G * H, 128))
       return fail(h, AFD_ECUDA, "cuTensorMapEncodeTiled failed for a weight operand");

@@ -13,10 +13,10 @@ namespace afd {
 
 // ---------------------------------------------------------------- constants
 constexpr int kWarp = 32;
-constexpr int kRouterTokTile = 16;  // tokens per router CTA
-constexpr int kRouterExpTile = 32;  // experts per router CTA
+constexpr int kRouterTokTile = 32;  // tokens per router CTA
 constexpr int kGemmBN = 256;        // max tokens per GEMM tile (MMA N)
 constexpr int kGemmBM = 128;        // weight rows per MMA (MMA M)
+constexpr int kGemmBNFp8 = 128;     // max tokens per fp8 GEMM tile
 constexpr int kMaxExperts = 257;    // routed + shared
 
 // device error word bits
@@ -74,6 +74,7 @@ struct LayerDims {
 
 cudaError_t launch_router(const SrcTable& st, const void* wrT, const float* bias, const LayerDims& d,
                           Workspace& ws, cudaStream_t s);
+cudaError_t router_setup();  // opt-in shared memory sizes (once per process)
 cudaError_t launch_routing(const LayerDims& d, int T, Workspace& ws, cudaStream_t s);
 cudaError_t launch_pack(const SrcTable& st, const LayerDims& d, int T, Workspace& ws, int num_sms,
                         cudaStream_t s);
@@ -93,6 +94,9 @@ struct TcWeights {
 cudaError_t launch_gemm_tc(const LayerDims& d, int T, const TcWeights& w, Workspace& ws, int num_sms,
                            cudaStream_t s, int which);  // which: 0 gate/up + SwiGLU, 1 down
 cudaError_t gemm_tc_setup();  // opt-in shared memory sizes (once per process)
+cudaError_t launch_gemm_fp8(const LayerDims& d, int T, const TcWeights& w, Workspace& ws, int num_sms,
+                            cudaStream_t s, int which);  // fp8 layer: 0 gate/up + SwiGLU + e4m3 h, 1 down
+cudaError_t gemm_fp8_setup();
 
 cudaError_t launch_transpose(const void* src, void* dst, int batch, int rows, int cols, int elem_bytes,
                              cudaStream_t s);
@@ -139,25 +143,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of `bar`, giving up after `limit_ns` or as soon as
-// another thread of the CTA raised `*abort`.  On a timeout the CTA abort flag
-// and the kTimeout bit of the device error word are set.  Returns false when
-// the caller must abandon its work.
+// Wait for phase `parity` of `bar`, giving up after about `limit_cycles` SM
+// clocks (~2 s at GB300 clocks) or as soon as another thread of the CTA raised
+// `*abort`.  The clock and the abort flag are read once every 256 failed
+// polls, so a wait that succeeds quickly costs nothing extra.  On a timeout
+// the CTA abort flag and the kErrTimeout bit of the device error word are set.
+// Returns false when the caller must abandon its work.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err,
-                                          uint64_t limit_ns = 2000000000ull) {
+                                          long long limit_cycles = 4000000000ll) {
   if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = global_timer_ns();
+  const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63) == 0) {
+    if ((it & 255u) == 0) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > limit_ns) {
+      if (clock64() - t0 > limit_cycles) {
         *abort = 1;
         atomicOr(err, kErrTimeout);
         return false;
       }
     }
   }
+}
+
+// Bounded wait without the abort flag (drains in-flight copies and MMAs).
+__device__ __forceinline__ bool mbar_wait_cycles(uint64_t* bar, uint32_t parity, long long limit_cycles) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > limit_cycles) return false;
+  return true;
 }
 
 // --- TMA (tiled, 2D) global -> shared, completion on an mbarrier

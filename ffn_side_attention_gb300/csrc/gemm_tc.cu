@@ -45,7 +45,7 @@ constexpr int kStageBytes = 2 * kATile + kBTile;  // 64 KB
 constexpr int kDynSmem = kStages * kStageBytes + 1024;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint64_t kDrainLimitNs = 200000000ull;
+constexpr long long kDrainCycles = 400000000ll;  // ~0.2 s
 
 struct TcArgs {
   const int32_t* counts;
@@ -85,12 +85,6 @@ __device__ __forceinline__ Item decode_item(int item, int MT, int G, const int* 
   return it;
 }
 
-__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
-  uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (global_timer_ns() - t0 > limit_ns) return false;
-  return true;
-}
 
 __device__ __forceinline__ uint16_t f2bf(float v) {
   __nv_bfloat16 b = __float2bfloat16_rn(v);
@@ -181,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok)  // let the copies already issued land before the CTA exits
         for (int q = 0; q < kStages; ++q)
-          if ((filled >> q) & 1u) mbar_wait_limit(&full[q], (fill_ph >> q) & 1u, kDrainLimitNs);
+          if ((filled >> q) & 1u) mbar_wait_cycles(&full[q], (fill_ph >> q) & 1u, kDrainCycles);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -222,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(tfull);
       }
       tc_commit(drain);  // all MMAs issued above complete before TMEM is freed
-      mbar_wait_limit(drain, 0, kDrainLimitNs);
+      mbar_wait_cycles(drain, 0, kDrainCycles);
     }
   } else {
     // ---------------- epilogue: warps 2..5

@@ -14,7 +14,7 @@
 // shared expert's row), accumulated in fp32 and rounded once; written to the
 // token's own output buffer.  No atomics: the result is run-to-run identical.
 //
-// Both are HBM/L2-bound row copies: one warp per row, 16-byte vector accesses.
+// Both are HBM-bound row moves: one warp per token, 16-byte vector accesses.
 #include "afd_internal.cuh"
 
 namespace afd {
@@ -30,56 +30,73 @@ __device__ __forceinline__ uint8_t* out_row(const SrcTable& st, int t, size_t ro
   return reinterpret_cast<uint8_t*>(st.out[m]) + (size_t)(t - st.row0[m]) * row_bytes;
 }
 
-// row copy (bf16 or fp32 layers): P[row] = x[perm[row]]
-__global__ void __launch_bounds__(256) pack_copy_kernel(SrcTable st, const int32_t* __restrict__ perm, int rows,
-                                                        int row_bytes, uint8_t* __restrict__ P) {
-  const int lane = threadIdx.x & 31;
-  const int nvec = row_bytes >> 4;
-  for (int row = blockIdx.x * 8 + (threadIdx.x >> 5); row < rows; row += gridDim.x * 8) {
-    int t = __ldg(perm + row);
-    const uint4* s = reinterpret_cast<const uint4*>(src_row(st, t, row_bytes));
-    uint4* d = reinterpret_cast<uint4*>(P + (size_t)row * row_bytes);
-    for (int v = lane; v < nvec; v += 32) d[v] = __ldg(s + v);
-  }
-}
-
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
 
-// fp8 layer: P[row] = e4m3 codes of x[perm[row]], P_scale[row][b] per 128 channels.
-// A 128-channel block is 16 lanes x 8 channels; one 16-byte load per lane.
-__global__ void __launch_bounds__(256) pack_fp8_kernel(SrcTable st, const int32_t* __restrict__ perm, int rows,
-                                                       int H, uint8_t* __restrict__ P, float* __restrict__ P_scale) {
+// Packed rows of token t: its k routed copies (pos[t*k + j]) and, with a
+// shared expert, row T*k + t.  One warp per token: each source row is read
+// once (and quantised once) and stored to all of its packed rows.
+constexpr int kMaxCopies = 17;  // k <= 16, plus the shared expert
+
+__device__ __forceinline__ int packed_rows(const int32_t* __restrict__ pos, int t, int T, int k, int S, int* rows) {
+  int n = 0;
+  for (int j = 0; j < k; ++j) rows[n++] = __ldg(pos + (size_t)t * k + j);
+  if (S) rows[n++] = T * k + t;
+  return n;
+}
+
+// bf16 / fp32 layers: row copy, 16 bytes per lane step.
+__global__ void __launch_bounds__(256) pack_copy_kernel(SrcTable st, const int32_t* __restrict__ pos, int T, int k,
+                                                        int S, int row_bytes, uint8_t* __restrict__ P) {
+  const int lane = threadIdx.x & 31;
+  const int nvec = row_bytes >> 4;
+  for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < T; t += gridDim.x * 8) {
+    int rows[kMaxCopies];
+    const int n = packed_rows(pos, t, T, k, S, rows);
+    const uint4* s = reinterpret_cast<const uint4*>(src_row(st, t, row_bytes));
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 u = __ldg(s + v);
+      for (int c = 0; c < n; ++c) reinterpret_cast<uint4*>(P + (size_t)rows[c] * row_bytes)[v] = u;
+    }
+  }
+}
+
+// fp8 layer: e4m3 codes + one fp32 scale per 128 channels, computed once per
+// token.  A 128-channel block is 16 lanes x 8 channels (one 16-byte load each).
+__global__ void __launch_bounds__(256) pack_fp8_kernel(SrcTable st, const int32_t* __restrict__ pos, int T, int k,
+                                                       int S, int H, uint8_t* __restrict__ P,
+                                                       float* __restrict__ P_scale) {
   const int lane = threadIdx.x & 31;
   const int nblk = H >> 7;
-  for (int row = blockIdx.x * 8 + (threadIdx.x >> 5); row < rows; row += gridDim.x * 8) {
-    int t = __ldg(perm + row);
+  for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < T; t += gridDim.x * 8) {
+    int rows[kMaxCopies];
+    const int n = packed_rows(pos, t, T, k, S, rows);
     const uint4* s = reinterpret_cast<const uint4*>(src_row(st, t, (size_t)H * 2));
-    uint2* d = reinterpret_cast<uint2*>(P + (size_t)row * H);
     for (int v = lane; v < (H >> 3); v += 32) {  // H % 256 == 0: whole warp active
-      uint4 u = __ldg(s + v);
-      float x[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
-                    bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
+      const uint4 u = __ldg(s + v);
+      const float x[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
+                          bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
       float amax = 0.0f;
 #pragma unroll
       for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(x[q]));
 #pragma unroll
       for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      float scale = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
-      uint32_t q01, q23, q45, q67;
-      if (amax == 0.0f) {
-        q01 = q23 = q45 = q67 = 0;
-      } else {
-        q01 = cvt_e4m3x2(__fdiv_rn(x[1], scale), __fdiv_rn(x[0], scale));
-        q23 = cvt_e4m3x2(__fdiv_rn(x[3], scale), __fdiv_rn(x[2], scale));
-        q45 = cvt_e4m3x2(__fdiv_rn(x[5], scale), __fdiv_rn(x[4], scale));
-        q67 = cvt_e4m3x2(__fdiv_rn(x[7], scale), __fdiv_rn(x[6], scale));
+      const float scale = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+      uint2 q = make_uint2(0u, 0u);
+      if (amax != 0.0f) {
+        const uint32_t q01 = cvt_e4m3x2(__fdiv_rn(x[1], scale), __fdiv_rn(x[0], scale));
+        const uint32_t q23 = cvt_e4m3x2(__fdiv_rn(x[3], scale), __fdiv_rn(x[2], scale));
+        const uint32_t q45 = cvt_e4m3x2(__fdiv_rn(x[5], scale), __fdiv_rn(x[4], scale));
+        const uint32_t q67 = cvt_e4m3x2(__fdiv_rn(x[7], scale), __fdiv_rn(x[6], scale));
+        q = make_uint2(q01 | (q23 << 16), q45 | (q67 << 16));
       }
-      d[v] = make_uint2(q01 | (q23 << 16), q45 | (q67 << 16));
-      if ((lane & 15) == 0) P_scale[(size_t)row * nblk + (v >> 4)] = scale;
+      for (int c = 0; c < n; ++c) {
+        reinterpret_cast<uint2*>(P + (size_t)rows[c] * H)[v] = q;
+        if ((lane & 15) == 0) P_scale[(size_t)rows[c] * nblk + (v >> 4)] = scale;
+      }
     }
   }
 }
@@ -90,17 +107,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // bf16 Y (bf16 / fp8 layers): one warp per token, 8 channels per lane step.
+// KC = k at compile time (0: runtime k) so the k row loads issue together.
+template <int KC>
 __global__ void __launch_bounds__(256) combine_bf16_kernel(SrcTable st, const int32_t* __restrict__ pos,
                                                            const float* __restrict__ topk_w,
-                                                           const uint16_t* __restrict__ Y, int T, int k, int S,
+                                                           const uint16_t* __restrict__ Y, int T, int k_rt, int S,
                                                            int H) {
   const int lane = threadIdx.x & 31;
+  const int k = KC ? KC : k_rt;
   for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < T; t += gridDim.x * 8) {
     uint4* o = reinterpret_cast<uint4*>(out_row(st, t, (size_t)H * 2));
     for (int v = lane; v < (H >> 3); v += 32) {
       float acc[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+#pragma unroll 8
       for (int j = 0; j < k; ++j) {
         int r = __ldg(pos + (size_t)t * k + j);
         float w = __ldg(topk_w + (size_t)t * k + j);
@@ -156,13 +177,12 @@ inline int grid_for(int rows_per_block_units, int units, int num_sms) {
 
 cudaError_t launch_pack(const SrcTable& st, const LayerDims& d, int T, Workspace& ws, int num_sms,
                         cudaStream_t s) {
-  const int rows = T * (d.k + d.S);
-  if (rows == 0) return cudaSuccess;
-  const int grid = grid_for(8, rows, num_sms);
+  if (T == 0) return cudaSuccess;
+  const int grid = grid_for(8, T, num_sms);
   if (d.dtype == AFD_FP8_E4M3)
-    pack_fp8_kernel<<<grid, 256, 0, s>>>(st, ws.perm, rows, d.H, static_cast<uint8_t*>(ws.P), ws.P_scale);
+    pack_fp8_kernel<<<grid, 256, 0, s>>>(st, ws.pos, T, d.k, d.S, d.H, static_cast<uint8_t*>(ws.P), ws.P_scale);
   else
-    pack_copy_kernel<<<grid, 256, 0, s>>>(st, ws.perm, rows, d.H * (d.dtype == AFD_FP32 ? 4 : 2),
+    pack_copy_kernel<<<grid, 256, 0, s>>>(st, ws.pos, T, d.k, d.S, d.H * (d.dtype == AFD_FP32 ? 4 : 2),
                                           static_cast<uint8_t*>(ws.P));
   return cudaGetLastError();
 }
@@ -175,8 +195,23 @@ cudaError_t launch_combine(const SrcTable& st, const LayerDims& d, int T, Worksp
     combine_f32_kernel<<<grid, 256, 0, s>>>(st, ws.pos, ws.topk_w, static_cast<const float*>(ws.Y), T, d.k, d.S,
                                             d.H);
   else
-    combine_bf16_kernel<<<grid, 256, 0, s>>>(st, ws.pos, ws.topk_w, static_cast<const uint16_t*>(ws.Y), T, d.k,
-                                             d.S, d.H);
+    switch (d.k) {
+#define AFD_COMBINE_K(KV)                                                                                      \
+  case KV:                                                                                                     \
+    combine_bf16_kernel<KV><<<grid, 256, 0, s>>>(st, ws.pos, ws.topk_w, static_cast<const uint16_t*>(ws.Y), T, \
+                                                 d.k, d.S, d.H);                                               \
+    break;
+      AFD_COMBINE_K(1)
+      AFD_COMBINE_K(2)
+      AFD_COMBINE_K(3)
+      AFD_COMBINE_K(4)
+      AFD_COMBINE_K(6)
+      AFD_COMBINE_K(8)
+#undef AFD_COMBINE_K
+      default:
+        combine_bf16_kernel<0><<<grid, 256, 0, s>>>(st, ws.pos, ws.topk_w, static_cast<const uint16_t*>(ws.Y), T,
+                                                    d.k, d.S, d.H);
+    }
   return cudaGetLastError();
 }
 

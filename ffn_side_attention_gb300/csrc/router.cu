@@ -16,42 +16,80 @@
 // slot j holds the j-th ranked expert.  Weights w_j = exp(l_j - l_0) / sum over
 // the selected (fp32, expf), so they sum to 1.
 //
-// Work split: CTA (x, y) computes logits of tokens [16x, 16x+16) against
-// experts [32y, 32y+32); warp w covers 4 tokens x 16 experts (64 fp32
-// accumulators per lane).  The last CTA to finish a token tile (counted with
-// an atomic ticket) runs the top-k for those 16 tokens from the complete
-// logit rows and resets the ticket for the next forward.
+// Work split: CTA (x, y) computes the logits of tokens [32x, 32x+32) against
+// experts [ET y, ET y + ET) (ET = 32 for bf16, 16 for fp32).  Channels are
+// consumed in slabs of 256 (32 chunks, so lane l always owns chunk l of a
+// slab, which keeps the order above); each slab of the token rows and expert
+// rows is staged in shared memory with cp.async (3 stages for bf16).  Warp w
+// owns 8 tokens x 8 experts (64 fp32 accumulators per lane).  For bf16 the
+// products use the mixed-precision fma.rn.f32.bf16 (bf16 x bf16 + f32, one
+// rounding): bf16 products are exact in fp32, so it equals fma on the
+// widened values and needs no conversion instructions.  The last CTA to
+// finish a token tile (atomic ticket) selects the top-k for its 32 tokens and
+// resets the ticket.
 #include "afd_internal.cuh"
 
 namespace afd {
 namespace {
 
-constexpr int kTokPerWarp = 4;
-constexpr int kExpPerWarp = 16;
+constexpr int kTT = kRouterTokTile;  // 32 tokens per CTA
+constexpr int kWT = 8;               // tokens per warp
+constexpr int kWE = 8;               // experts per warp
+constexpr int kSlab = 256;           // channels per slab
 constexpr int kMaxK = 16;
 
-struct Chunk8 {
-  float v[8];
+// per activation type: experts per CTA, threads, cp.async stages
+template <typename TA>
+struct Cfg;
+template <>
+struct Cfg<uint16_t> {
+  static constexpr int ET = 32, kThreads = 512, kStages = 3;
+};
+template <>
+struct Cfg<float> {
+  static constexpr int ET = 16, kThreads = 256, kStages = 2;
 };
 
 template <typename TA>
-__device__ __forceinline__ void load8(const TA* p, Chunk8& c);
-
-template <>
-__device__ __forceinline__ void load8<uint16_t>(const uint16_t* p, Chunk8& c) {
-  uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
-  c.v[0] = bf16_lo(u.x); c.v[1] = bf16_hi(u.x);
-  c.v[2] = bf16_lo(u.y); c.v[3] = bf16_hi(u.y);
-  c.v[4] = bf16_lo(u.z); c.v[5] = bf16_hi(u.z);
-  c.v[6] = bf16_lo(u.w); c.v[7] = bf16_hi(u.w);
+constexpr int slab_bytes() {
+  return (kTT + Cfg<TA>::ET) * kSlab * (int)sizeof(TA);
+}
+template <typename TA>
+constexpr int router_smem_bytes() {
+  return Cfg<TA>::kStages * slab_bytes<TA>();
 }
 
-template <>
-__device__ __forceinline__ void load8<float>(const float* p, Chunk8& c) {
-  float4 a = __ldg(reinterpret_cast<const float4*>(p));
-  float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
-  c.v[0] = a.x; c.v[1] = a.y; c.v[2] = a.z; c.v[3] = a.w;
-  c.v[4] = b.x; c.v[5] = b.y; c.v[6] = b.z; c.v[7] = b.w;
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// c + a * b for the low / high bf16 halves of two packed words (one rounding)
+__device__ __forceinline__ float fma_bf16_lo(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, al, bl, %3;\n\t}"
+      : "=f"(d)
+      : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fma_bf16_hi(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, ah, bh, %3;\n\t}"
+      : "=f"(d)
+      : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ void lds8(const float* p, float* v) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *(reinterpret_cast<const float4*>(p) + 1);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
 // (value, index) ordering of the selection: larger value first, then lower id.
@@ -59,77 +97,140 @@ __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib)
   return va > vb || (va == vb && ia < ib);
 }
 
+// Stage slab s (channels [256 s, 256 s + 256)) of the CTA's token rows and
+// expert rows into shared memory.  Rows past T or E are left untouched: their
+// accumulators are never written out.
 template <typename TA>
-__global__ void __launch_bounds__(256) router_kernel(SrcTable st, const TA* __restrict__ wrT,
-                                                     const float* __restrict__ bias, int H, int E, int k,
-                                                     float* __restrict__ logits, int32_t* __restrict__ topk_idx,
-                                                     float* __restrict__ topk_w, int32_t* __restrict__ ticket) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int T = st.T;
-  const int t_base = blockIdx.x * kRouterTokTile + (warp >> 1) * kTokPerWarp;
-  const int e_base = blockIdx.y * kRouterExpTile + (warp & 1) * kExpPerWarp;
-
-  // rows of this warp's tokens (nullptr past the batch)
-  const TA* xrow[kTokPerWarp];
-#pragma unroll
-  for (int i = 0; i < kTokPerWarp; ++i) {
-    int t = t_base + i;
-    if (t < T) {
-      int m = src_of_token(st, t);
-      xrow[i] = reinterpret_cast<const TA*>(st.src[m]) + (size_t)(t - st.row0[m]) * H;
+__device__ __forceinline__ void stage_slab(TA* sx, TA* sw, const TA* const* xrow, const TA* __restrict__ wrT,
+                                           int e0, int E, int H, int s) {
+  constexpr int kET = Cfg<TA>::ET, kThreads = Cfg<TA>::kThreads;
+  constexpr int kUnits = (int)sizeof(TA) * 8 / 16;  // 16-byte pieces per 8-channel chunk
+  const int nch = min(32, (H >> 3) - 32 * s);       // chunks in this slab
+  const int per_row = nch * kUnits;
+  for (int u = threadIdx.x; u < (kTT + kET) * per_row; u += kThreads) {
+    const int r = u / per_row, q = u - r * per_row;
+    const TA* src;
+    TA* dst;
+    if (r < kTT) {
+      if (!xrow[r]) continue;
+      src = xrow[r];
+      dst = sx + r * kSlab;
     } else {
-      xrow[i] = nullptr;
+      const int e = e0 + (r - kTT);
+      if (e >= E) continue;
+      src = wrT + (size_t)e * H;
+      dst = sw + (r - kTT) * kSlab;
+    }
+    const int off = q * (16 / (int)sizeof(TA));  // element offset inside the slab
+    cp_async16(dst + off, src + (size_t)s * kSlab + off);
+  }
+}
+
+// One 8-channel chunk of the warp's 8 x 8 block: acc[i][j] += x_i . w_j over
+// the chunk's channels in ascending order.
+__device__ __forceinline__ void chunk_fma(const uint16_t* sx, const uint16_t* sw, int lane,
+                                          float (&acc)[kWT][kWE]) {
+  uint4 xr[kWT];
+#pragma unroll
+  for (int i = 0; i < kWT; ++i) xr[i] = *reinterpret_cast<const uint4*>(sx + i * kSlab + 8 * lane);
+#pragma unroll
+  for (int j = 0; j < kWE; ++j) {
+    const uint4 wr = *reinterpret_cast<const uint4*>(sw + j * kSlab + 8 * lane);
+#pragma unroll
+    for (int i = 0; i < kWT; ++i) {
+      float a = acc[i][j];
+      a = fma_bf16_lo(xr[i].x, wr.x, a); a = fma_bf16_hi(xr[i].x, wr.x, a);
+      a = fma_bf16_lo(xr[i].y, wr.y, a); a = fma_bf16_hi(xr[i].y, wr.y, a);
+      a = fma_bf16_lo(xr[i].z, wr.z, a); a = fma_bf16_hi(xr[i].z, wr.z, a);
+      a = fma_bf16_lo(xr[i].w, wr.w, a); a = fma_bf16_hi(xr[i].w, wr.w, a);
+      acc[i][j] = a;
     }
   }
+}
+__device__ __forceinline__ void chunk_fma(const float* sx, const float* sw, int lane, float (&acc)[kWT][kWE]) {
+  float xf[kWT][8];
+#pragma unroll
+  for (int i = 0; i < kWT; ++i) lds8(sx + i * kSlab + 8 * lane, xf[i]);
+#pragma unroll
+  for (int j = 0; j < kWE; ++j) {
+    float wf[8];
+    lds8(sw + j * kSlab + 8 * lane, wf);
+#pragma unroll
+    for (int i = 0; i < kWT; ++i)
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[i][j] = fmaf(xf[i][q], wf[q], acc[i][j]);
+  }
+}
 
-  float acc[kTokPerWarp][kExpPerWarp];
-#pragma unroll
-  for (int i = 0; i < kTokPerWarp; ++i)
-#pragma unroll
-    for (int j = 0; j < kExpPerWarp; ++j) acc[i][j] = 0.0f;
+template <typename TA>
+__global__ void __launch_bounds__(Cfg<TA>::kThreads, 1)
+    router_kernel(SrcTable st, const TA* __restrict__ wrT, const float* __restrict__ bias, int H, int E, int k,
+                  float* __restrict__ logits, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                  int32_t* __restrict__ ticket) {
+  constexpr int kET = Cfg<TA>::ET, kThreads = Cfg<TA>::kThreads, kStages = Cfg<TA>::kStages;
+  constexpr int kEG = kET / kWE;  // expert groups of warps
+  extern __shared__ __align__(16) uint8_t router_smem[];
+  __shared__ const TA* xrow[kTT];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = st.T;
+  const int t0 = blockIdx.x * kTT, e0 = blockIdx.y * kET;
+  for (int r = threadIdx.x; r < kTT; r += kThreads) {
+    const int t = t0 + r;
+    if (t < T) {
+      const int m = src_of_token(st, t);
+      xrow[r] = reinterpret_cast<const TA*>(st.src[m]) + (size_t)(t - st.row0[m]) * H;
+    } else {
+      xrow[r] = nullptr;
+    }
+  }
+  __syncthreads();
 
-  const int nchunk = H >> 3;
-  for (int c = lane; c < nchunk; c += kWarp) {
-    Chunk8 xc[kTokPerWarp];
+  auto buf = [&](int b) { return reinterpret_cast<TA*>(router_smem + b * slab_bytes<TA>()); };
+  const int nslab = (H + kSlab - 1) / kSlab;
+  const int wt = (warp / kEG) * kWT;  // warp's first token (in the CTA tile)
+  const int we = (warp % kEG) * kWE;  // warp's first expert (in the CTA tile)
+
+  float acc[kWT][kWE];
 #pragma unroll
-    for (int i = 0; i < kTokPerWarp; ++i) {
-      if (xrow[i]) load8<TA>(xrow[i] + 8 * c, xc[i]);
-      else {
+  for (int i = 0; i < kWT; ++i)
 #pragma unroll
-        for (int q = 0; q < 8; ++q) xc[i].v[q] = 0.0f;
-      }
+    for (int j = 0; j < kWE; ++j) acc[i][j] = 0.0f;
+
+#pragma unroll
+  for (int p = 0; p < kStages - 1; ++p) {
+    if (p < nslab) stage_slab<TA>(buf(p), buf(p) + kTT * kSlab, xrow, wrT, e0, E, H, p);
+    cp_async_commit();
+  }
+  for (int s = 0; s < nslab; ++s) {
+    cp_async_wait<kStages - 2>();
+    __syncthreads();
+    if (s + kStages - 1 < nslab) {
+      TA* nb = buf((s + kStages - 1) % kStages);
+      stage_slab<TA>(nb, nb + kTT * kSlab, xrow, wrT, e0, E, H, s + kStages - 1);
     }
-#pragma unroll
-    for (int j = 0; j < kExpPerWarp; ++j) {
-      int e = e_base + j;
-      if (e >= E) continue;
-      Chunk8 wc;
-      load8<TA>(wrT + (size_t)e * H + 8 * c, wc);
-#pragma unroll
-      for (int i = 0; i < kTokPerWarp; ++i)
-#pragma unroll
-        for (int q = 0; q < 8; ++q) acc[i][j] = fmaf(xc[i].v[q], wc.v[q], acc[i][j]);
-    }
+    cp_async_commit();
+    const TA* sx = buf(s % kStages);
+    if (32 * s + lane < (H >> 3))  // lane owns chunk 32 s + lane
+      chunk_fma(sx + wt * kSlab, sx + (kTT + we) * kSlab, lane, acc);
   }
 
   // fold the 32 lane partial sums: xor 16, 8, 4, 2, 1
 #pragma unroll
-  for (int i = 0; i < kTokPerWarp; ++i)
+  for (int i = 0; i < kWT; ++i)
 #pragma unroll
-    for (int j = 0; j < kExpPerWarp; ++j) {
+    for (int j = 0; j < kWE; ++j) {
       float v = acc[i][j];
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) v = v + __shfl_xor_sync(0xffffffffu, v, o);
       acc[i][j] = v;
     }
-
-  // every lane now holds every sum; lane (p % 32) writes pair p
+  // every lane holds every sum; lane (p % 32) writes pair p
 #pragma unroll
-  for (int i = 0; i < kTokPerWarp; ++i)
+  for (int i = 0; i < kWT; ++i)
 #pragma unroll
-    for (int j = 0; j < kExpPerWarp; ++j) {
-      int p = i * kExpPerWarp + j;
-      int t = t_base + i, e = e_base + j;
+    for (int j = 0; j < kWE; ++j) {
+      const int p = i * kWE + j;
+      const int t = t0 + wt + i, e = e0 + we + j;
       if ((p & 31) == lane && t < T && e < E) {
         float v = acc[i][j];
         if (bias) v = __fadd_rn(v, __ldg(bias + e));
@@ -141,23 +242,20 @@ __global__ void __launch_bounds__(256) router_kernel(SrcTable st, const TA* __re
   __shared__ int s_last;
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int prev = atomicAdd(ticket + blockIdx.x, 1);
-    s_last = (prev == (int)gridDim.y - 1);
-  }
+  if (threadIdx.x == 0) s_last = (atomicAdd(ticket + blockIdx.x, 1) == (int)gridDim.y - 1);
   __syncthreads();
   if (!s_last) return;
   __threadfence();
 
   constexpr int kMaxPerLane = (kMaxExperts + 31) / 32;  // E <= 256 -> 8 per lane
-  for (int tt = warp; tt < kRouterTokTile; tt += 8) {
-    int t = blockIdx.x * kRouterTokTile + tt;
+  for (int tt = warp; tt < kTT; tt += kThreads / 32) {
+    const int t = t0 + tt;
     if (t >= T) break;
     float v[kMaxPerLane];
     bool taken[kMaxPerLane];
 #pragma unroll
     for (int q = 0; q < kMaxPerLane; ++q) {
-      int e = lane + 32 * q;
+      const int e = lane + 32 * q;
       v[q] = (e < E) ? __ldcg(logits + (size_t)t * E + e) : 0.0f;
       taken[q] = (e >= E);
     }
@@ -166,22 +264,20 @@ __global__ void __launch_bounds__(256) router_kernel(SrcTable st, const TA* __re
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
       if (j >= k) break;
-      // best untaken entry of this lane
       float bv = 0.0f;
       int bi = 0x7fffffff;
 #pragma unroll
       for (int q = 0; q < kMaxPerLane; ++q) {
-        int e = lane + 32 * q;
+        const int e = lane + 32 * q;
         if (!taken[q] && (bi == 0x7fffffff || ranks_before(v[q], e, bv, bi))) {
           bv = v[q];
           bi = e;
         }
       }
-      // warp arg-best
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) {
-        float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
         if (oi != 0x7fffffff && (bi == 0x7fffffff || ranks_before(ov, oi, bv, bi))) {
           bv = ov;
           bi = oi;
@@ -194,8 +290,7 @@ __global__ void __launch_bounds__(256) router_kernel(SrcTable st, const TA* __re
         if (lane + 32 * q == bi) taken[q] = true;
     }
     if (lane == 0) {
-      float den = 0.0f;
-      float ex[kMaxK];
+      float den = 0.0f, ex[kMaxK];
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j) {
         if (j >= k) break;
@@ -215,16 +310,28 @@ __global__ void __launch_bounds__(256) router_kernel(SrcTable st, const TA* __re
 
 }  // namespace
 
+cudaError_t router_setup() {
+  cudaError_t e = cudaFuncSetAttribute(router_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       router_smem_bytes<float>());
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(router_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              router_smem_bytes<uint16_t>());
+}
+
 cudaError_t launch_router(const SrcTable& st, const void* wrT, const float* bias, const LayerDims& d,
                           Workspace& ws, cudaStream_t s) {
   if (st.T == 0) return cudaSuccess;
-  dim3 grid((st.T + kRouterTokTile - 1) / kRouterTokTile, (d.E + kRouterExpTile - 1) / kRouterExpTile);
-  if (d.dtype == AFD_FP32)
-    router_kernel<float><<<grid, 256, 0, s>>>(st, static_cast<const float*>(wrT), bias, d.H, d.E, d.k,
-                                              ws.logits, ws.topk_idx, ws.topk_w, ws.tile_counter);
-  else
-    router_kernel<uint16_t><<<grid, 256, 0, s>>>(st, static_cast<const uint16_t*>(wrT), bias, d.H, d.E,
-                                                 d.k, ws.logits, ws.topk_idx, ws.topk_w, ws.tile_counter);
+  if (d.dtype == AFD_FP32) {
+    dim3 grid((st.T + kTT - 1) / kTT, (d.E + Cfg<float>::ET - 1) / Cfg<float>::ET);
+    router_kernel<float><<<grid, Cfg<float>::kThreads, router_smem_bytes<float>(), s>>>(
+        st, static_cast<const float*>(wrT), bias, d.H, d.E, d.k, ws.logits, ws.topk_idx, ws.topk_w,
+        ws.tile_counter);
+  } else {
+    dim3 grid((st.T + kTT - 1) / kTT, (d.E + Cfg<uint16_t>::ET - 1) / Cfg<uint16_t>::ET);
+    router_kernel<uint16_t><<<grid, Cfg<uint16_t>::kThreads, router_smem_bytes<uint16_t>(), s>>>(
+        st, static_cast<const uint16_t*>(wrT), bias, d.H, d.E, d.k, ws.logits, ws.topk_idx, ws.topk_w,
+        ws.tile_counter);
+  }
   return cudaGetLastError();
 }
 

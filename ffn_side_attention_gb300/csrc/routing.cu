@@ -31,6 +31,7 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
+constexpr int kBatch = 16;  // 32-entry steps whose ids are loaded together
 
 // inclusive scan of one value per lane
 __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
@@ -59,18 +60,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int i = threadIdx.x; i < kWarps * E; i += kThreads) hist[i] = 0;
   __syncthreads();
 
-  // pass 1: per-warp counts
+  // pass 1: per-warp counts.  The expert ids of kBatch steps are loaded up
+  // front (independent loads in flight), then walked in order.
   int* my = hist + warp * E;
-  for (int b = beg; b < end; b += 32) {
-    int i = b + lane;
-    int e = (i < end) ? __ldg(idx + i) : -1;
-    if (e >= E || e < -1) {
-      atomicOr(err, kErrRange);
-      e = -1;
+  for (int b0 = beg; b0 < end; b0 += 32 * kBatch) {
+    int ev[kBatch];
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      const int i = b0 + 32 * q + lane;
+      ev[q] = (i < end) ? __ldg(idx + i) : -1;
     }
-    unsigned peers = __match_any_sync(0xffffffffu, e);
-    if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
-    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      if (b0 + 32 * q >= end) break;
+      int e = ev[q];
+      if (e >= E || e < -1) {
+        atomicOr(err, kErrRange);
+        e = -1;
+      }
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
+      __syncwarp();
+    }
   }
   __syncthreads();
 
@@ -117,20 +128,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // pass 2: positions
-  for (int b = beg; b < end; b += 32) {
-    int i = b + lane;
-    int e = (i < end) ? __ldg(idx + i) : -1;
-    if (e >= E || e < -1) e = -1;
-    unsigned peers = __match_any_sync(0xffffffffu, e);
-    if (e >= 0) {
-      int rank = my[e] + __popc(peers & ((1u << lane) - 1u));
-      int row = s_off[e] + rank;
-      perm[row] = i / k;
-      pos[i] = row;
+  for (int b0 = beg; b0 < end; b0 += 32 * kBatch) {
+    int ev[kBatch];
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      const int i = b0 + 32 * q + lane;
+      ev[q] = (i < end) ? __ldg(idx + i) : -1;
     }
-    __syncwarp();
-    if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
-    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      if (b0 + 32 * q >= end) break;
+      const int i = b0 + 32 * q + lane;
+      int e = ev[q];
+      if (e >= E || e < -1) e = -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      if (e >= 0) {
+        const int rank = my[e] + __popc(peers & ((1u << lane) - 1u));
+        const int row = s_off[e] + rank;
+        perm[row] = i / k;
+        pos[i] = row;
+      }
+      __syncwarp();
+      if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
+      __syncwarp();
+    }
   }
   // shared expert rows: token order
   if (S)
@@ -143,7 +164,8 @@ cudaError_t launch_routing(const LayerDims& d, int T, Workspace& ws, cudaStream_
   if (T == 0) return cudaSuccess;
   const int G = d.E + d.S;
   size_t smem = sizeof(int) * ((size_t)kWarps * d.E + 2 * (G + 1));
-  routing_kernel<<<1, kThreads, smem, s>>>(ws.topk_idx, T, d.k, d.E, d.S, kGemmBN, ws.counts, ws.offsets,
+  const int bn = d.dtype == AFD_FP8_E4M3 ? kGemmBNFp8 : kGemmBN;  // tokens per GEMM tile
+  routing_kernel<<<1, kThreads, smem, s>>>(ws.topk_idx, T, d.k, d.E, d.S, bn, ws.counts, ws.offsets,
                                            ws.tile_base, ws.perm, ws.pos, ws.err);
   return cudaGetLastError();
 }

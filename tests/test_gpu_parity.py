@@ -134,3 +134,65 @@ def test_argument_errors():
         layer.forward(x[:1], n_micro=9)
     assert e.value.code == afd.AFD_EINVAL
     layer.check()
+
+
+@pytest.mark.parametrize("shape,counts", [
+    (dict(H=264, I=128, E=12, k=3), [7, 30]),     # partial 256-channel slab, partial expert tile
+    (dict(H=8, I=16, E=5, k=5), [3]),             # one chunk of channels, k = E
+])
+def test_fp32_router_edges(shape, counts):
+    c = _small(dtype="fp32", **shape)
+    layer, srcs, outs, r, ref = run_case(c, counts)
+    assert_routing_exact(c, r, ref, sum(counts))
+    assert_close(c, out_to_f64(outs), ref_to_f64(c, ref["out"]))
+
+
+@pytest.mark.parametrize("shape,counts", [
+    (dict(dtype="fp8", S=1), [17, 0, 40]),
+    (dict(dtype="fp8", E=4, k=2, H=512, I=384), [300, 301]),       # > 128 rows per expert: several N tiles
+    (dict(dtype="fp8", E=48, k=3, H=768, I=640, S=1), [2, 5]),
+])
+def test_fp8_shapes(shape, counts):
+    c = _small(**shape)
+    layer, srcs, outs, r, ref = run_case(c, counts)
+    assert_routing_exact(c, r, ref, sum(counts))
+    assert_close(c, out_to_f64(outs), ref_to_f64(c, ref["out"]))
+
+
+def _sampled(c, n_random=12, seed=13):
+    T = c.T
+    rng = np.random.default_rng(seed)
+    edges = {0, T - 1} | {m * c.B for m in range(c.M)} | {m * c.B - 1 for m in range(1, c.M)}
+    return sorted(edges | set(rng.choice(T, n_random, replace=False).tolist()))
+
+
+def test_qwen3_fp8_full_size_sampled():
+    c = synth.CONFIGS["qwen3_fp8"]
+    tokens = _sampled(c)
+    layer, srcs, outs, r, ref = run_case(c, [c.B] * c.M, tokens=tokens)
+    assert_routing_exact(c, r, ref, c.T)
+    assert_close(c, out_to_f64(outs)[tokens], ref_to_f64(c, ref["out"]))
+
+
+@pytest.mark.parametrize("B", [64, 512])
+def test_dsv3_fp8_zipf_sampled(B):
+    """DeepSeek-V3 shapes, Zipf-biased routing, shared expert; T = 8 x B."""
+    c = synth.CONFIGS["dsv3_fp8"].with_batch(B, 8)
+    tokens = _sampled(c, n_random=8)
+    layer, srcs, outs, r, ref = run_case(c, [c.B] * c.M, tokens=tokens)
+    assert_routing_exact(c, r, ref, c.T)
+    assert_close(c, out_to_f64(outs)[tokens], ref_to_f64(c, ref["out"]))
+
+
+def test_step3_bf16_three_microbatches_sampled():
+    """Step3 shapes: T = 8 x 256 as three pipelined micro-batches (683/683/682),
+    bitwise equal to one pass, sampled tokens against the oracle."""
+    c = synth.CONFIGS["step3_bf16"]
+    tokens = _sampled(c, n_random=8)
+    layer, srcs, outs, r, ref = run_case(c, [c.B] * c.M, tokens=tokens)
+    assert_routing_exact(c, r, ref, c.T)
+    assert_close(c, out_to_f64(outs)[tokens], ref_to_f64(c, ref["out"]))
+    piped = layer.forward(srcs, n_micro=3)
+    torch.cuda.synchronize()
+    for x, y in zip(outs, piped):
+        assert torch.equal(x, y)
