@@ -48,7 +48,7 @@ constexpr int kRegsHigh = 224;                  // setmaxnreg of the epilogue wa
 constexpr int kRegsNeeded = (128 * kRegsLow + 256 * kRegsHigh + kThreads - 1) / kThreads;  // 168
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kDrainCycles = 400000000ll;  // ~0.2 s
-constexpr int kChunk = 16;                        // TMEM columns per load
+constexpr int kMaxKb = 56;                        // K blocks per GEMM (K <= 7168)
 
 struct Fp8Args {
   const int32_t* counts;
@@ -133,6 +133,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int s_abort;
   __shared__ int s_tb[kMaxExperts + 1], s_off[kMaxExperts + 1], s_cnt[kMaxExperts];
   __shared__ float s_red[2][4][64];  // per column half, quadrant, column: |h| maxima
+  __shared__ __align__(16) float s_sc[kMaxKb][kBN];  // this item's activation scales, [kb][token column]
+  __shared__ float s_w[2][kMaxKb];                   // this item's weight block scales (A0, A1)
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* pfull = bars + 2 * kStages;       // [2] MMA -> epilogue
@@ -262,34 +264,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item it = decode_item(item, args.MT, G, s_tb, s_off, s_cnt);
       const int c0 = half * 64;
       const int nc = max(0, min(64, it.nrows - c0));  // this warp's columns
-      const size_t blk0 = (size_t)it.g * (args.a_rows_per_group / 128) + it.mt * (args.a_mt_stride / 128);
-      const float* sA0 = args.sA0 + blk0 * args.num_kb;
-      const float* sA1 = args.sA1 + (blk0 + args.sa1_block_offset) * args.num_kb;
-      const float* sB = args.sB + (size_t)(it.row0 + c0) * args.num_kb;
+      const int nkb = args.num_kb;
+      // stage the item's scales in shared memory (the previous item is done with them)
+      if (!epi_sync(ebar, ephase, lane, abort, args.err)) break;
+      {
+        const size_t blk0 = (size_t)it.g * (args.a_rows_per_group / 128) + it.mt * (args.a_mt_stride / 128);
+        const float* sB = args.sB + (size_t)it.row0 * nkb;  // rows row0 .. row0+nrows-1 are contiguous
+        for (int q = ew * 32 + lane; q < it.nrows * nkb; q += 32 * kEpiWarps) {
+          const int col = q / nkb, kb = q - col * nkb;
+          s_sc[kb][col] = __ldg(sB + q);
+        }
+        for (int q = ew * 32 + lane; q < 2 * nkb; q += 32 * kEpiWarps) {
+          const int which = q / nkb, kb = q - which * nkb;
+          s_w[which][kb] = __ldg((which ? args.sA1 + (blk0 + args.sa1_block_offset) * nkb : args.sA0 + blk0 * nkb) + kb);
+        }
+      }
+      if (!epi_sync(ebar, ephase, lane, abort, args.err)) break;
       float acc0[64], acc1[64];
 #pragma unroll
       for (int j = 0; j < 64; ++j) acc0[j] = acc1[j] = 0.0f;
-      for (int kb = 0; kb < args.num_kb; ++kb, ++gstep) {
+      for (int kb = 0; kb < nkb; ++kb, ++gstep) {
         const uint32_t b = gstep & 1u, use = gstep >> 1;
         if (!mbar_wait(&pfull[b], use & 1u, abort, args.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const float w0 = __ldg(sA0 + kb), w1 = __ldg(sA1 + kb);
+        const float w0 = s_w[0][kb], w1 = s_w[1][kb];
 #pragma unroll
-        for (int cc = 0; cc < 64; cc += kChunk) {
+        for (int cc = 0; cc < 64; cc += 32) {
           if (cc < nc) {
-            float p0[kChunk], p1[kChunk];
-            tmem_ld_x16(t_lane + b * 256u + (uint32_t)(c0 + cc), p0);
-            tmem_ld_x16(t_lane + b * 256u + 128u + (uint32_t)(c0 + cc), p1);
+            float p0[32], p1[32];
+            const uint32_t col = t_lane + b * 256u + (uint32_t)(c0 + cc);
+            tmem_ld_x16(col, p0);
+            tmem_ld_x16(col + 16u, p0 + 16);
+            tmem_ld_x16(col + 128u, p1);
+            tmem_ld_x16(col + 144u, p1 + 16);
             tmem_ld_wait();
+            const float4* sc4 = reinterpret_cast<const float4*>(&s_sc[kb][c0 + cc]);
 #pragma unroll
-            for (int j = 0; j < kChunk; ++j) {
-              if (cc + j < nc) {
-                const float sa = __ldg(sB + (size_t)(cc + j) * args.num_kb + kb);
-                acc0[cc + j] = fmaf(w0 * sa, p0[j], acc0[cc + j]);
-                acc1[cc + j] = fmaf(w1 * sa, p1[j], acc1[cc + j]);
+            for (int j4 = 0; j4 < 8; ++j4) {
+              const float4 sa = sc4[j4];
+              const float sv[4] = {sa.x, sa.y, sa.z, sa.w};
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int j = 4 * j4 + u;
+                acc0[cc + j] = fmaf(w0 * sv[u], p0[j], acc0[cc + j]);
+                acc1[cc + j] = fmaf(w1 * sv[u], p1[j], acc1[cc + j]);
               }
             }
           }
@@ -329,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (r == 0) args.out_scale[row * nblk + it.mt] = sc;
           }
         }
-        if (!epi_sync(ebar, ephase, lane, abort, args.err)) break;  // s_red is reused by the next item
+        // s_red is reused by the next item: the sync at the next item's start orders it
       } else {
         uint16_t* outy = static_cast<uint16_t*>(args.out);
         const int col = it.mt * 2 * kGemmBM + r;
