@@ -31,9 +31,9 @@ struct afd_ffn {
   // weights in kernel layout
   void* wrT = nullptr;      // [E, H] router, K-major
   float* bias = nullptr;    // [E] or null
-  void* wgT = nullptr;      // [(E+S), I, H]
-  void* wuT = nullptr;      // [(E+S), I, H]
-  void* wdT = nullptr;      // [(E+S), H, I]
+  void* wgT = nullptr;      // gate, per group [I/128][H/KW][128][KW] (KW = 128 bytes of K)
+  void* wuT = nullptr;      // up, same
+  void* wdT = nullptr;      // down, per group [H/128][I/KW][128][KW]
   float* sgT = nullptr;     // fp8: [(E+S), I/128, H/128]
   float* suT = nullptr;
   float* sdT = nullptr;     // fp8: [(E+S), H/128, I/128]
@@ -313,13 +313,13 @@ int create_impl(const afd_ffn_config* cfg, const afd_ffn_weights* w, afd_ffn* h)
     uint8_t* g8 = static_cast<uint8_t*>(h->wgT);
     uint8_t* u8 = static_cast<uint8_t*>(h->wuT);
     uint8_t* d8 = static_cast<uint8_t*>(h->wdT);
-    CUDA_TRY(h, afd::launch_transpose(w->w_gate, g8, (int)E, (int)H, (int)I, (int)wb, s));
-    CUDA_TRY(h, afd::launch_transpose(w->w_up, u8, (int)E, (int)H, (int)I, (int)wb, s));
-    CUDA_TRY(h, afd::launch_transpose(w->w_down, d8, (int)E, (int)I, (int)H, (int)wb, s));
+    CUDA_TRY(h, afd::launch_tile_weights(w->w_gate, g8, (int)E, (int)H, (int)I, (int)wb, s));
+    CUDA_TRY(h, afd::launch_tile_weights(w->w_up, u8, (int)E, (int)H, (int)I, (int)wb, s));
+    CUDA_TRY(h, afd::launch_tile_weights(w->w_down, d8, (int)E, (int)I, (int)H, (int)wb, s));
     if (S) {
-      CUDA_TRY(h, afd::launch_transpose(w->sh_gate, g8 + E * I * H * wb, 1, (int)H, (int)I, (int)wb, s));
-      CUDA_TRY(h, afd::launch_transpose(w->sh_up, u8 + E * I * H * wb, 1, (int)H, (int)I, (int)wb, s));
-      CUDA_TRY(h, afd::launch_transpose(w->sh_down, d8 + E * H * I * wb, 1, (int)I, (int)H, (int)wb, s));
+      CUDA_TRY(h, afd::launch_tile_weights(w->sh_gate, g8 + E * I * H * wb, 1, (int)H, (int)I, (int)wb, s));
+      CUDA_TRY(h, afd::launch_tile_weights(w->sh_up, u8 + E * I * H * wb, 1, (int)H, (int)I, (int)wb, s));
+      CUDA_TRY(h, afd::launch_tile_weights(w->sh_down, d8 + E * H * I * wb, 1, (int)I, (int)H, (int)wb, s));
     }
     const bool fp8 = c.dtype == AFD_FP8_E4M3;
     if (fp8) {
@@ -337,8 +337,10 @@ int create_impl(const afd_ffn_config* cfg, const afd_ffn_weights* w, afd_ffn* h)
         CUDA_TRY(h, afd::launch_transpose_f32(w->sh_s_down, h->sdT + E * hb * ib, 1, (int)ib, (int)hb, s));
       }
     }
-    if (!make_map(&h->tm_wg, h->wgT, fp8, H, G * I, 128) || !make_map(&h->tm_wu, h->wuT, fp8, H, G * I, 128) ||
-        !make_map(&h->tm_wd, h->wdT, fp8, I, G * H, 128))
+    // tiled weights: rows of 128 bytes (one K block of one output row), 128-row boxes
+    const uint64_t kw = 128 / wb, tile_rows = G * H * I / kw;
+    if (!make_map(&h->tm_wg, h->wgT, fp8, kw, tile_rows, 128) ||
+        !make_map(&h->tm_wu, h->wuT, fp8, kw, tile_rows, 128) || !make_map(&h->tm_wd, h->wdT, fp8, kw, tile_rows, 128))
       return fail(h, AFD_ECUDA, "cuTensorMapEncodeTiled failed for a weight operand");
   }
   if ((rc = alloc_workspace(h, h->ws[0]))) return rc;

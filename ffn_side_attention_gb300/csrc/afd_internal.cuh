@@ -84,9 +84,9 @@ cudaError_t launch_gemm_simt(const LayerDims& d, int T, const float* wg, const f
                              Workspace& ws, cudaStream_t s, int which);  // which: 0 gate/up, 1 down
 
 struct TcWeights {
-  const CUtensorMap* tm_wg;  // [(E+S)*I, H] K-major
-  const CUtensorMap* tm_wu;
-  const CUtensorMap* tm_wd;  // [(E+S)*H, I] K-major
+  const CUtensorMap* tm_wg;  // gate, tiled: per group (I/128) x (H/KW) tiles of 128 rows x 128 bytes
+  const CUtensorMap* tm_wu;  // up, same
+  const CUtensorMap* tm_wd;  // down, tiled: per group (H/128) x (I/KW) tiles
   const float* sg;           // fp8: [(E+S), I/128, H/128]  (m-block major)
   const float* su;
   const float* sd;           // fp8: [(E+S), H/128, I/128]
@@ -100,6 +100,9 @@ cudaError_t gemm_fp8_setup();
 
 cudaError_t launch_transpose(const void* src, void* dst, int batch, int rows, int cols, int elem_bytes,
                              cudaStream_t s);
+// batch x [K][R] -> per matrix 16 KB tiles (128 rows of R x 128 bytes of K), (row block, K block) order
+cudaError_t launch_tile_weights(const void* src, void* dst, int batch, int K, int R, int elem_bytes,
+                                cudaStream_t s);
 cudaError_t launch_transpose_f32(const float* src, float* dst, int batch, int rows, int cols,
                                  cudaStream_t s);
 

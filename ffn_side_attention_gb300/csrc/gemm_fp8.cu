@@ -188,8 +188,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
         const Item it = decode_item(item, args.MT, G, s_tb, s_off, s_cnt);
-        const int a0 = it.g * args.a_rows_per_group + it.mt * args.a_mt_stride;
-        const int a1 = a0 + args.a1_offset;
+        // tiled weights: tile (row block rb, K block kb) starts at tile row (rb * num_kb + kb) * 128
+        const int rb0 = it.g * (args.a_rows_per_group / 128) + it.mt * (args.a_mt_stride / 128);
+        const int rb1 = rb0 + args.a1_offset / 128;
         const int nbox = (it.nrows + kBBoxRows - 1) / kBBoxRows;
         const uint32_t bytes = 2 * kATile + nbox * kBBoxRows * kRowBytes;
         for (int kb = 0; kb < args.num_kb; ++kb) {
@@ -199,8 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* st = smem + s * kStageBytes;
           mbar_arrive_expect_tx(&full[s], bytes);
-          tma_load_2d_hint(st, &tmA0, &full[s], kb * 128, a0, pol_w);
-          tma_load_2d_hint(st + kATile, &tmA1, &full[s], kb * 128, a1, pol_w);
+          tma_load_2d_hint(st, &tmA0, &full[s], 0, (rb0 * args.num_kb + kb) * 128, pol_w);
+          tma_load_2d_hint(st + kATile, &tmA1, &full[s], 0, (rb1 * args.num_kb + kb) * 128, pol_w);
           for (int b = 0; b < nbox; ++b)
             tma_load_2d_hint(st + 2 * kATile + b * kBBoxRows * kRowBytes, &tmB, &full[s], kb * 128,
                              it.row0 + b * kBBoxRows, pol_b);

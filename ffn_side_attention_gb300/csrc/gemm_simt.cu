@@ -74,7 +74,44 @@ __global__ void transpose_kernel(const Elem* __restrict__ src, Elem* __restrict_
   }
 }
 
+// Weight tiling for the tensor-core GEMMs.  src holds `batch` matrices
+// [K][R] (the caller's [in][out] layout); dst holds, per matrix, tiles of 128
+// output rows x 128 bytes of K, ordered (row block, K block): tile (rb, kb) is
+// one contiguous 16 KB block holding rows rb*128 .. +127 of the transposed
+// matrix, K elements kb*KW .. +KW-1, so every TMA box of the GEMM reads one
+// contiguous block and an item's K blocks follow each other in memory.
+template <typename Elem>
+__global__ void __launch_bounds__(256) tile_weights_kernel(const Elem* __restrict__ src, Elem* __restrict__ dst,
+                                                           int K, int R) {
+  constexpr int KW = 128 / (int)sizeof(Elem);
+  __shared__ Elem tile[KW][128 + 4];
+  const int rb = blockIdx.x, kb = blockIdx.y;
+  const size_t base = (size_t)blockIdx.z * K * R;
+  const Elem* s = src + base + (size_t)kb * KW * R + (size_t)rb * 128;
+  for (int i = threadIdx.x; i < KW * 128; i += 256) tile[i >> 7][i & 127] = s[(size_t)(i >> 7) * R + (i & 127)];
+  __syncthreads();
+  Elem* d = dst + base + ((size_t)rb * (K / KW) + kb) * 128 * KW;
+  for (int i = threadIdx.x; i < KW * 128; i += 256) d[i] = tile[i % KW][i / KW];
+}
+
 }  // namespace
+
+cudaError_t launch_tile_weights(const void* src, void* dst, int batch, int K, int R, int elem_bytes,
+                                cudaStream_t s) {
+  if ((size_t)batch * K * R == 0) return cudaSuccess;
+  const int kw = 128 / elem_bytes;
+  if (R % 128 || K % kw) return cudaErrorInvalidValue;
+  dim3 grid(R / 128, K / kw, batch);
+  if (elem_bytes == 1)
+    tile_weights_kernel<uint8_t><<<grid, 256, 0, s>>>(static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst),
+                                                      K, R);
+  else if (elem_bytes == 2)
+    tile_weights_kernel<uint16_t><<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(src),
+                                                       static_cast<uint16_t*>(dst), K, R);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gemm_simt(const LayerDims& d, int T, const float* wg, const float* wu, const float* wd,
                              Workspace& ws, cudaStream_t s, int which) {
