@@ -14,7 +14,7 @@ namespace afd {
 // ---------------------------------------------------------------- constants
 constexpr int kWarp = 32;
 constexpr int kRouterTokTile = 32;  // tokens per router CTA
-constexpr int kGemmBN = 256;        // max tokens per GEMM tile (MMA N)
+constexpr int kGemmBN = 256;        // largest token tile of the bf16 GEMMs (MMA N)
 constexpr int kGemmBM = 128;        // weight rows per MMA (MMA M)
 constexpr int kGemmBNFp8 = 128;     // max tokens per fp8 GEMM tile
 constexpr int kMaxExperts = 257;    // routed + shared
@@ -94,6 +94,7 @@ struct TcWeights {
 cudaError_t launch_gemm_tc(const LayerDims& d, int T, const TcWeights& w, Workspace& ws, int num_sms,
                            cudaStream_t s, int which);  // which: 0 gate/up + SwiGLU, 1 down
 cudaError_t gemm_tc_setup();  // opt-in shared memory sizes (once per process)
+int bf16_tile_tokens(const LayerDims& d, int T);  // token-tile width of the bf16 GEMMs for a batch of T
 cudaError_t launch_gemm_fp8(const LayerDims& d, int T, const TcWeights& w, Workspace& ws, int num_sms,
                             cudaStream_t s, int which);  // fp8 layer: 0 gate/up + SwiGLU + e4m3 h, 1 down
 cudaError_t gemm_fp8_setup();

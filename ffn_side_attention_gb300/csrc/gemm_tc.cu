@@ -9,7 +9,7 @@
 //
 // Swap-AB: decode batches give an expert few tokens (1..~250), so the weight
 // matrix is the MMA's M side (128 weight rows per MMA) and the expert's tokens
-// are the N side (16..256, padded to 16).  At create time the weights are
+// are the N side (16..128, padded to 16).  At create time the weights are
 // re-laid as contiguous 16 KB tiles (128 output rows x 128 bytes of K, K
 // blocks of one row block consecutive), so each TMA box is one sequential
 // DRAM read and both operands are K-major.
@@ -17,14 +17,15 @@
 //             h[row, i] = silu(D0) * D1 -> bf16   (one CTA item = 128 channels)
 //   down:     D0 = Wd^T[e][o0:o0+128, :] * h^T,   D1 = rows o0+128..o0+256
 //             Y[row, o] = D -> bf16                (one CTA item = 256 columns)
-// Two accumulators of up to 256 fp32 columns fill the 512 TMEM columns.
+// Two accumulators of up to 128 fp32 columns, double buffered (the epilogue of
+// one item overlaps the MMAs of the next), fill the 512 TMEM columns.
 //
 // Work list: item = (group g, m tile, token tile) in that order, enumerated on
 // the device from tile_base (no host sync); items of one (g, m tile) are
 // adjacent so concurrently running CTAs share the weight tile in L2.  The
 // kernel is persistent: grid = SM count, CTA c takes items c, c+grid, ...
 //
-// Warp roles (192 threads): warp 0 lane 0 issues TMA into a 3-stage ring
+// Warp roles (192 threads): warp 0 lane 0 issues TMA into a 4-stage ring
 // (weights with an L2 evict-first hint, activations evict-last); warp 1
 // owns TMEM and lane 0 issues tcgen05.mma; warps 2-5 are the epilogue
 // (warp w reads TMEM lanes 32*(w%4) .. +31).  Every mbarrier wait is bounded:
@@ -38,14 +39,23 @@
 namespace afd {
 namespace {
 
-constexpr int kStages = 3;
-constexpr int kRowBytes = 128;                    // one 128-byte swizzle row of K
-constexpr int kATile = kGemmBM * kRowBytes;       // 16 KB
-constexpr int kBTile = kGemmBN * kRowBytes;       // 32 KB
-constexpr int kBBoxRows = 32;                     // rows per TMA box of B
-constexpr int kStageBytes = 2 * kATile + kBTile;  // 64 KB
-constexpr int kDynSmem = kStages * kStageBytes + 1024;
+constexpr int kRowBytes = 128;               // one 128-byte swizzle row of K
+constexpr int kATile = kGemmBM * kRowBytes;  // 16 KB
+constexpr int kBBoxRows = 32;                // rows per TMA box of B
 constexpr int kThreads = 192;
+
+// Tile shape per token-tile width BN: 128 -> 4 stages of 48 KB and two TMEM
+// accumulator buffers (epilogue overlaps the next item); 256 -> 3 stages of
+// 64 KB and one accumulator buffer (an expert's <= 256 tokens share one pass
+// over its weights).
+template <int BN>
+struct TileCfg {
+  static constexpr int kStages = BN == 256 ? 3 : 4;
+  static constexpr int kBTile = BN * kRowBytes;
+  static constexpr int kStageBytes = 2 * kATile + kBTile;
+  static constexpr int kDynSmem = kStages * kStageBytes + 1024;
+  static constexpr int kAbuf = 512 / (2 * BN);  // TMEM accumulator buffers
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kDrainCycles = 400000000ll;  // ~0.2 s
 
@@ -69,6 +79,7 @@ struct Item {
   int g, mt, row0, nrows;
 };
 
+template <int BN>
 __device__ __forceinline__ Item decode_item(int item, int MT, int G, const int* tb, const int* off,
                                             const int* cnt) {
   int lo = 0, hi = G - 1;  // last g with MT * tb[g] <= item
@@ -82,8 +93,8 @@ __device__ __forceinline__ Item decode_item(int item, int MT, int G, const int* 
   const int local = item - MT * tb[lo];
   it.mt = local / nt_g;
   const int nt = local - it.mt * nt_g;
-  it.row0 = off[lo] + nt * kGemmBN;
-  it.nrows = min(kGemmBN, cnt[lo] - nt * kGemmBN);
+  it.row0 = off[lo] + nt * BN;
+  it.nrows = min(BN, cnt[lo] - nt * BN);
   return it;
 }
 
@@ -93,21 +104,24 @@ __device__ __forceinline__ uint16_t f2bf(float v) {
   return *reinterpret_cast<uint16_t*>(&b);
 }
 
+template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                      const __grid_constant__ CUtensorMap tmB, const TcArgs args) {
+  constexpr int kStages = TileCfg<BN>::kStages, kStageBytes = TileCfg<BN>::kStageBytes;
+  constexpr uint32_t kAbuf = TileCfg<BN>::kAbuf;
   extern __shared__ uint8_t dyn_smem[];
   uint8_t* smem = dyn_smem + ((1024u - (smem_u32(dyn_smem) & 1023u)) & 1023u);
 
-  __shared__ __align__(8) uint64_t bars[2 * kStages + 3];
+  __shared__ __align__(8) uint64_t bars[2 * kStages + 5];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_tb[kMaxExperts + 1], s_off[kMaxExperts + 1], s_cnt[kMaxExperts];
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
-  uint64_t* tfull = bars + 2 * kStages;
-  uint64_t* tempty = tfull + 1;
-  uint64_t* drain = tfull + 2;
+  uint64_t* tfull = bars + 2 * kStages;  // [2] accumulator buffer ready for the epilogue
+  uint64_t* tempty = tfull + 2;          // [2] accumulator buffer drained by the epilogue
+  uint64_t* drain = tfull + 4;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = args.G;
@@ -121,8 +135,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(tfull, 1);
-    mbar_init(tempty, 4);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
     mbar_init(drain, 1);
     s_abort = 0;
     fence_mbar_init();
@@ -150,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0, filled = 0, fill_ph = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
-        const Item it = decode_item(item, args.MT, G, s_tb, s_off, s_cnt);
+        const Item it = decode_item<BN>(item, args.MT, G, s_tb, s_off, s_cnt);
         // tiled weights: tile (row block rb, K block kb) starts at tile row (rb * num_kb + kb) * 128
         const int rb0 = it.g * (args.a_rows_per_group / 128) + it.mt * (args.a_mt_stride / 128);
         const int rb1 = rb0 + args.a1_offset / 128;
@@ -184,15 +200,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // ---------------- MMA issuer
       int s = 0;
-      uint32_t ph = 0, tph = 0;
+      uint32_t ph = 0, ic = 0;
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
-        const Item it = decode_item(item, args.MT, G, s_tb, s_off, s_cnt);
+      for (int item = blockIdx.x; ok && item < total; item += gridDim.x, ++ic) {
+        const Item it = decode_item<BN>(item, args.MT, G, s_tb, s_off, s_cnt);
         const int N = (it.nrows + 15) & ~15;
         const uint32_t idesc = mma_idesc(1u, kGemmBM, N);
-        if (!mbar_wait(tempty, tph ^ 1u, abort, args.err)) break;
-        tph ^= 1u;
+        const uint32_t a = ic % kAbuf;  // accumulator buffer of this item
+        if (!mbar_wait(&tempty[a], ((ic / kAbuf) & 1u) ^ 1u, abort, args.err)) break;
         tc_fence_after();
+        const uint32_t d0 = tmem + a * (2u * BN), d1 = d0 + BN;
         for (int kb = 0; kb < args.num_kb; ++kb) {
           if (!mbar_wait(&full[s], ph, abort, args.err)) {
             ok = false;
@@ -206,8 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {  // 4 x K=16 per 128-byte row
             const uint32_t acc = (kb | kk) ? 1u : 0u;
-            mma_f16(tmem, da0 + 2 * kk, db + 2 * kk, idesc, acc);
-            mma_f16(tmem + kGemmBN, da1 + 2 * kk, db + 2 * kk, idesc, acc);
+            mma_f16(d0, da0 + 2 * kk, db + 2 * kk, idesc, acc);
+            mma_f16(d1, da1 + 2 * kk, db + 2 * kk, idesc, acc);
           }
           tc_commit(&empty[s]);
           if (++s == kStages) {
@@ -216,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        tc_commit(tfull);
+        tc_commit(&tfull[a]);
       }
       tc_commit(drain);  // all MMAs issued above complete before TMEM is freed
       mbar_wait_cycles(drain, 0, kDrainCycles);
@@ -226,16 +243,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // row of the 128-row MMA tile
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
-    uint32_t tph = 0;
-    for (int item = blockIdx.x; item < total; item += gridDim.x) {
-      const Item it = decode_item(item, args.MT, G, s_tb, s_off, s_cnt);
-      if (!mbar_wait(tfull, tph, abort, args.err)) break;
-      tph ^= 1u;
+    uint32_t ic = 0;
+    for (int item = blockIdx.x; item < total; item += gridDim.x, ++ic) {
+      const Item it = decode_item<BN>(item, args.MT, G, s_tb, s_off, s_cnt);
+      const uint32_t a = ic % kAbuf;
+      if (!mbar_wait(&tfull[a], (ic / kAbuf) & 1u, abort, args.err)) break;
       tc_fence_after();
+      const uint32_t t_buf = t_lane + a * (2u * BN);
       for (int c = 0; c < it.nrows; c += 32) {
         float d0[32], d1[32];
-        tmem_ld_32x32b_x32(t_lane + (uint32_t)c, d0);
-        tmem_ld_32x32b_x32(t_lane + (uint32_t)(kGemmBN + c), d1);
+        tmem_ld_32x32b_x32(t_buf + (uint32_t)c, d0);
+        tmem_ld_32x32b_x32(t_buf + (uint32_t)(BN + c), d1);
         tmem_ld_wait();
         const int nn = min(32, it.nrows - c);
         uint16_t* o = args.out + (size_t)(it.row0 + c) * args.ld_out;
@@ -262,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty);
+      if (lane == 0) mbar_arrive(&tempty[a]);
     }
   }
 
@@ -277,53 +295,68 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t gemm_tc_setup() {
-  return cudaFuncSetAttribute(gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
+  cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       TileCfg<128>::kDynSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(gemm_bf16_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              TileCfg<256>::kDynSmem);
 }
 
-cudaError_t launch_gemm_tc(const LayerDims& d, int T, const TcWeights& w, Workspace& ws, int num_sms,
-                           cudaStream_t s, int which) {
-  if (T == 0) return cudaSuccess;
-  if (d.dtype != AFD_BF16) return cudaErrorNotSupported;
+template <int BN>
+static cudaError_t launch_bn(const LayerDims& d, int T, const TcWeights& w, Workspace& ws, int num_sms,
+                             cudaStream_t s, int which) {
   const int G = d.E + d.S;
   const long rows = (long)T * (d.k + d.S);
-  const long tiles_ub = rows / kGemmBN + G + 1;
-
+  const long tiles_ub = rows / BN + G + 1;
   TcArgs a{};
   a.counts = ws.counts;
   a.offsets = ws.offsets;
   a.tile_base = ws.tile_base;
   a.G = G;
   a.err = ws.err;
-
-  if (which == 0) {
-  // gate/up + SwiGLU: K = H, items of 128 intermediate channels
-  a.num_kb = d.H / 64;
-  a.MT = d.I / kGemmBM;
-  a.a_rows_per_group = d.I;
-  a.a_mt_stride = kGemmBM;
-  a.a1_offset = 0;
-  a.out = static_cast<uint16_t*>(ws.Hb);
-  a.ld_out = d.I;
-  a.mode = 0;
+  const CUtensorMap *m0, *m1, *mb;
+  if (which == 0) {  // gate/up + SwiGLU: K = H, items of 128 intermediate channels
+    a.num_kb = d.H / 64;
+    a.MT = d.I / kGemmBM;
+    a.a_rows_per_group = d.I;
+    a.a_mt_stride = kGemmBM;
+    a.a1_offset = 0;
+    a.out = static_cast<uint16_t*>(ws.Hb);
+    a.ld_out = d.I;
+    a.mode = 0;
+    m0 = w.tm_wg;
+    m1 = w.tm_wu;
+    mb = &ws.tm_P;
+  } else {  // down: K = I, items of 256 output columns (two 128-row MMAs)
+    a.num_kb = d.I / 64;
+    a.MT = d.H / (2 * kGemmBM);
+    a.a_rows_per_group = d.H;
+    a.a_mt_stride = 2 * kGemmBM;
+    a.a1_offset = kGemmBM;
+    a.out = static_cast<uint16_t*>(ws.Y);
+    a.ld_out = d.H;
+    a.mode = 1;
+    m0 = w.tm_wd;
+    m1 = w.tm_wd;
+    mb = &ws.tm_H;
+  }
   const long items_ub = tiles_ub * a.MT;
   const int grid = (int)(items_ub < num_sms ? items_ub : num_sms);
-  gemm_bf16_kernel<<<grid, kThreads, kDynSmem, s>>>(*w.tm_wg, *w.tm_wu, ws.tm_P, a);
+  gemm_bf16_kernel<BN><<<grid, kThreads, TileCfg<BN>::kDynSmem, s>>>(*m0, *m1, *mb, a);
   return cudaGetLastError();
-  }
+}
 
-  // down: K = I, items of 256 output columns (two 128-row MMAs)
-  a.num_kb = d.I / 64;
-  a.MT = d.H / (2 * kGemmBM);
-  a.a_rows_per_group = d.H;
-  a.a_mt_stride = 2 * kGemmBM;
-  a.a1_offset = kGemmBM;
-  a.out = static_cast<uint16_t*>(ws.Y);
-  a.ld_out = d.H;
-  a.mode = 1;
-  const long items_ub2 = tiles_ub * a.MT;
-  const int grid2 = (int)(items_ub2 < num_sms ? items_ub2 : num_sms);
-  gemm_bf16_kernel<<<grid2, kThreads, kDynSmem, s>>>(*w.tm_wd, *w.tm_wd, ws.tm_H, a);
-  return cudaGetLastError();
+int bf16_tile_tokens(const LayerDims& d, int T) {
+  // one pass over an expert's weights for its tokens when they are many
+  return (long)T * d.k > 112L * d.E ? 256 : 128;
+}
+
+cudaError_t launch_gemm_tc(const LayerDims& d, int T, const TcWeights& w, Workspace& ws, int num_sms,
+                           cudaStream_t s, int which) {
+  if (T == 0) return cudaSuccess;
+  if (d.dtype != AFD_BF16) return cudaErrorNotSupported;
+  return bf16_tile_tokens(d, T) == 256 ? launch_bn<256>(d, T, w, ws, num_sms, s, which)
+                                       : launch_bn<128>(d, T, w, ws, num_sms, s, which);
 }
 
 }  // namespace afd

@@ -164,7 +164,7 @@ cudaError_t launch_routing(const LayerDims& d, int T, Workspace& ws, cudaStream_
   if (T == 0) return cudaSuccess;
   const int G = d.E + d.S;
   size_t smem = sizeof(int) * ((size_t)kWarps * d.E + 2 * (G + 1));
-  const int bn = d.dtype == AFD_FP8_E4M3 ? kGemmBNFp8 : kGemmBN;  // tokens per GEMM tile
+  const int bn = d.dtype == AFD_FP8_E4M3 ? kGemmBNFp8 : bf16_tile_tokens(d, T);  // tokens per GEMM tile
   routing_kernel<<<1, kThreads, smem, s>>>(ws.topk_idx, T, d.k, d.E, d.S, bn, ws.counts, ws.offsets,
                                            ws.tile_base, ws.perm, ws.pos, ws.err);
   return cudaGetLastError();
