@@ -129,7 +129,8 @@ int alloc_workspace(afd_ffn* h, Workspace& ws) {
       (rc = dmalloc_t(h, &ws.logits, T * E)) ||
       (rc = dmalloc_t(h, &ws.tile_counter, (T + afd::kRouterTokTile - 1) / afd::kRouterTokTile)) ||
       (rc = dmalloc_t(h, &ws.counts, G)) || (rc = dmalloc_t(h, &ws.offsets, G + 1)) ||
-      (rc = dmalloc_t(h, &ws.tile_base, G + 1)) || (rc = dmalloc_t(h, &ws.perm, R)) ||
+      (rc = dmalloc_t(h, &ws.tile_base, G + 1)) || (rc = dmalloc_t(h, &ws.block_hist, ((T + 255) / 256) * E)) ||
+      (rc = dmalloc_t(h, &ws.perm, R)) ||
       (rc = dmalloc_t(h, &ws.pos, T * k)) || (rc = dmalloc(h, &ws.P, R * c.H * ab)) ||
       (rc = dmalloc(h, &ws.Hb, R * c.I * (c.dtype == AFD_FP8_E4M3 ? 1 : act_bytes(c)))) ||
       (rc = dmalloc(h, &ws.Y, R * c.H * yb)) || (rc = dmalloc_t(h, &ws.err, 1)))
@@ -152,7 +153,7 @@ int alloc_workspace(afd_ffn* h, Workspace& ws) {
 }
 
 void free_workspace(Workspace& ws) {
-  void* ptrs[] = {ws.topk_idx, ws.topk_w, ws.logits, ws.tile_counter, ws.counts, ws.offsets, ws.tile_base,
+  void* ptrs[] = {ws.topk_idx, ws.topk_w, ws.logits, ws.tile_counter, ws.counts, ws.offsets, ws.tile_base, ws.block_hist,
                   ws.perm, ws.pos, ws.P, ws.P_scale, ws.Hb, ws.H_scale, ws.Y, ws.err, ws.stage};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -540,7 +541,8 @@ int afd_ffn_profile_end(afd_ffn_t h, double* ms_per_kernel, int* n_forwards) {
   return AFD_OK;
 }
 
-int afd_ffn_launches_per_forward(afd_ffn_t h) { return h ? AFD_NUM_KERNELS : AFD_EINVAL; }
+// router, two routing-table kernels, pack, two GEMMs, combine
+int afd_ffn_launches_per_forward(afd_ffn_t h) { return h ? AFD_NUM_KERNELS + 1 : AFD_EINVAL; }
 
 const char* afd_ffn_last_error(afd_ffn_t h) { return h ? h->err.c_str() : "handle is NULL"; }
 

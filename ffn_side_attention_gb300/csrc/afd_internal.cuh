@@ -51,7 +51,8 @@ struct Workspace {
   int32_t* tile_counter = nullptr;  // [ceil(maxT/kRouterTokTile)]
   int32_t* counts = nullptr;    // [E+S]
   int32_t* offsets = nullptr;   // [E+S+1]
-  int32_t* tile_base = nullptr; // [E+S+1], prefix of ceil(counts/kGemmBN)
+  int32_t* tile_base = nullptr; // [E+S+1], prefix of ceil(counts / GEMM tile tokens)
+  int32_t* block_hist = nullptr; // [ceil(maxT/256)][E] per-block expert counts of the routing kernels
   int32_t* perm = nullptr;      // [max_rows] token of each packed row
   int32_t* pos = nullptr;       // [maxT*k]  packed row of each (t, j)
   float* row_w = nullptr;       // [max_rows] routing weight of each packed row

@@ -48,55 +48,60 @@ __device__ __forceinline__ int packed_rows(const int32_t* __restrict__ pos, int 
   return n;
 }
 
-// bf16 / fp32 layers: row copy, 16 bytes per lane step.
+// Work unit = (token, 512-byte chunk of its row): one warp, 16 bytes per lane;
+// units spread over the grid keep many rows' copies in flight at once.
+// bf16 / fp32 layers: row copy.
 __global__ void __launch_bounds__(256) pack_copy_kernel(SrcTable st, const int32_t* __restrict__ pos, int T, int k,
                                                         int S, int row_bytes, uint8_t* __restrict__ P) {
   const int lane = threadIdx.x & 31;
+  const int nchunk = (row_bytes + 511) >> 9;  // 512 bytes per warp step
   const int nvec = row_bytes >> 4;
-  for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < T; t += gridDim.x * 8) {
+  const long units = (long)T * nchunk;
+  for (long u = (long)blockIdx.x * 8 + (threadIdx.x >> 5); u < units; u += (long)gridDim.x * 8) {
+    const int t = (int)(u / nchunk), c = (int)(u - (long)t * nchunk);
+    const int v = c * 32 + lane;
+    if (v >= nvec) continue;
     int rows[kMaxCopies];
     const int n = packed_rows(pos, t, T, k, S, rows);
-    const uint4* s = reinterpret_cast<const uint4*>(src_row(st, t, row_bytes));
-    for (int v = lane; v < nvec; v += 32) {
-      const uint4 u = __ldg(s + v);
-      for (int c = 0; c < n; ++c) reinterpret_cast<uint4*>(P + (size_t)rows[c] * row_bytes)[v] = u;
-    }
+    const uint4 x = __ldg(reinterpret_cast<const uint4*>(src_row(st, t, row_bytes)) + v);
+    for (int q = 0; q < n; ++q) reinterpret_cast<uint4*>(P + (size_t)rows[q] * row_bytes)[v] = x;
   }
 }
 
 // fp8 layer: e4m3 codes + one fp32 scale per 128 channels, computed once per
-// token.  A 128-channel block is 16 lanes x 8 channels (one 16-byte load each).
+// token.  A 256-channel warp step holds two 128-channel blocks of 16 lanes.
 __global__ void __launch_bounds__(256) pack_fp8_kernel(SrcTable st, const int32_t* __restrict__ pos, int T, int k,
                                                        int S, int H, uint8_t* __restrict__ P,
                                                        float* __restrict__ P_scale) {
   const int lane = threadIdx.x & 31;
   const int nblk = H >> 7;
-  for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < T; t += gridDim.x * 8) {
+  const int nchunk = H >> 8;  // H % 256 == 0: whole warp active
+  const long units = (long)T * nchunk;
+  for (long u = (long)blockIdx.x * 8 + (threadIdx.x >> 5); u < units; u += (long)gridDim.x * 8) {
+    const int t = (int)(u / nchunk), c = (int)(u - (long)t * nchunk);
+    const int v = c * 32 + lane;
     int rows[kMaxCopies];
     const int n = packed_rows(pos, t, T, k, S, rows);
-    const uint4* s = reinterpret_cast<const uint4*>(src_row(st, t, (size_t)H * 2));
-    for (int v = lane; v < (H >> 3); v += 32) {  // H % 256 == 0: whole warp active
-      const uint4 u = __ldg(s + v);
-      const float x[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
-                          bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
-      float amax = 0.0f;
+    const uint4 x8 = __ldg(reinterpret_cast<const uint4*>(src_row(st, t, (size_t)H * 2)) + v);
+    const float x[8] = {bf16_lo(x8.x), bf16_hi(x8.x), bf16_lo(x8.y), bf16_hi(x8.y),
+                        bf16_lo(x8.z), bf16_hi(x8.z), bf16_lo(x8.w), bf16_hi(x8.w)};
+    float amax = 0.0f;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(x[q]));
+    for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(x[q]));
 #pragma unroll
-      for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      const float scale = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
-      uint2 q = make_uint2(0u, 0u);
-      if (amax != 0.0f) {
-        const uint32_t q01 = cvt_e4m3x2(__fdiv_rn(x[1], scale), __fdiv_rn(x[0], scale));
-        const uint32_t q23 = cvt_e4m3x2(__fdiv_rn(x[3], scale), __fdiv_rn(x[2], scale));
-        const uint32_t q45 = cvt_e4m3x2(__fdiv_rn(x[5], scale), __fdiv_rn(x[4], scale));
-        const uint32_t q67 = cvt_e4m3x2(__fdiv_rn(x[7], scale), __fdiv_rn(x[6], scale));
-        q = make_uint2(q01 | (q23 << 16), q45 | (q67 << 16));
-      }
-      for (int c = 0; c < n; ++c) {
-        reinterpret_cast<uint2*>(P + (size_t)rows[c] * H)[v] = q;
-        if ((lane & 15) == 0) P_scale[(size_t)rows[c] * nblk + (v >> 4)] = scale;
-      }
+    for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float scale = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+    uint2 q = make_uint2(0u, 0u);
+    if (amax != 0.0f) {
+      const uint32_t q01 = cvt_e4m3x2(__fdiv_rn(x[1], scale), __fdiv_rn(x[0], scale));
+      const uint32_t q23 = cvt_e4m3x2(__fdiv_rn(x[3], scale), __fdiv_rn(x[2], scale));
+      const uint32_t q45 = cvt_e4m3x2(__fdiv_rn(x[5], scale), __fdiv_rn(x[4], scale));
+      const uint32_t q67 = cvt_e4m3x2(__fdiv_rn(x[7], scale), __fdiv_rn(x[6], scale));
+      q = make_uint2(q01 | (q23 << 16), q45 | (q67 << 16));
+    }
+    for (int r = 0; r < n; ++r) {
+      reinterpret_cast<uint2*>(P + (size_t)rows[r] * H)[v] = q;
+      if ((lane & 15) == 0) P_scale[(size_t)rows[r] * nblk + (v >> 4)] = scale;
     }
   }
 }
@@ -106,8 +111,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&b);
 }
 
-// bf16 Y (bf16 / fp8 layers): one warp per token, 8 channels per lane step.
-// KC = k at compile time (0: runtime k) so the k row loads issue together.
+// bf16 Y (bf16 / fp8 layers): work unit = (token, 256-column chunk), one warp,
+// 8 channels per lane.  KC = k at compile time (0: runtime k) so the k row
+// loads of a unit are all in flight together.
 template <int KC>
 __global__ void __launch_bounds__(256) combine_bf16_kernel(SrcTable st, const int32_t* __restrict__ pos,
                                                            const float* __restrict__ topk_w,
@@ -115,30 +121,32 @@ __global__ void __launch_bounds__(256) combine_bf16_kernel(SrcTable st, const in
                                                            int H) {
   const int lane = threadIdx.x & 31;
   const int k = KC ? KC : k_rt;
-  for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < T; t += gridDim.x * 8) {
-    uint4* o = reinterpret_cast<uint4*>(out_row(st, t, (size_t)H * 2));
-    for (int v = lane; v < (H >> 3); v += 32) {
-      float acc[8];
+  const int nchunk = H >> 8;
+  const long units = (long)T * nchunk;
+  for (long u = (long)blockIdx.x * 8 + (threadIdx.x >> 5); u < units; u += (long)gridDim.x * 8) {
+    const int t = (int)(u / nchunk), c = (int)(u - (long)t * nchunk);
+    const int v = c * 32 + lane;
+    float acc[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+    for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
 #pragma unroll 8
-      for (int j = 0; j < k; ++j) {
-        int r = __ldg(pos + (size_t)t * k + j);
-        float w = __ldg(topk_w + (size_t)t * k + j);
-        uint4 u = __ldg(reinterpret_cast<const uint4*>(Y + (size_t)r * H) + v);
-        acc[0] = fmaf(w, bf16_lo(u.x), acc[0]); acc[1] = fmaf(w, bf16_hi(u.x), acc[1]);
-        acc[2] = fmaf(w, bf16_lo(u.y), acc[2]); acc[3] = fmaf(w, bf16_hi(u.y), acc[3]);
-        acc[4] = fmaf(w, bf16_lo(u.z), acc[4]); acc[5] = fmaf(w, bf16_hi(u.z), acc[5]);
-        acc[6] = fmaf(w, bf16_lo(u.w), acc[6]); acc[7] = fmaf(w, bf16_hi(u.w), acc[7]);
-      }
-      if (S) {
-        uint4 u = __ldg(reinterpret_cast<const uint4*>(Y + (size_t)(T * k + t) * H) + v);
-        acc[0] += bf16_lo(u.x); acc[1] += bf16_hi(u.x); acc[2] += bf16_lo(u.y); acc[3] += bf16_hi(u.y);
-        acc[4] += bf16_lo(u.z); acc[5] += bf16_hi(u.z); acc[6] += bf16_lo(u.w); acc[7] += bf16_hi(u.w);
-      }
-      o[v] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
-                        pack_bf16x2(acc[6], acc[7]));
+    for (int j = 0; j < k; ++j) {
+      const int r = __ldg(pos + (size_t)t * k + j);
+      const float w = __ldg(topk_w + (size_t)t * k + j);
+      const uint4 y = __ldg(reinterpret_cast<const uint4*>(Y + (size_t)r * H) + v);
+      acc[0] = fmaf(w, bf16_lo(y.x), acc[0]); acc[1] = fmaf(w, bf16_hi(y.x), acc[1]);
+      acc[2] = fmaf(w, bf16_lo(y.y), acc[2]); acc[3] = fmaf(w, bf16_hi(y.y), acc[3]);
+      acc[4] = fmaf(w, bf16_lo(y.z), acc[4]); acc[5] = fmaf(w, bf16_hi(y.z), acc[5]);
+      acc[6] = fmaf(w, bf16_lo(y.w), acc[6]); acc[7] = fmaf(w, bf16_hi(y.w), acc[7]);
     }
+    if (S) {
+      const uint4 y = __ldg(reinterpret_cast<const uint4*>(Y + (size_t)(T * k + t) * H) + v);
+      acc[0] += bf16_lo(y.x); acc[1] += bf16_hi(y.x); acc[2] += bf16_lo(y.y); acc[3] += bf16_hi(y.y);
+      acc[4] += bf16_lo(y.z); acc[5] += bf16_hi(y.z); acc[6] += bf16_lo(y.w); acc[7] += bf16_hi(y.w);
+    }
+    reinterpret_cast<uint4*>(out_row(st, t, (size_t)H * 2))[v] =
+        make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                   pack_bf16x2(acc[6], acc[7]));
   }
 }
 
@@ -169,7 +177,7 @@ __global__ void __launch_bounds__(256) combine_f32_kernel(SrcTable st, const int
 
 inline int grid_for(int rows_per_block_units, int units, int num_sms) {
   int want = (units + rows_per_block_units - 1) / rows_per_block_units;
-  int cap = num_sms * 8;
+  int cap = num_sms * 16;
   return want < cap ? (want > 0 ? want : 1) : cap;
 }
 
@@ -178,19 +186,19 @@ inline int grid_for(int rows_per_block_units, int units, int num_sms) {
 cudaError_t launch_pack(const SrcTable& st, const LayerDims& d, int T, Workspace& ws, int num_sms,
                         cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const int grid = grid_for(8, T, num_sms);
+  const int row_bytes = d.H * (d.dtype == AFD_FP32 ? 4 : 2);
+  const int grid = grid_for(8, T * ((row_bytes + 511) / 512), num_sms);
   if (d.dtype == AFD_FP8_E4M3)
     pack_fp8_kernel<<<grid, 256, 0, s>>>(st, ws.pos, T, d.k, d.S, d.H, static_cast<uint8_t*>(ws.P), ws.P_scale);
   else
-    pack_copy_kernel<<<grid, 256, 0, s>>>(st, ws.pos, T, d.k, d.S, d.H * (d.dtype == AFD_FP32 ? 4 : 2),
-                                          static_cast<uint8_t*>(ws.P));
+    pack_copy_kernel<<<grid, 256, 0, s>>>(st, ws.pos, T, d.k, d.S, row_bytes, static_cast<uint8_t*>(ws.P));
   return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const SrcTable& st, const LayerDims& d, int T, Workspace& ws, int num_sms,
                            cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const int grid = grid_for(8, T, num_sms);
+  const int grid = grid_for(8, d.dtype == AFD_FP32 ? T : T * (d.H / 256), num_sms);
   if (d.dtype == AFD_FP32)
     combine_f32_kernel<<<grid, 256, 0, s>>>(st, ws.pos, ws.topk_w, static_cast<const float*>(ws.Y), T, d.k, d.S,
                                             d.H);

@@ -16,98 +16,99 @@
 // T*k .. T*k+T-1.  tile_base[g] = sum over g' < g of ceil(counts[g'] / BN), the
 // GEMM work list (BN = tokens per GEMM tile).
 //
-// One CTA of 32 warps.  Entries are split into 32 contiguous segments, one
-// per warp, so segment order is entry order.  Pass 1: each warp counts its
-// segment per expert (match.any groups equal experts of a 32-entry step; the
-// group's lowest lane adds the group size).  A column scan over warps turns
-// the counts into per-warp bases, a scan over experts gives the offsets.
-// Pass 2 repeats the walk and gives each entry
-//   row = offsets[e] + base[warp][e] + (equal experts in earlier lanes),
-// which is exactly the stable (by token) counting-sort position.
+// Two launches, both one thread per token in blocks of 256 tokens:
+//   block_rank: per block, the per-expert counts (to a [blocks][E] array) and
+//     each entry's rank among the block's entries of the same expert, in
+//     token order.  A token's k experts are distinct, so that rank is the
+//     number of earlier tokens of the block that chose the expert: each warp
+//     sets bit `lane` of a per-expert word for every expert its token chose;
+//     the rank is the popcount of the lower lanes' bits plus the popcounts of
+//     the earlier warps' words.
+//   place: every block re-adds the block counts (totals, its own base per
+//     expert), scans them into offsets and tile bases, and writes
+//     pos = offsets[e] + base + rank and perm[pos] = token.
 #include "afd_internal.cuh"
 
 namespace afd {
 namespace {
 
-constexpr int kThreads = 1024;
-constexpr int kWarps = kThreads / 32;
-constexpr int kBatch = 16;  // 32-entry steps whose ids are loaded together
+constexpr int kTok = 256;                  // tokens per block (one per thread)
+constexpr int kWarpsPerBlock = kTok / 32;  // 8
+
+__global__ void __launch_bounds__(kTok) block_rank_kernel(const int32_t* __restrict__ idx, int T, int k, int E,
+                                                          int32_t* __restrict__ block_hist,
+                                                          int32_t* __restrict__ rank, int* err) {
+  extern __shared__ uint32_t bits[];  // [kWarpsPerBlock][E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kTok + threadIdx.x;
+  for (int i = threadIdx.x; i < kWarpsPerBlock * E; i += kTok) bits[i] = 0;
+  __syncthreads();
+  uint32_t* my = bits + warp * E;
+  if (t < T)
+    for (int j = 0; j < k; ++j) {
+      const int e = __ldg(idx + (size_t)t * k + j);
+      if (e < 0 || e >= E) {
+        atomicOr(err, kErrRange);
+        continue;
+      }
+      atomicOr(my + e, 1u << lane);
+    }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kTok) {
+    int total = 0;
+    for (int w = 0; w < kWarpsPerBlock; ++w) total += __popc(bits[w * E + e]);
+    block_hist[(size_t)blockIdx.x * E + e] = total;
+  }
+  if (t < T) {
+    const uint32_t lower = (1u << lane) - 1u;
+    for (int j = 0; j < k; ++j) {
+      const int e = __ldg(idx + (size_t)t * k + j);
+      if (e < 0 || e >= E) continue;
+      int r = __popc(my[e] & lower);
+      for (int w = 0; w < warp; ++w) r += __popc(bits[w * E + e]);
+      rank[(size_t)t * k + j] = r;
+    }
+  }
+}
 
 // inclusive scan of one value per lane
 __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int n = __shfl_up_sync(0xffffffffu, v, o);
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
     if (lane >= o) v += n;
   }
   return v;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    routing_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int S, int BN,
-                   int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ tile_base,
-                   int32_t* __restrict__ perm, int32_t* __restrict__ pos, int* err) {
-  extern __shared__ int smem[];
-  const int G = E + S;                 // groups (routed + shared)
-  int* hist = smem;                    // [kWarps][E]
-  int* s_off = smem + kWarps * E;      // [G + 1]
-  int* s_tb = s_off + G + 1;           // [G + 1]
+__global__ void __launch_bounds__(kTok)
+    place_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ block_hist, int nblocks, int T, int k,
+                 int E, int S, int BN, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                 int32_t* __restrict__ tile_base, int32_t* __restrict__ perm, int32_t* __restrict__ pos) {
+  __shared__ int s_cnt[kMaxExperts + 1], s_base[kMaxExperts], s_off[kMaxExperts + 1], s_tb[kMaxExperts + 1];
+  const int G = E + S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int N = T * k;
-  const int seg = ((N + kWarps * 32 - 1) / (kWarps * 32)) * 32;
-  const int beg = warp * seg, end = min(N, beg + seg);
-
-  for (int i = threadIdx.x; i < kWarps * E; i += kThreads) hist[i] = 0;
-  __syncthreads();
-
-  // pass 1: per-warp counts.  The expert ids of kBatch steps are loaded up
-  // front (independent loads in flight), then walked in order.
-  int* my = hist + warp * E;
-  for (int b0 = beg; b0 < end; b0 += 32 * kBatch) {
-    int ev[kBatch];
-#pragma unroll
-    for (int q = 0; q < kBatch; ++q) {
-      const int i = b0 + 32 * q + lane;
-      ev[q] = (i < end) ? __ldg(idx + i) : -1;
+  for (int e = threadIdx.x; e < E; e += kTok) {
+    int before = 0, total = 0;
+    for (int b = 0; b < nblocks; ++b) {
+      const int c = __ldg(block_hist + (size_t)b * E + e);
+      if (b < (int)blockIdx.x) before += c;
+      total += c;
     }
-#pragma unroll
-    for (int q = 0; q < kBatch; ++q) {
-      if (b0 + 32 * q >= end) break;
-      int e = ev[q];
-      if (e >= E || e < -1) {
-        atomicOr(err, kErrRange);
-        e = -1;
-      }
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
-      if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
-      __syncwarp();
-    }
-  }
-  __syncthreads();
-
-  // per-expert column scan over warps -> per-warp bases; totals -> counts
-  __shared__ int s_cnt[kMaxExperts + 1];
-  for (int e = threadIdx.x; e < E; e += kThreads) {
-    int run = 0;
-    for (int w = 0; w < kWarps; ++w) {
-      int c = hist[w * E + e];
-      hist[w * E + e] = run;
-      run += c;
-    }
-    s_cnt[e] = run;
+    s_cnt[e] = total;
+    s_base[e] = before;
   }
   if (threadIdx.x == 0 && S) s_cnt[E] = T;
   __syncthreads();
-
-  // exclusive scans over the groups: offsets and GEMM tile bases (warp 0)
+  // exclusive scans over the groups (warp 0): offsets and GEMM tile bases
   if (warp == 0) {
     int carry_o = 0, carry_t = 0;
     for (int g0 = 0; g0 < G; g0 += 32) {
-      int g = g0 + lane;
-      int c = (g < G) ? s_cnt[g] : 0;
-      int nt = (c + BN - 1) / BN;
-      int io = warp_incl_scan(c, lane);
-      int it = warp_incl_scan(nt, lane);
+      const int g = g0 + lane;
+      const int c = (g < G) ? s_cnt[g] : 0;
+      const int nt = (c + BN - 1) / BN;
+      const int io = warp_incl_scan(c, lane);
+      const int it = warp_incl_scan(nt, lane);
       if (g < G) {
         s_off[g] = carry_o + io - c;
         s_tb[g] = carry_t + it - nt;
@@ -121,52 +122,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  for (int g = threadIdx.x; g <= G; g += kThreads) {
-    offsets[g] = s_off[g];
-    tile_base[g] = s_tb[g];
-    if (g < G) counts[g] = s_cnt[g];
-  }
-
-  // pass 2: positions
-  for (int b0 = beg; b0 < end; b0 += 32 * kBatch) {
-    int ev[kBatch];
-#pragma unroll
-    for (int q = 0; q < kBatch; ++q) {
-      const int i = b0 + 32 * q + lane;
-      ev[q] = (i < end) ? __ldg(idx + i) : -1;
+  if (blockIdx.x == 0)
+    for (int g = threadIdx.x; g <= G; g += kTok) {
+      offsets[g] = s_off[g];
+      tile_base[g] = s_tb[g];
+      if (g < G) counts[g] = s_cnt[g];
     }
-#pragma unroll
-    for (int q = 0; q < kBatch; ++q) {
-      if (b0 + 32 * q >= end) break;
-      const int i = b0 + 32 * q + lane;
-      int e = ev[q];
-      if (e >= E || e < -1) e = -1;
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
-      if (e >= 0) {
-        const int rank = my[e] + __popc(peers & ((1u << lane) - 1u));
-        const int row = s_off[e] + rank;
-        perm[row] = i / k;
-        pos[i] = row;
-      }
-      __syncwarp();
-      if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
-      __syncwarp();
+  const int t = blockIdx.x * kTok + threadIdx.x;
+  if (t < T) {
+    for (int j = 0; j < k; ++j) {
+      const size_t i = (size_t)t * k + j;
+      const int e = __ldg(idx + i);
+      if (e < 0 || e >= E) continue;
+      const int row = s_off[e] + s_base[e] + pos[i];  // pos holds the in-block rank
+      pos[i] = row;
+      perm[row] = t;
     }
+    if (S) perm[(size_t)T * k + t] = t;
   }
-  // shared expert rows: token order
-  if (S)
-    for (int t = threadIdx.x; t < T; t += kThreads) perm[N + t] = t;
 }
 
 }  // namespace
 
 cudaError_t launch_routing(const LayerDims& d, int T, Workspace& ws, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const int G = d.E + d.S;
-  size_t smem = sizeof(int) * ((size_t)kWarps * d.E + 2 * (G + 1));
+  const int nblocks = (T + kTok - 1) / kTok;
   const int bn = d.dtype == AFD_FP8_E4M3 ? kGemmBNFp8 : bf16_tile_tokens(d, T);  // tokens per GEMM tile
-  routing_kernel<<<1, kThreads, smem, s>>>(ws.topk_idx, T, d.k, d.E, d.S, bn, ws.counts, ws.offsets,
-                                           ws.tile_base, ws.perm, ws.pos, ws.err);
+  block_rank_kernel<<<nblocks, kTok, sizeof(uint32_t) * kWarpsPerBlock * d.E, s>>>(ws.topk_idx, T, d.k, d.E,
+                                                                                  ws.block_hist, ws.pos, ws.err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  place_kernel<<<nblocks, kTok, 0, s>>>(ws.topk_idx, ws.block_hist, nblocks, T, d.k, d.E, d.S, bn, ws.counts,
+                                        ws.offsets, ws.tile_base, ws.perm, ws.pos);
   return cudaGetLastError();
 }
 
