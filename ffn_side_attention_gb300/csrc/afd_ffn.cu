@@ -31,6 +31,8 @@ struct afd_ffn {
   // weights in kernel layout
   void* wrT = nullptr;      // [E, H] router, K-major
   float* bias = nullptr;    // [E] or null
+  float* wnorm = nullptr;   // [E] ||w_e||_2 rounded up (bf16/fp8 router bound)
+  CUtensorMap tm_wr{};      // router weights for the tensor-core logits
   void* wgT = nullptr;      // gate, per group [I/128][H/KW][128][KW] (KW = 128 bytes of K)
   void* wuT = nullptr;      // up, same
   void* wdT = nullptr;      // down, per group [H/128][I/KW][128][KW]
@@ -139,13 +141,20 @@ int alloc_workspace(afd_ffn* h, Workspace& ws) {
     if ((rc = dmalloc_t(h, &ws.P_scale, R * (c.H / 128))) || (rc = dmalloc_t(h, &ws.H_scale, R * (c.I / 128))))
       return rc;
   }
+  if (c.dtype != AFD_FP32) {
+    if ((rc = dmalloc(h, &ws.Xc, T * c.H * 2)) || (rc = dmalloc_t(h, &ws.xnorm, T)) ||
+        (rc = dmalloc_t(h, &ws.rpart, (size_t)afd::kRouterMaxSplits * T * E)))
+      return rc;
+    CUDA_TRY(h, cudaMemset(ws.Xc, 0, T * c.H * 2));
+  }
   CUDA_TRY(h, cudaMemset(ws.tile_counter, 0, sizeof(int32_t) * ((T + afd::kRouterTokTile - 1) / afd::kRouterTokTile)));
   CUDA_TRY(h, cudaMemset(ws.err, 0, sizeof(int)));
   CUDA_TRY(h, cudaMemset(ws.P, 0, R * c.H * ab));
   CUDA_TRY(h, cudaMemset(ws.Hb, 0, R * c.I * (c.dtype == AFD_FP8_E4M3 ? 1 : act_bytes(c))));
   if (c.dtype != AFD_FP32) {
     const bool fp8 = c.dtype == AFD_FP8_E4M3;
-    if (!make_map(&ws.tm_P, ws.P, fp8, c.H, R, 32) || !make_map(&ws.tm_H, ws.Hb, fp8, c.I, R, 32))
+    if (!make_map(&ws.tm_P, ws.P, fp8, c.H, R, 32) || !make_map(&ws.tm_H, ws.Hb, fp8, c.I, R, 32) ||
+        !make_map(&ws.tm_X, ws.Xc, false, c.H, T, 128))
       return fail(h, AFD_ECUDA, "cuTensorMapEncodeTiled failed for a workspace operand");
   }
   ws.ready = true;
@@ -153,8 +162,9 @@ int alloc_workspace(afd_ffn* h, Workspace& ws) {
 }
 
 void free_workspace(Workspace& ws) {
-  void* ptrs[] = {ws.topk_idx, ws.topk_w, ws.logits, ws.tile_counter, ws.counts, ws.offsets, ws.tile_base, ws.block_hist,
-                  ws.perm, ws.pos, ws.P, ws.P_scale, ws.Hb, ws.H_scale, ws.Y, ws.err, ws.stage};
+  void* ptrs[] = {ws.topk_idx, ws.topk_w, ws.logits, ws.tile_counter, ws.counts, ws.offsets, ws.tile_base,
+                  ws.block_hist, ws.perm, ws.pos, ws.P, ws.P_scale, ws.Hb, ws.H_scale, ws.Y, ws.err,
+                  ws.stage, ws.Xc, ws.xnorm, ws.rpart};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   ws = Workspace{};
@@ -244,7 +254,10 @@ int run_layer(afd_ffn* h, const SrcTable& st, Workspace& ws, cudaStream_t s) {
   int rc;
   afd::TcWeights w{&h->tm_wg, &h->tm_wu, &h->tm_wd, h->sgT, h->suT, h->sdT};
   if ((rc = prof_mark(h, 0, s))) return rc;
-  CUDA_TRY(h, afd::launch_router(st, h->wrT, h->bias, d, ws, s));
+  if (d.dtype == AFD_FP32)
+    CUDA_TRY(h, afd::launch_router(st, h->wrT, h->bias, d, ws, s));
+  else
+    CUDA_TRY(h, afd::launch_router_tc(st, h->wrT, h->bias, h->wnorm, &h->tm_wr, d, ws, h->num_sms, s));
   if ((rc = prof_mark(h, 1, s))) return rc;
   CUDA_TRY(h, afd::launch_routing(d, T, ws, s));
   if ((rc = prof_mark(h, 2, s))) return rc;
@@ -280,6 +293,7 @@ int create_impl(const afd_ffn_config* cfg, const afd_ffn_weights* w, afd_ffn* h)
     if (!get_encoder()) return fail(h, AFD_ECUDA, "cuTensorMapEncodeTiled entry point unavailable");
     CUDA_TRY(h, afd::gemm_tc_setup());
     CUDA_TRY(h, afd::gemm_fp8_setup());
+    CUDA_TRY(h, afd::router_tc_setup());
   }
 
   const size_t H = c.H, I = c.I, E = c.E, S = c.n_shared, G = E + S;
@@ -290,6 +304,12 @@ int create_impl(const afd_ffn_config* cfg, const afd_ffn_weights* w, afd_ffn* h)
   // router: [H, E] -> [E, H]
   if ((rc = dmalloc(h, &h->wrT, E * H * ab))) return rc;
   CUDA_TRY(h, afd::launch_transpose(w->w_router, h->wrT, 1, (int)H, (int)E, (int)ab, s));
+  if (c.dtype != AFD_FP32) {
+    if ((rc = dmalloc_t(h, &h->wnorm, E))) return rc;
+    CUDA_TRY(h, afd::launch_router_wnorm(h->wrT, (int)H, (int)E, h->wnorm, s));
+    if (!make_map(&h->tm_wr, h->wrT, false, H, E, 128))
+      return fail(h, AFD_ECUDA, "cuTensorMapEncodeTiled failed for the router weights");
+  }
   if (w->router_bias) {
     if ((rc = dmalloc_t(h, &h->bias, E))) return rc;
     CUDA_TRY(h, cudaMemcpy(h->bias, w->router_bias, E * sizeof(float), cudaMemcpyDeviceToDevice));
@@ -541,8 +561,12 @@ int afd_ffn_profile_end(afd_ffn_t h, double* ms_per_kernel, int* n_forwards) {
   return AFD_OK;
 }
 
-// router, two routing-table kernels, pack, two GEMMs, combine
-int afd_ffn_launches_per_forward(afd_ffn_t h) { return h ? AFD_NUM_KERNELS + 1 : AFD_EINVAL; }
+// router (stage, tensor-core logits, select for bf16/fp8; one kernel for fp32),
+// two routing-table kernels, pack, two GEMMs, combine
+int afd_ffn_launches_per_forward(afd_ffn_t h) {
+  if (!h) return AFD_EINVAL;
+  return AFD_NUM_KERNELS + 1 + (h->cfg.dtype == AFD_FP32 ? 0 : 2);
+}
 
 const char* afd_ffn_last_error(afd_ffn_t h) { return h ? h->err.c_str() : "handle is NULL"; }
 
@@ -552,7 +576,7 @@ void afd_ffn_destroy(afd_ffn_t h) {
   if (!h) return;
   cudaDeviceSynchronize();
   for (auto& ws : h->ws) free_workspace(ws);
-  void* ptrs[] = {h->wrT, h->bias, h->wgT, h->wuT, h->wdT, h->sgT, h->suT, h->sdT, h->wg32, h->wu32, h->wd32};
+  void* ptrs[] = {h->wrT, h->bias, h->wnorm, h->wgT, h->wuT, h->wdT, h->sgT, h->suT, h->sdT, h->wg32, h->wu32, h->wd32};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   for (auto s : h->mstream)

@@ -18,6 +18,7 @@ constexpr int kGemmBN = 256;        // largest token tile of the bf16 GEMMs (MMA
 constexpr int kGemmBM = 128;        // weight rows per MMA (MMA M)
 constexpr int kGemmBNFp8 = 128;     // max tokens per fp8 GEMM tile
 constexpr int kMaxExperts = 257;    // routed + shared
+constexpr int kRouterMaxSplits = 8; // K splits of the tensor-core router logits
 
 // device error word bits
 constexpr int kErrTimeout = 1;
@@ -63,6 +64,10 @@ struct Workspace {
   void* Y = nullptr;            // [max_rows, H] weighted expert outputs
   int* err = nullptr;           // device error word
   void* stage = nullptr;        // forward_host staging: [maxT, H] in + [maxT, H] out
+  void* Xc = nullptr;           // [maxT, H] bf16 token rows, contiguous (tensor-core router)
+  float* xnorm = nullptr;       // [maxT] ||x_t||_2 rounded up
+  float* rpart = nullptr;       // [kRouterMaxSplits][maxT][E] router logit partials
+  CUtensorMap tm_X;
   int last_T = 0;
   CUtensorMap tm_P, tm_H;       // B operands of the two GEMMs
   bool ready = false;
@@ -76,6 +81,11 @@ struct LayerDims {
 cudaError_t launch_router(const SrcTable& st, const void* wrT, const float* bias, const LayerDims& d,
                           Workspace& ws, cudaStream_t s);
 cudaError_t router_setup();  // opt-in shared memory sizes (once per process)
+cudaError_t router_tc_setup();
+cudaError_t launch_router_wnorm(const void* wrT, int H, int E, float* wnorm, cudaStream_t s);
+cudaError_t launch_router_tc(const SrcTable& st, const void* wrT, const float* bias, const float* wnorm,
+                             const CUtensorMap* tm_wr, const LayerDims& d, Workspace& ws, int num_sms,
+                             cudaStream_t s);
 cudaError_t launch_routing(const LayerDims& d, int T, Workspace& ws, cudaStream_t s);
 cudaError_t launch_pack(const SrcTable& st, const LayerDims& d, int T, Workspace& ws, int num_sms,
                         cudaStream_t s);

@@ -1,0 +1,453 @@
+// router_tc.cu -- R1 for bf16/fp8 layers: the same top-k as the canonical
+// fp32 router (router.cu), with the bulk of the logits on the tensor cores.
+//
+// "MoE 大规模分布式推理工程实战", section 4.1: logits of a bias-free linear
+// gate (+ optional bias), top-k on the logits, softmax over the selected.
+//
+// The selection is defined by the canonical fp32 logits L (router.cu's order).
+// Computing all T*E of them on CUDA cores is most of the router's cost, but
+// only the experts near a token's k-th largest logit can change the answer:
+//   1. stage: the token rows are copied into one contiguous bf16 matrix X and
+//      ||x_t||_2 is computed per token (rounded up);
+//   2. logits: Lt = X . Wr on tcgen05 (bf16 in, fp32 accumulate), K split
+//      over CTAs into fp32 partials that are added in a fixed order;
+//   3. select (one warp per token): with b_e a bound on |Lt_e - L_e|, the
+//      canonical top-k is contained in C = {e : Lt_e + b_e >= m}, m = k-th
+//      largest of Lt - b (k experts have L >= m, and any e outside C has
+//      L_e <= Lt_e + b_e < m).  The canonical L is then computed for the
+//      candidates only (same order as router.cu), and the top-k and weights
+//      are taken from those exact values.  Over 64 candidates -> all experts.
+// Bound: |Lt - exact| + |L - exact| <= (g_tc + g_c) * sum_h |x_h w_h|, and
+// sum |x w| <= ||x|| ||w_e|| (Cauchy-Schwarz, both norms rounded up).
+// g_c = n u / (1 - n u), n = H/32 + 6, u = 2^-24 (the fp32 fma chain and fold);
+// g_tc = (H + splits + 2) * 2^-21: the tensor core multiplies bf16 values
+// exactly and is taken to lose at most 2^-21 relative per accumulation step
+// (fp32 accumulation with truncation loses at most 2^-23; the factor 4 is
+// margin).  Each side's bias addition adds 2^-24 |Lt| rounding, covered by an
+// extra 2^-22 (|Lt_e| + |bias_e|) + 2^-100.
+#include <cuda_bf16.h>
+
+#include "afd_internal.cuh"
+
+namespace afd {
+namespace {
+
+constexpr int kMaxK = 16;
+constexpr int kMaxCand = 64;
+
+// ---------------------------------------------------------------- 1. stage
+__global__ void __launch_bounds__(256) stage_x_kernel(SrcTable st, int H, uint16_t* __restrict__ Xc,
+                                                      float* __restrict__ xnorm) {
+  const int lane = threadIdx.x & 31;
+  for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < st.T; t += gridDim.x * 8) {
+    const int m = src_of_token(st, t);
+    const uint4* s = reinterpret_cast<const uint4*>(st.src[m]) + (size_t)(t - st.row0[m]) * (H >> 3);
+    uint4* d = reinterpret_cast<uint4*>(Xc) + (size_t)t * (H >> 3);
+    float ss = 0.0f;
+    for (int v = lane; v < (H >> 3); v += 32) {
+      const uint4 u = __ldg(s + v);
+      d[v] = u;
+      const float f[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
+                          bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
+#pragma unroll
+      for (int q = 0; q < 8; ++q) ss = fmaf(f[q], f[q], ss);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) xnorm[t] = sqrtf(ss) * (1.0f + 1.0f / 1024.0f);  // rounded up
+  }
+}
+
+// ---------------------------------------------------------------- 2. logits
+constexpr int kRBM = 128;                     // experts per MMA tile
+constexpr int kRBN = 128;                     // tokens per tile
+constexpr int kRStages = 4;
+constexpr int kRTile = 128 * 128;             // 16 KB: 128 rows x 64 bf16
+constexpr int kRStageBytes = 2 * kRTile;
+constexpr int kRDynSmem = kRStages * kRStageBytes + 1024;
+constexpr long long kRDrainCycles = 400000000ll;
+
+struct LogitArgs {
+  int T, E, num_kb, kb_per_split;
+  float* part;  // [splits][T][E]
+  int* err;
+};
+
+// CTA (n, m, s): tokens [128 n, +128), experts [128 m, +128), K blocks of split s.
+__global__ void __launch_bounds__(192, 1)
+    router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                            const LogitArgs args) {
+  extern __shared__ uint8_t dyn_smem[];
+  uint8_t* smem = dyn_smem + ((1024u - (smem_u32(dyn_smem) & 1023u)) & 1023u);
+  __shared__ __align__(8) uint64_t bars[2 * kRStages + 2];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kRStages;
+  uint64_t* tfull = bars + 2 * kRStages;
+  uint64_t* drain = tfull + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * kRBN, m0 = blockIdx.y * kRBM;
+  const int kb0 = blockIdx.z * args.kb_per_split;
+  const int nkb = min(args.kb_per_split, args.num_kb - kb0);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(drain, 1);
+    s_abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 1) {
+    tmem_alloc(&s_tmem, 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  volatile int* abort = &s_abort;
+  if (warp == 0 && lane == 0) {
+    int s = 0;
+    uint32_t ph = 0, filled = 0, fill_ph = 0;
+    bool ok = true;
+    for (int kb = 0; kb < nkb; ++kb) {
+      if (!mbar_wait(&empty[s], ph ^ 1u, abort, args.err)) {
+        ok = false;
+        break;
+      }
+      uint8_t* st = smem + s * kRStageBytes;
+      mbar_arrive_expect_tx(&full[s], 2 * kRTile);
+      tma_load_2d(st, &tmW, &full[s], (kb0 + kb) * 64, m0);
+      tma_load_2d(st + kRTile, &tmX, &full[s], (kb0 + kb) * 64, n0);
+      filled |= 1u << s;
+      fill_ph = (fill_ph & ~(1u << s)) | (ph << s);
+      if (++s == kRStages) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+    if (!ok)
+      for (int q = 0; q < kRStages; ++q)
+        if ((filled >> q) & 1u) mbar_wait_cycles(&full[q], (fill_ph >> q) & 1u, kRDrainCycles);
+  } else if (warp == 1 && lane == 0) {
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    const uint32_t idesc = mma_idesc(1u, kRBM, kRBN);
+    for (int kb = 0; kb < nkb; ++kb) {
+      if (!mbar_wait(&full[s], ph, abort, args.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint8_t* st = smem + s * kRStageBytes;
+      const uint64_t da = sw128_desc(st), db = sw128_desc(st + kRTile);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) mma_f16(tmem, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
+      tc_commit(&empty[s]);
+      if (++s == kRStages) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+    if (ok) tc_commit(tfull);
+    tc_commit(drain);
+    mbar_wait_cycles(drain, 0, kRDrainCycles);
+  } else if (warp >= 2) {
+    const int quad = warp & 3;
+    const int e = m0 + quad * 32 + lane;
+    if (nkb > 0 && mbar_wait(tfull, 0, abort, args.err)) {
+      tc_fence_after();
+      const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
+      float* out = args.part + (size_t)blockIdx.z * args.T * args.E;
+      for (int c = 0; c < kRBN && n0 + c < args.T; c += 32) {
+        float d[32];
+        tmem_ld_32x32b_x32(t_lane + (uint32_t)c, d);
+        tmem_ld_wait();
+        if (e < args.E) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (n0 + c + j < args.T) out[(size_t)(n0 + c + j) * args.E + e] = d[j];
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
+}
+
+// ---------------------------------------------------------------- 3. select
+__device__ __forceinline__ float fma_bf16_lo(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, al, bl, %3;\n\t}"
+      : "=f"(d)
+      : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fma_bf16_hi(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, ah, bh, %3;\n\t}"
+      : "=f"(d)
+      : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+
+// Canonical dot (router.cu's order): lane l runs the fma chain over chunks
+// l, l+32, ... of 8 channels, then the xor fold.  All lanes return the sum.
+__device__ __forceinline__ float canonical_dot_warp(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w,
+                                                    int H, int lane) {
+  float p = 0.0f;
+  for (int c = lane; c < (H >> 3); c += 32) {
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(x) + c);
+    const uint4 b = __ldg(reinterpret_cast<const uint4*>(w) + c);
+    p = fma_bf16_lo(a.x, b.x, p); p = fma_bf16_hi(a.x, b.x, p);
+    p = fma_bf16_lo(a.y, b.y, p); p = fma_bf16_hi(a.y, b.y, p);
+    p = fma_bf16_lo(a.z, b.z, p); p = fma_bf16_hi(a.z, b.z, p);
+    p = fma_bf16_lo(a.w, b.w, p); p = fma_bf16_hi(a.w, b.w, p);
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) p = p + __shfl_xor_sync(0xffffffffu, p, o);
+  return p;
+}
+
+__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+// warp-wide best (value desc, id asc) among this lane's untaken entries
+template <int PER>
+__device__ __forceinline__ void warp_best(const float (&v)[PER], const bool (&taken)[PER], int lane, float& bv,
+                                         int& bi) {
+  bv = 0.0f;
+  bi = 0x7fffffff;
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int e = lane + 32 * q;
+    if (!taken[q] && (bi == 0x7fffffff || ranks_before(v[q], e, bv, bi))) {
+      bv = v[q];
+      bi = e;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (oi != 0x7fffffff && (bi == 0x7fffffff || ranks_before(ov, oi, bv, bi))) {
+      bv = ov;
+      bi = oi;
+    }
+  }
+}
+
+struct SelectArgs {
+  const uint16_t* Xc;
+  const uint16_t* wrT;  // [E][H]
+  const float* wnorm;   // [E], rounded up
+  const float* xnorm;   // [T], rounded up
+  const float* bias;
+  const float* part;    // [splits][T][E]
+  int splits, T, H, E, k;
+  float g;              // g_tc + g_c
+  float* logits;
+  int32_t* topk_idx;
+  float* topk_w;
+};
+
+__global__ void __launch_bounds__(256) router_select_kernel(const SelectArgs a) {
+  constexpr int PER = (kMaxExperts + 31) / 32;  // 8 entries per lane for E <= 256
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= a.T) return;
+  const int E = a.E, k = a.k;
+  const uint16_t* x = a.Xc + (size_t)t * a.H;
+  const float xn = __ldg(a.xnorm + t);
+  float est[PER], lo[PER], hi[PER];  // estimate and its bounds
+  bool taken[PER];
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int e = lane + 32 * q;
+    taken[q] = e >= E;
+    est[q] = lo[q] = hi[q] = 0.0f;
+    if (e < E) {
+      float s = 0.0f;
+      for (int sp = 0; sp < a.splits; ++sp) s += __ldcg(a.part + ((size_t)sp * a.T + t) * E + e);
+      const float bs = a.bias ? __ldg(a.bias + e) : 0.0f;
+      if (a.bias) s = __fadd_rn(s, bs);
+      const float b = a.g * xn * __ldg(a.wnorm + e) + 0x1p-22f * (fabsf(s) + fabsf(bs)) + 0x1p-100f;
+      est[q] = s;
+      lo[q] = s - b;
+      hi[q] = s + b;
+    }
+  }
+  // m = k-th largest lower end
+  float m = 0.0f;
+  {
+    bool tk[PER];
+#pragma unroll
+    for (int q = 0; q < PER; ++q) tk[q] = taken[q];
+    for (int j = 0; j < k; ++j) {
+      float bv;
+      int bi;
+      warp_best<PER>(lo, tk, lane, bv, bi);
+      m = bv;
+#pragma unroll
+      for (int q = 0; q < PER; ++q)
+        if (lane + 32 * q == bi) tk[q] = true;
+    }
+  }
+  // candidates: upper end >= m
+  unsigned cmask[PER];
+  int ncand = 0;
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    cmask[q] = __ballot_sync(0xffffffffu, !taken[q] && hi[q] >= m);
+    ncand += __popc(cmask[q]);
+  }
+  const bool all = ncand > kMaxCand;
+  // canonical logits of the candidates (all experts when too many)
+  float lc[PER];
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    lc[q] = -INFINITY;
+    unsigned msk = all ? __ballot_sync(0xffffffffu, !taken[q]) : cmask[q];
+    while (msk) {
+      const int src = __ffs(msk) - 1;
+      msk &= msk - 1;
+      const int e = src + 32 * q;
+      float v = canonical_dot_warp(x, a.wrT + (size_t)e * a.H, a.H, lane);
+      if (a.bias) v = __fadd_rn(v, __ldg(a.bias + e));
+      if (lane == src) lc[q] = v;
+    }
+  }
+  // logits row for inspection: canonical where computed, tensor-core estimate elsewhere
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int e = lane + 32 * q;
+    if (e < E) {
+      const bool isc = all || ((cmask[q] >> lane) & 1u);
+      a.logits[(size_t)t * E + e] = isc ? lc[q] : est[q];
+    }
+  }
+  // top-k among the exact values (non-candidates are -inf and never win)
+  bool tk[PER];
+#pragma unroll
+  for (int q = 0; q < PER; ++q) tk[q] = taken[q] || !(all || ((cmask[q] >> lane) & 1u));
+  float sel_v[kMaxK];
+  int sel_i[kMaxK];
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    if (j >= k) break;
+    float bv;
+    int bi;
+    warp_best<PER>(lc, tk, lane, bv, bi);
+    sel_v[j] = bv;
+    sel_i[j] = bi;
+#pragma unroll
+    for (int q = 0; q < PER; ++q)
+      if (lane + 32 * q == bi) tk[q] = true;
+  }
+  if (lane == 0) {
+    float den = 0.0f, ex[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      if (j >= k) break;
+      ex[j] = expf(sel_v[j] - sel_v[0]);
+      den += ex[j];
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      if (j >= k) break;
+      a.topk_idx[(size_t)t * k + j] = sel_i[j];
+      a.topk_w[(size_t)t * k + j] = ex[j] / den;
+    }
+  }
+}
+
+__global__ void wnorm_kernel(const uint16_t* __restrict__ wrT, int H, int E, float* __restrict__ wnorm) {
+  const int lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (e >= E) return;
+  double ss = 0.0;
+  for (int h = lane; h < H; h += 32) {
+    const double v = (double)__uint_as_float((uint32_t)wrT[(size_t)e * H + h] << 16);
+    ss += v * v;
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if (lane == 0) wnorm[e] = (float)(sqrt(ss) * (1.0 + 1.0 / 1024.0));
+}
+
+}  // namespace
+
+cudaError_t router_tc_setup() {
+  return cudaFuncSetAttribute(router_logits_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRDynSmem);
+}
+
+cudaError_t launch_router_wnorm(const void* wrT, int H, int E, float* wnorm, cudaStream_t s) {
+  wnorm_kernel<<<(E + 7) / 8, 256, 0, s>>>(static_cast<const uint16_t*>(wrT), H, E, wnorm);
+  return cudaGetLastError();
+}
+
+int router_tc_splits(const LayerDims& d, int T, int num_sms) {
+  const int tiles = ((T + kRBN - 1) / kRBN) * ((d.E + kRBM - 1) / kRBM);
+  const int num_kb = d.H / 64;
+  int splits = (num_sms + tiles - 1) / tiles;
+  splits = splits < 1 ? 1 : splits;
+  const int max_splits = num_kb / 4 > 0 ? num_kb / 4 : 1;
+  if (splits > max_splits) splits = max_splits;
+  if (splits > kRouterMaxSplits) splits = kRouterMaxSplits;
+  return splits;
+}
+
+cudaError_t launch_router_tc(const SrcTable& st, const void* wrT, const float* bias, const float* wnorm,
+                             const CUtensorMap* tm_wr, const LayerDims& d, Workspace& ws, int num_sms,
+                             cudaStream_t s) {
+  const int T = st.T;
+  if (T == 0) return cudaSuccess;
+  stage_x_kernel<<<(T + 7) / 8, 256, 0, s>>>(st, d.H, static_cast<uint16_t*>(ws.Xc), ws.xnorm);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int splits = router_tc_splits(d, T, num_sms);
+  const int num_kb = d.H / 64;
+  LogitArgs la{T, d.E, num_kb, (num_kb + splits - 1) / splits, ws.rpart, ws.err};
+  const int nsplit = (num_kb + la.kb_per_split - 1) / la.kb_per_split;
+  dim3 grid((T + kRBN - 1) / kRBN, (d.E + kRBM - 1) / kRBM, nsplit);
+  router_logits_tc_kernel<<<grid, 192, kRDynSmem, s>>>(*tm_wr, ws.tm_X, la);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  SelectArgs sa{};
+  sa.Xc = static_cast<const uint16_t*>(ws.Xc);
+  sa.wrT = static_cast<const uint16_t*>(wrT);
+  sa.wnorm = wnorm;
+  sa.xnorm = ws.xnorm;
+  sa.bias = bias;
+  sa.part = ws.rpart;
+  sa.splits = nsplit;
+  sa.T = T;
+  sa.H = d.H;
+  sa.E = d.E;
+  sa.k = d.k;
+  const double u = 1.0 / 16777216.0;  // 2^-24
+  const double n = d.H / 32.0 + 6.0;
+  const double g_c = n * u / (1.0 - n * u);
+  const double g_tc = (d.H + nsplit + 2.0) * (1.0 / 2097152.0);  // 2^-21
+  sa.g = (float)((g_c + g_tc) * 1.0001);
+  sa.logits = ws.logits;
+  sa.topk_idx = ws.topk_idx;
+  sa.topk_w = ws.topk_w;
+  router_select_kernel<<<(T + 7) / 8, 256, 0, s>>>(sa);
+  return cudaGetLastError();
+}
+
+}  // namespace afd

@@ -155,6 +155,13 @@ int afd_ffn_forward_host(afd_ffn_t h, void* stream, const void* const* src_ptrs_
  *   (exclusive prefix sum, offsets[E] = T*k), perm_token [T*k] int32 (token of
  *   each packed row; rows of an expert in ascending token order), pos [T*k]
  *   int32 (packed row of each (token, slot)), logits [T*E] fp32.
+ * Logits: for AFD_FP32 every entry is the canonical fp32 dot product (plus
+ * bias).  For AFD_BF16 and AFD_FP8_E4M3 the router first estimates all
+ * logits on the tensor cores, then recomputes in the canonical order every
+ * expert whose estimate could reach the k-th largest once the estimate's
+ * error bound is taken into account; those entries (always including the k
+ * selected ones) hold the canonical value and the rest hold the estimate.
+ * The selection and the weights are therefore those of the canonical logits.
  * Enqueued on `stream`; T is the token count of that forward. */
 int afd_ffn_debug_routing(afd_ffn_t h, void* stream, int* topk_idx, float* topk_w, int* counts, int* offsets,
                           int* perm_token, int* pos, float* logits);
@@ -191,7 +198,8 @@ size_t afd_ffn_device_bytes(afd_ffn_t h);
  * reserves HBM for its KV cache) cannot cudaMalloc, and one inside a
  * latency-critical decode loop must not make an allocation call, which can
  * block or synchronise the device.  This computes exactly the routing of
- * afd_ffn_forward (same logits bit for bit, same top-k slots, same weights)
+ * afd_ffn_forward (same top-k slots and weights, both from the canonical
+ * fp32 logits, which this call computes for every expert)
  * without a handle and without allocating.
  *   src_ptrs_dev[m], src_counts_host[m], M  as afd_ffn_forward (16-byte
  *                    aligned rows of H activations, fp32 for AFD_FP32, bf16

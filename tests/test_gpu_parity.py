@@ -196,3 +196,27 @@ def test_step3_bf16_three_microbatches_sampled():
     torch.cuda.synchronize()
     for x, y in zip(outs, piped):
         assert torch.equal(x, y)
+
+
+def test_tensor_core_router_error_within_guard_band():
+    """The tensor-core logits that are not recomputed exactly must lie within
+    the bound the candidate rule assumes, with a wide margin (the model's
+    2^-21 per accumulation step is itself conservative)."""
+    c = synth.CONFIGS["qwen3_bf16"].with_batch(197, 2)
+    counts = [c.B] * c.M
+    layer, srcs, outs, r, ref = run_case(c, counts)
+    T, E = c.T, c.E
+    got = r["logits"].cpu().numpy().reshape(T, E).astype(np.float64)
+    exact = ref["logits"].astype(np.float64)
+    x = torch.cat([s.float() for s in srcs]).cpu().numpy().astype(np.float64)
+    w = synth.make_weights(c, "cuda")["w_router"].float().cpu().numpy().astype(np.float64)
+    xn = np.linalg.norm(x, axis=1) * (1 + 1 / 1024)
+    wn = np.linalg.norm(w, axis=0) * (1 + 1 / 1024)
+    u = 2.0 ** -24
+    n = c.H / 32 + 6
+    g = (n * u / (1 - n * u) + (c.H + 8 + 2) * 2.0 ** -21) * 1.0001
+    bound = g * xn[:, None] * wn[None, :]
+    est = got != exact  # entries holding the tensor-core estimate
+    assert est.sum() > T * (E - 3 * c.k)  # most entries are estimates
+    ratio = np.abs(got - exact)[est] / bound[est]
+    assert ratio.max() < 1 / 16, f"tensor-core error reached {ratio.max():.3f} of the guard band"
