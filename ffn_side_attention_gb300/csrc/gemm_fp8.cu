@@ -6,24 +6,32 @@
 // 3.3: FP8 activations).  Weights carry one fp32 scale per 128x128 block,
 // activations one per token per 128 channels, so the product of one 128-wide
 // K block is
-//     sW[m-block, kb] * sA[token, kb] * sum_{k in kb} qW[m, k] * qA[token, k]
+//     sA[token, kb] * sW[n-block, kb] * sum_{k in kb} qA[token, k] * qW[n, k]
 // and the result is the sum of those over kb.  The tensor core computes the
-// inner sums; the scales are applied in fp32 ("promotion"):
-//   * one pipeline stage = one K block (128 bytes of e4m3 per row);
-//   * the MMA writes each block's partial into one of two TMEM buffers
-//     (ping-pong), accumulating only inside the block;
-//   * eight epilogue warps read the partial, multiply by sW * sA[token] and
-//     add it to fp32 accumulators held in registers (warp w covers TMEM lanes
-//     32*(w%4) .. +31 and half of the 128 token columns); the producer
-//     warpgroup gives registers up (setmaxnreg) so the 128 accumulators of an
-//     epilogue thread stay in registers;
-//   * after the last block: gate/up -> h = silu(G) * U, re-quantised per token
-//     per 128 channels of I (scale = amax/448, e4m3 RNE, saturating); down ->
-//     Y in bf16.
-// Tiles: 128 weight rows per MMA (two accumulators: gate+up, or two halves of
-// 256 down rows), up to 128 tokens per tile; TMEM = 2 buffers x 2 accumulators
-// x 128 columns.  TMA ring of 4 stages x 48 KB.  Same device-side work list,
-// persistent CTAs and bounded waits as the bf16 kernel.
+// inner sums; the scales are applied in fp32 ("promotion").
+//
+// Operands: the expert's tokens are the MMA's M side (128 TMEM lanes, one
+// token per lane) and 256 weight rows its N side (gate/up: 128 rows of W_gate
+// then the same 128 rows of W_up; down: 256 rows of W_down).  One token per
+// lane makes the scale of a K block one scalar per thread,
+// sA[token] * sW[block], and puts a token's gate and up values in the same
+// thread, so SwiGLU and the per-token re-quantisation need no exchange.
+//   * one pipeline stage = one K block: 128 token rows x 128 bytes (TMA boxes
+//     of 32 rows, only as many as the tile has tokens) and two 16 KB weight
+//     tiles, adjacent in shared memory so one descriptor spans all 256 rows;
+//   * the MMA writes each block's 128 x 256 partial into one of two TMEM
+//     buffers (ping-pong), accumulating only inside the block;
+//   * eight epilogue warps (warp w reads TMEM lanes 32*(w%4) .. +31 and one
+//     half of each 128-column block) read the partial and add it, times the
+//     thread's scale, to fp32 accumulators in registers with packed fp32x2
+//     FMAs; warps whose lanes hold no token skip the math;
+//   * after the last block: gate/up -> h = silu(G) * U, re-quantised per
+//     token per 128 channels of I (scale = amax/448, e4m3 RNE, saturating);
+//     down -> Y in bf16.  Each thread stores contiguous 16-byte runs of its
+//     token's row.
+// TMA ring of 4 stages x 48 KB.  Same device-side work list, persistent CTAs
+// and bounded waits as the bf16 kernel; the producer warpgroup gives
+// registers up (setmaxnreg) for the epilogue's 128 accumulators.
 #include <cuda_bf16.h>
 
 #include "afd_internal.cuh"
@@ -31,13 +39,14 @@
 namespace afd {
 namespace {
 
-constexpr int kBN = kGemmBNFp8;                   // 128 tokens per tile
+constexpr int kBM = kGemmBNFp8;                    // 128 tokens per tile = MMA M = TMEM lanes
+constexpr int kBN = 2 * kGemmBM;                     // 256 weight rows per item = MMA N
 constexpr int kStages = 4;
-constexpr int kRowBytes = 128;                    // one K block of e4m3
-constexpr int kATile = kGemmBM * kRowBytes;       // 16 KB
-constexpr int kBTile = kBN * kRowBytes;           // 16 KB
-constexpr int kBBoxRows = 32;
-constexpr int kStageBytes = 2 * kATile + kBTile;  // 48 KB
+constexpr int kRowBytes = 128;                       // one K block of e4m3
+constexpr int kWTile = kGemmBM * kRowBytes;          // 16 KB: 128 weight rows
+constexpr int kXTile = kBM * kRowBytes;              // 16 KB: 128 token rows
+constexpr int kXBoxRows = 32;
+constexpr int kStageBytes = kXTile + 2 * kWTile;     // 48 KB
 constexpr int kDynSmem = kStages * kStageBytes + 1024;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 128 + 32 * kEpiWarps;  // 384: warpgroup 0 = producer, MMA, 2 idle; 1-2 = epilogue
@@ -56,14 +65,14 @@ struct Fp8Args {
   const int32_t* tile_base;
   int G;
   int num_kb;            // K / 128
-  int MT;                // m tiles per group
-  int a_rows_per_group;
-  int a_mt_stride;
-  int a1_offset;
-  const float* sA0;      // weight block scales of A0: [G][a_rows_per_group/128][num_kb]
-  const float* sA1;
-  int sa1_block_offset;  // A1's 128-row block relative to A0's (0: own scale array; 1: next block)
-  const float* sB;       // activation scales [rows][num_kb]
+  int MT;                // weight-row items per group (256 rows each)
+  int w_rows_per_group;  // weight rows of one group
+  int w_mt_stride;       // weight rows between consecutive items of a group
+  int w1_offset;         // rows of W1's block relative to W0's (0: separate matrix)
+  const float* sW0;      // weight block scales of W0: [G][w_rows_per_group/128][num_kb]
+  const float* sW1;
+  int sw1_block_offset;  // W1's 128-row block relative to W0's (0: own scale array; 1: next block)
+  const float* sX;       // activation scales [rows][num_kb]
   void* out;             // mode 0: e4m3 codes [rows][ld_out]; mode 1: bf16 [rows][ld_out]
   float* out_scale;      // mode 0: [rows][ld_out/128]
   int ld_out;
@@ -87,25 +96,29 @@ __device__ __forceinline__ Item decode_item(int item, int MT, int G, const int* 
   const int local = item - MT * tb[lo];
   it.mt = local / nt_g;
   const int nt = local - it.mt * nt_g;
-  it.row0 = off[lo] + nt * kBN;
-  it.nrows = min(kBN, cnt[lo] - nt * kBN);
+  it.row0 = off[lo] + nt * kBM;
+  it.nrows = min(kBM, cnt[lo] - nt * kBM);
   return it;
 }
 
-__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, float* v) {
-  uint32_t* r = reinterpret_cast<uint32_t*>(v);
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
+// Packed fp32 pairs (sm_100 family): c += s * p for two lanes of a pair in
+// one instruction, each an IEEE round-to-nearest fused multiply-add.
+__device__ __forceinline__ uint64_t pack2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
 }
-
-__device__ __forceinline__ uint8_t cvt_e4m3(float v) {
+__device__ __forceinline__ void fma2(float& c0, float& c1, uint64_t s2, float p0, float p1) {
+  asm("{\n .reg .b64 rp, rc;\n mov.b64 rp, {%3, %4};\n mov.b64 rc, {%0, %1};\n"
+      " fma.rn.f32x2 rc, %2, rp, rc;\n mov.b64 {%0, %1}, rc;\n}"
+      : "+f"(c0), "+f"(c1)
+      : "l"(s2), "f"(p0), "f"(p1));
+}
+// two e4m3 codes (RNE, saturating): v0 in the low byte, v1 in the high byte
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float v0, float v1) {
   uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
-  return (uint8_t)(r & 0xff);
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(v1), "f"(v0));
+  return r;
 }
 
 __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow)); }
@@ -123,8 +136,8 @@ __device__ __forceinline__ bool epi_sync(uint64_t* bar, uint32_t& phase, int lan
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
-                    const __grid_constant__ CUtensorMap tmB, const Fp8Args args) {
+    gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1,
+                    const __grid_constant__ CUtensorMap tmX, const Fp8Args args) {
   extern __shared__ uint8_t dyn_smem[];
   uint8_t* smem = dyn_smem + ((1024u - (smem_u32(dyn_smem) & 1023u)) & 1023u);
 
@@ -132,9 +145,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_tb[kMaxExperts + 1], s_off[kMaxExperts + 1], s_cnt[kMaxExperts];
-  __shared__ float s_red[2][4][64];  // per column half, quadrant, column: |h| maxima
-  __shared__ __align__(16) float s_sc[kMaxKb][kBN];  // this item's activation scales, [kb][token column]
-  __shared__ float s_w[2][kMaxKb];                   // this item's weight block scales (A0, A1)
+  __shared__ float s_red[2][kBM];                    // per column half, token: |h| maxima
+  __shared__ __align__(16) float s_sc[kMaxKb][kBM];  // this item's activation scales, [kb][token]
+  __shared__ float s_w[2][kMaxKb];                   // this item's weight block scales (W0, W1)
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* pfull = bars + 2 * kStages;       // [2] MMA -> epilogue
@@ -162,9 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(ebar, kEpiWarps);
     s_abort = 0;
     fence_mbar_init();
-    tma_prefetch_desc(&tmA0);
-    tma_prefetch_desc(&tmA1);
-    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmW0);
+    tma_prefetch_desc(&tmW1);
+    tma_prefetch_desc(&tmX);
   }
   if (warp == 1) {
     tmem_alloc(&s_tmem, kTmemCols);
@@ -182,17 +195,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
       // ---------------- TMA producer
       const uint64_t pol_w = l2_policy_evict_first();
-      const uint64_t pol_b = l2_policy_evict_last();
+      const uint64_t pol_x = l2_policy_evict_last();
       int s = 0;
       uint32_t ph = 0, filled = 0, fill_ph = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
         const Item it = decode_item(item, args.MT, G, s_tb, s_off, s_cnt);
         // tiled weights: tile (row block rb, K block kb) starts at tile row (rb * num_kb + kb) * 128
-        const int rb0 = it.g * (args.a_rows_per_group / 128) + it.mt * (args.a_mt_stride / 128);
-        const int rb1 = rb0 + args.a1_offset / 128;
-        const int nbox = (it.nrows + kBBoxRows - 1) / kBBoxRows;
-        const uint32_t bytes = 2 * kATile + nbox * kBBoxRows * kRowBytes;
+        const int rb0 = it.g * (args.w_rows_per_group / 128) + it.mt * (args.w_mt_stride / 128);
+        const int rb1 = rb0 + args.w1_offset / 128;
+        const int nbox = (it.nrows + kXBoxRows - 1) / kXBoxRows;
+        const uint32_t bytes = 2 * kWTile + nbox * kXBoxRows * kRowBytes;
         for (int kb = 0; kb < args.num_kb; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u, abort, args.err)) {
             ok = false;
@@ -200,11 +213,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* st = smem + s * kStageBytes;
           mbar_arrive_expect_tx(&full[s], bytes);
-          tma_load_2d_hint(st, &tmA0, &full[s], 0, (rb0 * args.num_kb + kb) * 128, pol_w);
-          tma_load_2d_hint(st + kATile, &tmA1, &full[s], 0, (rb1 * args.num_kb + kb) * 128, pol_w);
           for (int b = 0; b < nbox; ++b)
-            tma_load_2d_hint(st + 2 * kATile + b * kBBoxRows * kRowBytes, &tmB, &full[s], kb * 128,
-                             it.row0 + b * kBBoxRows, pol_b);
+            tma_load_2d_hint(st + b * kXBoxRows * kRowBytes, &tmX, &full[s], kb * 128, it.row0 + b * kXBoxRows,
+                             pol_x);
+          tma_load_2d_hint(st + kXTile, &tmW0, &full[s], 0, (rb0 * args.num_kb + kb) * 128, pol_w);
+          tma_load_2d_hint(st + kXTile + kWTile, &tmW1, &full[s], 0, (rb1 * args.num_kb + kb) * 128, pol_w);
           filled |= 1u << s;
           fill_ph = (fill_ph & ~(1u << s)) | (ph << s);
           if (++s == kStages) {
@@ -217,14 +230,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < kStages; ++q)
           if ((filled >> q) & 1u) mbar_wait_cycles(&full[q], (fill_ph >> q) & 1u, kDrainCycles);
     } else if (warp == 1 && lane == 0) {
-      // ---------------- MMA issuer: one fresh partial per K block
+      // ---------------- MMA issuer: one fresh 128 x 256 partial per K block
+      const uint32_t idesc = mma_idesc(0u, kBM, kBN);  // e4m3 x e4m3 -> f32, M = tokens, N = weight rows
       int s = 0;
       uint32_t ph = 0, gstep = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
-        const Item it = decode_item(item, args.MT, G, s_tb, s_off, s_cnt);
-        const int N = (it.nrows + 15) & ~15;
-        const uint32_t idesc = mma_idesc(0u, kGemmBM, N);  // e4m3 x e4m3 -> f32
         for (int kb = 0; kb < args.num_kb; ++kb, ++gstep) {
           const uint32_t b = gstep & 1u, use = gstep >> 1;
           if (!mbar_wait(&pempty[b], (use & 1u) ^ 1u, abort, args.err) ||
@@ -234,13 +245,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           uint8_t* st = smem + s * kStageBytes;
-          const uint64_t da0 = sw128_desc(st), da1 = sw128_desc(st + kATile), db = sw128_desc(st + 2 * kATile);
-          const uint32_t d0 = tmem + b * 256u, d1 = d0 + 128u;
+          const uint64_t dx = sw128_desc(st), dw = sw128_desc(st + kXTile);
+          const uint32_t d = tmem + b * (uint32_t)kBN;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {  // 4 x K=32 per 128-byte block
-            mma_f8(d0, da0 + 2 * kk, db + 2 * kk, idesc, kk ? 1u : 0u);
-            mma_f8(d1, da1 + 2 * kk, db + 2 * kk, idesc, kk ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 4; ++kk)  // 4 x K=32 per 128-byte block
+            mma_f8(d, dx + 2 * kk, dw + 2 * kk, idesc, kk ? 1u : 0u);
           tc_commit(&empty[s]);
           tc_commit(&pfull[b]);
           if (++s == kStages) {
@@ -257,31 +266,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- epilogue: warps 4..11
     const int ew = warp - 4;
     const int quad = warp & 3, half = ew >> 2;
-    const int r = quad * 32 + lane;  // row of the 128-row tile
-    const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
+    const int r = quad * 32 + lane;  // token (TMEM lane) of the 128-token tile
+    const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * 64);
     uint32_t gstep = 0, ephase = 0;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
       const Item it = decode_item(item, args.MT, G, s_tb, s_off, s_cnt);
-      const int c0 = half * 64;
-      const int nc = max(0, min(64, it.nrows - c0));  // this warp's columns
       const int nkb = args.num_kb;
+      const bool active = quad * 32 < it.nrows;  // some lane of this warp holds a token
       // stage the item's scales in shared memory (the previous item is done with them)
       if (!epi_sync(ebar, ephase, lane, abort, args.err)) break;
       {
-        const size_t blk0 = (size_t)it.g * (args.a_rows_per_group / 128) + it.mt * (args.a_mt_stride / 128);
-        const float* sB = args.sB + (size_t)it.row0 * nkb;  // rows row0 .. row0+nrows-1 are contiguous
+        const size_t blk0 = (size_t)it.g * (args.w_rows_per_group / 128) + it.mt * (args.w_mt_stride / 128);
+        const float* sX = args.sX + (size_t)it.row0 * nkb;  // rows row0 .. row0+nrows-1 are contiguous
         for (int q = ew * 32 + lane; q < it.nrows * nkb; q += 32 * kEpiWarps) {
-          const int col = q / nkb, kb = q - col * nkb;
-          s_sc[kb][col] = __ldg(sB + q);
+          const int tok = q / nkb, kb = q - tok * nkb;
+          s_sc[kb][tok] = __ldg(sX + q);
         }
         for (int q = ew * 32 + lane; q < 2 * nkb; q += 32 * kEpiWarps) {
           const int which = q / nkb, kb = q - which * nkb;
-          s_w[which][kb] = __ldg((which ? args.sA1 + (blk0 + args.sa1_block_offset) * nkb : args.sA0 + blk0 * nkb) + kb);
+          s_w[which][kb] =
+              __ldg((which ? args.sW1 + (blk0 + args.sw1_block_offset) * nkb : args.sW0 + blk0 * nkb) + kb);
         }
       }
       if (!epi_sync(ebar, ephase, lane, abort, args.err)) break;
-      float acc0[64], acc1[64];
+      float acc0[64], acc1[64];  // columns half*64 + j of weight rows 0..127 and 128..255
 #pragma unroll
       for (int j = 0; j < 64; ++j) acc0[j] = acc1[j] = 0.0f;
       for (int kb = 0; kb < nkb; ++kb, ++gstep) {
@@ -291,28 +300,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const float w0 = s_w[0][kb], w1 = s_w[1][kb];
+        if (active) {
+          const float sx = s_sc[kb][r];
+          const uint64_t s0 = pack2(sx * s_w[0][kb], sx * s_w[0][kb]);
+          const uint64_t s1 = pack2(sx * s_w[1][kb], sx * s_w[1][kb]);
 #pragma unroll
-        for (int cc = 0; cc < 64; cc += 32) {
-          if (cc < nc) {
+          for (int cc = 0; cc < 64; cc += 32) {
             float p0[32], p1[32];
-            const uint32_t col = t_lane + b * 256u + (uint32_t)(c0 + cc);
-            tmem_ld_x16(col, p0);
-            tmem_ld_x16(col + 16u, p0 + 16);
-            tmem_ld_x16(col + 128u, p1);
-            tmem_ld_x16(col + 144u, p1 + 16);
+            const uint32_t col = t_lane + b * (uint32_t)kBN + (uint32_t)cc;
+            tmem_ld_32x32b_x32(col, p0);
+            tmem_ld_32x32b_x32(col + 128u, p1);
             tmem_ld_wait();
-            const float4* sc4 = reinterpret_cast<const float4*>(&s_sc[kb][c0 + cc]);
 #pragma unroll
-            for (int j4 = 0; j4 < 8; ++j4) {
-              const float4 sa = sc4[j4];
-              const float sv[4] = {sa.x, sa.y, sa.z, sa.w};
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int j = 4 * j4 + u;
-                acc0[cc + j] = fmaf(w0 * sv[u], p0[j], acc0[cc + j]);
-                acc1[cc + j] = fmaf(w1 * sv[u], p1[j], acc1[cc + j]);
-              }
+            for (int j = 0; j < 32; j += 2) {
+              fma2(acc0[cc + j], acc0[cc + j + 1], s0, p0[j], p0[j + 1]);
+              fma2(acc1[cc + j], acc1[cc + j + 1], s1, p1[j], p1[j + 1]);
             }
           }
         }
@@ -321,47 +323,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&pempty[b]);
       }
       if (!ok) break;
-      // ---- item epilogue
+      // ---- item epilogue (this thread: token row0 + r, 64 columns of each block)
+      const bool mine = r < it.nrows;
+      const size_t row = (size_t)(it.row0 + r);
       if (args.mode == 0) {
-        // h = silu(G) * U, then e4m3 per token per 128 channels (this tile's rows)
+        // h = silu(G) * U, then e4m3 per token per 128 channels of I (this item's channels)
+        float amax = 0.0f;
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
           const float g = acc0[j];
           acc0[j] = g / (1.0f + expf(-g)) * acc1[j];
+          amax = fmaxf(amax, fabsf(acc0[j]));
         }
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          float a = fabsf(acc0[j]);
-#pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-          if (lane == 0) s_red[half][quad][j] = a;
-        }
+        s_red[half][r] = amax;
         if (!epi_sync(ebar, ephase, lane, abort, args.err)) break;
-        uint8_t* outq = static_cast<uint8_t*>(args.out);
-        const int nblk = args.ld_out / 128;
+        if (mine) {
+          const float am = fmaxf(s_red[0][r], s_red[1][r]);
+          const float sc = am == 0.0f ? 1.0f : __fdiv_rn(am, 448.0f);
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(args.out) + row * args.ld_out + it.mt * 128 +
+                                                half * 64);
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          if (j < nc) {
-            const float amax = fmaxf(fmaxf(s_red[half][0][j], s_red[half][1][j]),
-                                     fmaxf(s_red[half][2][j], s_red[half][3][j]));
-            const float sc = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
-            const size_t row = (size_t)(it.row0 + c0 + j);
-            outq[row * args.ld_out + it.mt * 128 + r] =
-                amax == 0.0f ? (uint8_t)0 : cvt_e4m3(__fdiv_rn(acc0[j], sc));
-            if (r == 0) args.out_scale[row * nblk + it.mt] = sc;
+          for (int v = 0; v < 4; ++v) {
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int j = 16 * v + 4 * q;
+              const uint32_t lo = am == 0.0f ? 0u : cvt_e4m3x2(__fdiv_rn(acc0[j], sc), __fdiv_rn(acc0[j + 1], sc));
+              const uint32_t hi =
+                  am == 0.0f ? 0u : cvt_e4m3x2(__fdiv_rn(acc0[j + 2], sc), __fdiv_rn(acc0[j + 3], sc));
+              w[q] = lo | (hi << 16);
+            }
+            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
           }
+          if (half == 0) args.out_scale[row * (args.ld_out / 128) + it.mt] = sc;
         }
         // s_red is reused by the next item: the sync at the next item's start orders it
-      } else {
-        uint16_t* outy = static_cast<uint16_t*>(args.out);
-        const int col = it.mt * 2 * kGemmBM + r;
+      } else if (mine) {
+        uint16_t* yrow = static_cast<uint16_t*>(args.out) + row * args.ld_out + it.mt * kBN + half * 64;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          if (j < nc) {
-            const size_t row = (size_t)(it.row0 + c0 + j);
-            __nv_bfloat16 y0 = __float2bfloat16_rn(acc0[j]), y1 = __float2bfloat16_rn(acc1[j]);
-            outy[row * args.ld_out + col] = *reinterpret_cast<uint16_t*>(&y0);
-            outy[row * args.ld_out + col + kGemmBM] = *reinterpret_cast<uint16_t*>(&y1);
+        for (int part = 0; part < 2; ++part) {
+          const float* acc = part ? acc1 : acc0;
+          uint4* dst = reinterpret_cast<uint4*>(yrow + part * 128);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const __nv_bfloat162 y = __floats2bfloat162_rn(acc[8 * v + 2 * q], acc[8 * v + 2 * q + 1]);
+              w[q] = *reinterpret_cast<const uint32_t*>(&y);
+            }
+            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
       }
@@ -393,23 +404,23 @@ cudaError_t launch_gemm_fp8(const LayerDims& d, int T, const TcWeights& w, Works
   if (T == 0) return cudaSuccess;
   const int G = d.E + d.S;
   const long rows = (long)T * (d.k + d.S);
-  const long tiles_ub = rows / kBN + G + 1;
+  const long tiles_ub = rows / kBM + G + 1;
   Fp8Args a{};
   a.counts = ws.counts;
   a.offsets = ws.offsets;
   a.tile_base = ws.tile_base;
   a.G = G;
   a.err = ws.err;
-  if (which == 0) {  // gate/up + SwiGLU + e4m3 h: K = H
+  if (which == 0) {  // gate/up + SwiGLU + e4m3 h: K = H, items of 128 channels of I
     a.num_kb = d.H / 128;
     a.MT = d.I / kGemmBM;
-    a.a_rows_per_group = d.I;
-    a.a_mt_stride = kGemmBM;
-    a.a1_offset = 0;
-    a.sA0 = w.sg;
-    a.sA1 = w.su;
-    a.sa1_block_offset = 0;
-    a.sB = ws.P_scale;
+    a.w_rows_per_group = d.I;
+    a.w_mt_stride = kGemmBM;
+    a.w1_offset = 0;
+    a.sW0 = w.sg;
+    a.sW1 = w.su;
+    a.sw1_block_offset = 0;
+    a.sX = ws.P_scale;
     a.out = ws.Hb;
     a.out_scale = ws.H_scale;
     a.ld_out = d.I;
@@ -421,14 +432,14 @@ cudaError_t launch_gemm_fp8(const LayerDims& d, int T, const TcWeights& w, Works
   }
   // down: K = I, items of 256 output columns
   a.num_kb = d.I / 128;
-  a.MT = d.H / (2 * kGemmBM);
-  a.a_rows_per_group = d.H;
-  a.a_mt_stride = 2 * kGemmBM;
-  a.a1_offset = kGemmBM;
-  a.sA0 = w.sd;
-  a.sA1 = w.sd;
-  a.sa1_block_offset = 1;
-  a.sB = ws.H_scale;
+  a.MT = d.H / kBN;
+  a.w_rows_per_group = d.H;
+  a.w_mt_stride = kBN;
+  a.w1_offset = kGemmBM;
+  a.sW0 = w.sd;
+  a.sW1 = w.sd;
+  a.sw1_block_offset = 1;
+  a.sX = ws.H_scale;
   a.out = ws.Y;
   a.out_scale = nullptr;
   a.ld_out = d.H;
