@@ -205,16 +205,31 @@ __device__ __forceinline__ float fma_bf16_hi(uint32_t a, uint32_t b, float c) {
 
 // Canonical dot (router.cu's order): lane l runs the fma chain over chunks
 // l, l+32, ... of 8 channels, then the xor fold.  All lanes return the sum.
+// Loads are issued D chunks ahead of the chain; the chain's order is
+// unchanged.
+template <int D>
 __device__ __forceinline__ float canonical_dot_warp(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w,
                                                     int H, int lane) {
+  const int nc = H >> 3;
+  const uint4* xa = reinterpret_cast<const uint4*>(x);
+  const uint4* wa = reinterpret_cast<const uint4*>(w);
   float p = 0.0f;
-  for (int c = lane; c < (H >> 3); c += 32) {
-    const uint4 a = __ldg(reinterpret_cast<const uint4*>(x) + c);
-    const uint4 b = __ldg(reinterpret_cast<const uint4*>(w) + c);
-    p = fma_bf16_lo(a.x, b.x, p); p = fma_bf16_hi(a.x, b.x, p);
-    p = fma_bf16_lo(a.y, b.y, p); p = fma_bf16_hi(a.y, b.y, p);
-    p = fma_bf16_lo(a.z, b.z, p); p = fma_bf16_hi(a.z, b.z, p);
-    p = fma_bf16_lo(a.w, b.w, p); p = fma_bf16_hi(a.w, b.w, p);
+  for (int c0 = lane; c0 < nc; c0 += 32 * D) {
+    uint4 a[D], b[D];
+#pragma unroll
+    for (int i = 0; i < D; ++i)
+      if (c0 + 32 * i < nc) {
+        a[i] = __ldg(xa + c0 + 32 * i);
+        b[i] = __ldg(wa + c0 + 32 * i);
+      }
+#pragma unroll
+    for (int i = 0; i < D; ++i)
+      if (c0 + 32 * i < nc) {
+        p = fma_bf16_lo(a[i].x, b[i].x, p); p = fma_bf16_hi(a[i].x, b[i].x, p);
+        p = fma_bf16_lo(a[i].y, b[i].y, p); p = fma_bf16_hi(a[i].y, b[i].y, p);
+        p = fma_bf16_lo(a[i].z, b[i].z, p); p = fma_bf16_hi(a[i].z, b[i].z, p);
+        p = fma_bf16_lo(a[i].w, b[i].w, p); p = fma_bf16_hi(a[i].w, b[i].w, p);
+      }
   }
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) p = p + __shfl_xor_sync(0xffffffffu, p, o);
@@ -264,7 +279,9 @@ struct SelectArgs {
   float* topk_w;
 };
 
-__global__ void __launch_bounds__(256) router_select_kernel(const SelectArgs a) {
+// One warp per token (8 tokens per block): for many tokens, every warp runs
+// its token from the bounds to the weights without waiting for the others.
+__global__ void __launch_bounds__(256) router_select_warp_kernel(const SelectArgs a) {
   constexpr int PER = (kMaxExperts + 31) / 32;  // 8 entries per lane for E <= 256
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -325,10 +342,147 @@ __global__ void __launch_bounds__(256) router_select_kernel(const SelectArgs a) 
       const int src = __ffs(msk) - 1;
       msk &= msk - 1;
       const int e = src + 32 * q;
-      float v = canonical_dot_warp(x, a.wrT + (size_t)e * a.H, a.H, lane);
+      float v = canonical_dot_warp<1>(x, a.wrT + (size_t)e * a.H, a.H, lane);
       if (a.bias) v = __fadd_rn(v, __ldg(a.bias + e));
       if (lane == src) lc[q] = v;
     }
+  }
+  // logits row for inspection: canonical where computed, tensor-core estimate elsewhere
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int e = lane + 32 * q;
+    if (e < E) {
+      const bool isc = all || ((cmask[q] >> lane) & 1u);
+      a.logits[(size_t)t * E + e] = isc ? lc[q] : est[q];
+    }
+  }
+  // top-k among the exact values (non-candidates are -inf and never win)
+  bool tk[PER];
+#pragma unroll
+  for (int q = 0; q < PER; ++q) tk[q] = taken[q] || !(all || ((cmask[q] >> lane) & 1u));
+  float sel_v[kMaxK];
+  int sel_i[kMaxK];
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    if (j >= k) break;
+    float bv;
+    int bi;
+    warp_best<PER>(lc, tk, lane, bv, bi);
+    sel_v[j] = bv;
+    sel_i[j] = bi;
+#pragma unroll
+    for (int q = 0; q < PER; ++q)
+      if (lane + 32 * q == bi) tk[q] = true;
+  }
+  if (lane == 0) {
+    float den = 0.0f, ex[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      if (j >= k) break;
+      ex[j] = expf(sel_v[j] - sel_v[0]);
+      den += ex[j];
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      if (j >= k) break;
+      a.topk_idx[(size_t)t * k + j] = sel_i[j];
+      a.topk_w[(size_t)t * k + j] = ex[j] / den;
+    }
+  }
+}
+
+// Few tokens: eight warps per block, WPT warps per token (8 / WPT tokens per
+// block).  The token's first warp bounds the estimates and lists the
+// candidates; the token's WPT warps compute their canonical logits (round
+// robin); the first warp then selects among the exact values and writes the
+// weights, so the candidate dot products of one token run in parallel.
+constexpr int kSelWarps = 8;
+
+template <int WPT>
+__global__ void __launch_bounds__(32 * kSelWarps) router_select_kernel(const SelectArgs a) {
+  constexpr int PER = (kMaxExperts + 31) / 32;  // 8 entries per lane for E <= 256
+  constexpr int kTok = kSelWarps / WPT;        // tokens per block
+  __shared__ int s_list[kTok][kMaxExperts];
+  __shared__ float s_lc[kTok][kMaxExperts];
+  __shared__ int s_n[kTok];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int slot = warp / WPT, sub = warp % WPT;
+  const int t = blockIdx.x * kTok + slot;
+  const bool valid = t < a.T;
+  const int E = a.E, k = a.k;
+  const uint16_t* x = a.Xc + (size_t)(valid ? t : 0) * a.H;
+  float est[PER];
+  unsigned cmask[PER];
+  bool taken[PER], all = false;
+  if (sub == 0 && valid) {
+    const float xn = __ldg(a.xnorm + t);
+    float lo[PER], hi[PER];  // bounds of the estimate
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const int e = lane + 32 * q;
+      taken[q] = e >= E;
+      est[q] = lo[q] = hi[q] = 0.0f;
+      if (e < E) {
+        float sum = 0.0f;
+        for (int sp = 0; sp < a.splits; ++sp) sum += __ldcg(a.part + ((size_t)sp * a.T + t) * E + e);
+        const float bs = a.bias ? __ldg(a.bias + e) : 0.0f;
+        if (a.bias) sum = __fadd_rn(sum, bs);
+        const float b = a.g * xn * __ldg(a.wnorm + e) + 0x1p-22f * (fabsf(sum) + fabsf(bs)) + 0x1p-100f;
+        est[q] = sum;
+        lo[q] = sum - b;
+        hi[q] = sum + b;
+        s_lc[slot][e] = -INFINITY;
+      }
+    }
+    // m = k-th largest lower end
+    float m = 0.0f;
+    {
+      bool tk[PER];
+#pragma unroll
+      for (int q = 0; q < PER; ++q) tk[q] = taken[q];
+      for (int j = 0; j < k; ++j) {
+        float bv;
+        int bi;
+        warp_best<PER>(lo, tk, lane, bv, bi);
+        m = bv;
+#pragma unroll
+        for (int q = 0; q < PER; ++q)
+          if (lane + 32 * q == bi) tk[q] = true;
+      }
+    }
+    // candidates: upper end >= m (every expert when there are too many)
+    int ncand = 0;
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      cmask[q] = __ballot_sync(0xffffffffu, !taken[q] && hi[q] >= m);
+      ncand += __popc(cmask[q]);
+    }
+    all = ncand > kMaxCand;
+    int n = 0;
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const unsigned msk = all ? __ballot_sync(0xffffffffu, !taken[q]) : cmask[q];
+      if ((msk >> lane) & 1u) s_list[slot][n + __popc(msk & ((1u << lane) - 1u))] = lane + 32 * q;
+      n += __popc(msk);
+    }
+    if (lane == 0) s_n[slot] = n;
+  }
+  __syncthreads();
+  // canonical logits of the listed experts
+  const int n = valid ? s_n[slot] : 0;
+  for (int i = sub; i < n; i += WPT) {
+    const int e = s_list[slot][i];
+    float v = canonical_dot_warp<8>(x, a.wrT + (size_t)e * a.H, a.H, lane);
+    if (a.bias) v = __fadd_rn(v, __ldg(a.bias + e));
+    if (lane == 0) s_lc[slot][e] = v;
+  }
+  __syncthreads();
+  if (sub != 0 || !valid) return;
+  float lc[PER];
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int e = lane + 32 * q;
+    lc[q] = e < E ? s_lc[slot][e] : -INFINITY;
   }
   // logits row for inspection: canonical where computed, tensor-core estimate elsewhere
 #pragma unroll
@@ -446,7 +600,16 @@ cudaError_t launch_router_tc(const SrcTable& st, const void* wrT, const float* b
   sa.logits = ws.logits;
   sa.topk_idx = ws.topk_idx;
   sa.topk_w = ws.topk_w;
-  router_select_kernel<<<(T + 7) / 8, 256, 0, s>>>(sa);
+  // warps per token: the most (up to 8) that still leaves about one warp per
+  // token once 32 warps per SM are busy
+  int wpt = 8;
+  while (wpt > 1 && (long)T * wpt > 32l * num_sms) wpt >>= 1;
+  const int tok = kSelWarps / wpt;
+  const int blocks = (T + tok - 1) / tok;
+  if (wpt == 8) router_select_kernel<8><<<blocks, 32 * kSelWarps, 0, s>>>(sa);
+  else if (wpt == 4) router_select_kernel<4><<<blocks, 32 * kSelWarps, 0, s>>>(sa);
+  else if (wpt == 2) router_select_kernel<2><<<blocks, 32 * kSelWarps, 0, s>>>(sa);
+  else router_select_warp_kernel<<<blocks, 32 * kSelWarps, 0, s>>>(sa);
   return cudaGetLastError();
 }
 
