@@ -24,7 +24,7 @@
 //   * eight epilogue warps (warp w reads TMEM lanes 32*(w%4) .. +31 and one
 //     half of each 128-column block) read the partial and add it, times the
 //     thread's scale, to fp32 accumulators in registers with packed fp32x2
-//     FMAs; warps whose lanes hold no token skip the math;
+//     FMAs (__ffma2_rn); warps whose lanes hold no token skip the math;
 //   * after the last block: gate/up -> h = silu(G) * U, re-quantised per
 //     token per 128 channels of I (scale = amax/448, e4m3 RNE, saturating);
 //     down -> Y in bf16.  Each thread stores contiguous 16-byte runs of its
@@ -101,19 +101,6 @@ __device__ __forceinline__ Item decode_item(int item, int MT, int G, const int* 
   return it;
 }
 
-// Packed fp32 pairs (sm_100 family): c += s * p for two lanes of a pair in
-// one instruction, each an IEEE round-to-nearest fused multiply-add.
-__device__ __forceinline__ uint64_t pack2(float a, float b) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ void fma2(float& c0, float& c1, uint64_t s2, float p0, float p1) {
-  asm("{\n .reg .b64 rp, rc;\n mov.b64 rp, {%3, %4};\n mov.b64 rc, {%0, %1};\n"
-      " fma.rn.f32x2 rc, %2, rp, rc;\n mov.b64 {%0, %1}, rc;\n}"
-      : "+f"(c0), "+f"(c1)
-      : "l"(s2), "f"(p0), "f"(p1));
-}
 // two e4m3 codes (RNE, saturating): v0 in the low byte, v1 in the high byte
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float v0, float v1) {
   uint16_t r;
@@ -290,9 +277,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!epi_sync(ebar, ephase, lane, abort, args.err)) break;
-      float acc0[64], acc1[64];  // columns half*64 + j of weight rows 0..127 and 128..255
+      // columns half*64 + 2j, +1 of weight rows 0..127 (acc0) and 128..255 (acc1); packed fp32
+      // pairs so the promotion is one fma.rn.f32x2 per two columns
+      float2 acc0[32], acc1[32];
 #pragma unroll
-      for (int j = 0; j < 64; ++j) acc0[j] = acc1[j] = 0.0f;
+      for (int j = 0; j < 32; ++j) acc0[j] = acc1[j] = make_float2(0.0f, 0.0f);
       for (int kb = 0; kb < nkb; ++kb, ++gstep) {
         const uint32_t b = gstep & 1u, use = gstep >> 1;
         if (!mbar_wait(&pfull[b], use & 1u, abort, args.err)) {
@@ -302,8 +291,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         if (active) {
           const float sx = s_sc[kb][r];
-          const uint64_t s0 = pack2(sx * s_w[0][kb], sx * s_w[0][kb]);
-          const uint64_t s1 = pack2(sx * s_w[1][kb], sx * s_w[1][kb]);
+          const float sw0 = sx * s_w[0][kb], sw1 = sx * s_w[1][kb];
+          const float2 s0 = make_float2(sw0, sw0), s1 = make_float2(sw1, sw1);
 #pragma unroll
           for (int cc = 0; cc < 64; cc += 32) {
             float p0[32], p1[32];
@@ -312,9 +301,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_32x32b_x32(col + 128u, p1);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              fma2(acc0[cc + j], acc0[cc + j + 1], s0, p0[j], p0[j + 1]);
-              fma2(acc1[cc + j], acc1[cc + j + 1], s1, p1[j], p1[j + 1]);
+            for (int j = 0; j < 16; ++j) {
+              acc0[cc / 2 + j] = __ffma2_rn(s0, make_float2(p0[2 * j], p0[2 * j + 1]), acc0[cc / 2 + j]);
+              acc1[cc / 2 + j] = __ffma2_rn(s1, make_float2(p1[2 * j], p1[2 * j + 1]), acc1[cc / 2 + j]);
             }
           }
         }
@@ -328,12 +317,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const size_t row = (size_t)(it.row0 + r);
       if (args.mode == 0) {
         // h = silu(G) * U, then e4m3 per token per 128 channels of I (this item's channels)
-        float amax = 0.0f;
+        float h[64], amax = 0.0f;
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
-          const float g = acc0[j];
-          acc0[j] = g / (1.0f + expf(-g)) * acc1[j];
-          amax = fmaxf(amax, fabsf(acc0[j]));
+          const float g = (j & 1) ? acc0[j >> 1].y : acc0[j >> 1].x;
+          const float u = (j & 1) ? acc1[j >> 1].y : acc1[j >> 1].x;
+          h[j] = __fdividef(g, 1.0f + __expf(-g)) * u;  // fast SiLU: error far below e4m3 rounding
+          amax = fmaxf(amax, fabsf(h[j]));
         }
         s_red[half][r] = amax;
         if (!epi_sync(ebar, ephase, lane, abort, args.err)) break;
@@ -348,9 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const int j = 16 * v + 4 * q;
-              const uint32_t lo = am == 0.0f ? 0u : cvt_e4m3x2(__fdiv_rn(acc0[j], sc), __fdiv_rn(acc0[j + 1], sc));
-              const uint32_t hi =
-                  am == 0.0f ? 0u : cvt_e4m3x2(__fdiv_rn(acc0[j + 2], sc), __fdiv_rn(acc0[j + 3], sc));
+              const uint32_t lo = am == 0.0f ? 0u : cvt_e4m3x2(__fdiv_rn(h[j], sc), __fdiv_rn(h[j + 1], sc));
+              const uint32_t hi = am == 0.0f ? 0u : cvt_e4m3x2(__fdiv_rn(h[j + 2], sc), __fdiv_rn(h[j + 3], sc));
               w[q] = lo | (hi << 16);
             }
             dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -362,14 +351,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint16_t* yrow = static_cast<uint16_t*>(args.out) + row * args.ld_out + it.mt * kBN + half * 64;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
-          const float* acc = part ? acc1 : acc0;
+          const float2* acc = part ? acc1 : acc0;
           uint4* dst = reinterpret_cast<uint4*>(yrow + part * 128);
 #pragma unroll
           for (int v = 0; v < 8; ++v) {
             uint32_t w[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const __nv_bfloat162 y = __floats2bfloat162_rn(acc[8 * v + 2 * q], acc[8 * v + 2 * q + 1]);
+              const __nv_bfloat162 y = __float22bfloat162_rn(acc[4 * v + q]);
               w[q] = *reinterpret_cast<const uint32_t*>(&y);
             }
             dst[v] = make_uint4(w[0], w[1], w[2], w[3]);

@@ -25,10 +25,17 @@
 // adjacent so concurrently running CTAs share the weight tile in L2.  The
 // kernel is persistent: grid = SM count, CTA c takes items c, c+grid, ...
 //
-// Warp roles (192 threads): warp 0 lane 0 issues TMA into a 4-stage ring
-// (weights with an L2 evict-first hint, activations evict-last); warp 1
-// owns TMEM and lane 0 issues tcgen05.mma; warps 2-5 are the epilogue
-// (warp w reads TMEM lanes 32*(w%4) .. +31).  Every mbarrier wait is bounded:
+// Warp roles (352 threads): warp 0 lane 0 streams weight tiles into their
+// own ring (L2 evict-first); warp 10 lane 0 streams the token tiles into a
+// second, shallower ring (evict-last); warp 1 owns TMEM and lane 0 issues
+// tcgen05.mma; warps 2-9 are the epilogue (warp w reads TMEM lanes
+// 32*(w%4) .. +31; the two warps of a lane quarter take alternate 32-token
+// chunks).  With one accumulator buffer (256-token tiles) the next item's
+// MMAs wait for the epilogue, so it runs on two warps per SM sub-partition
+// and uses the fast exponential and division for SiLU (their error is far
+// below bf16 rounding).  Separate rings keep more weight bytes in flight than a
+// ring of (weights + tokens) stages would in the same shared memory: the
+// weights come from HBM, the tokens from L2.  Every mbarrier wait is bounded:
 // on a timeout the CTA raises its abort flag and the device error word, every
 // role stops, issued copies and MMAs are drained, TMEM is freed and the kernel
 // returns.
@@ -42,18 +49,21 @@ namespace {
 constexpr int kRowBytes = 128;               // one 128-byte swizzle row of K
 constexpr int kATile = kGemmBM * kRowBytes;  // 16 KB
 constexpr int kBBoxRows = 32;                // rows per TMA box of B
-constexpr int kThreads = 192;
+constexpr int kThreads = 352;
+constexpr int kEpiWarps = 8;
+constexpr int kWTileBytes = 2 * kATile;      // one weight stage: two 128-row tiles
+constexpr int kPfSteps = 4;                  // weight K blocks prefetched into L2 ahead of the loads
 
-// Tile shape per token-tile width BN: 128 -> 4 stages of 48 KB and two TMEM
-// accumulator buffers (epilogue overlaps the next item); 256 -> 3 stages of
-// 64 KB and one accumulator buffer (an expert's <= 256 tokens share one pass
+// Tile shape per token-tile width BN: 128 -> 5 weight + 3 token stages and
+// two TMEM accumulator buffers (epilogue overlaps the next item); 256 -> 3 + 3
+// stages and one accumulator buffer (an expert's <= 256 tokens share one pass
 // over its weights).
 template <int BN>
 struct TileCfg {
-  static constexpr int kStages = BN == 256 ? 3 : 4;
+  static constexpr int kWStages = BN == 256 ? 3 : 5;
+  static constexpr int kXStages = 3;
   static constexpr int kBTile = BN * kRowBytes;
-  static constexpr int kStageBytes = 2 * kATile + kBTile;
-  static constexpr int kDynSmem = kStages * kStageBytes + 1024;
+  static constexpr int kDynSmem = kWStages * kWTileBytes + kXStages * kBTile + 1024;
   static constexpr int kAbuf = 512 / (2 * BN);  // TMEM accumulator buffers
 };
 constexpr uint32_t kTmemCols = 512;
@@ -108,18 +118,22 @@ template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                      const __grid_constant__ CUtensorMap tmB, const TcArgs args) {
-  constexpr int kStages = TileCfg<BN>::kStages, kStageBytes = TileCfg<BN>::kStageBytes;
+  constexpr int kWS = TileCfg<BN>::kWStages, kXS = TileCfg<BN>::kXStages, kBTile = TileCfg<BN>::kBTile;
   constexpr uint32_t kAbuf = TileCfg<BN>::kAbuf;
   extern __shared__ uint8_t dyn_smem[];
   uint8_t* smem = dyn_smem + ((1024u - (smem_u32(dyn_smem) & 1023u)) & 1023u);
+  uint8_t* wsm = smem;                     // [kWS][2 x 16 KB]
+  uint8_t* xsm = smem + kWS * kWTileBytes;  // [kXS][BN x 128 B]
 
-  __shared__ __align__(8) uint64_t bars[2 * kStages + 5];
+  __shared__ __align__(8) uint64_t bars[2 * kWS + 2 * kXS + 5];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_tb[kMaxExperts + 1], s_off[kMaxExperts + 1], s_cnt[kMaxExperts];
-  uint64_t* full = bars;
-  uint64_t* empty = bars + kStages;
-  uint64_t* tfull = bars + 2 * kStages;  // [2] accumulator buffer ready for the epilogue
+  uint64_t* wfull = bars;
+  uint64_t* wempty = bars + kWS;
+  uint64_t* xfull = bars + 2 * kWS;
+  uint64_t* xempty = xfull + kXS;
+  uint64_t* tfull = xempty + kXS;        // [2] accumulator buffer ready for the epilogue
   uint64_t* tempty = tfull + 2;          // [2] accumulator buffer drained by the epilogue
   uint64_t* drain = tfull + 4;
 
@@ -131,13 +145,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (g < G) s_cnt[g] = args.counts[g];
   }
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < kWS; ++s) {
+      mbar_init(&wfull[s], 1);
+      mbar_init(&wempty[s], 1);
+    }
+    for (int s = 0; s < kXS; ++s) {
+      mbar_init(&xfull[s], 1);
+      mbar_init(&xempty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+      mbar_init(&tempty[a], kEpiWarps);
     }
     mbar_init(drain, 1);
     s_abort = 0;
@@ -157,50 +175,75 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total = args.MT * s_tb[G];
   volatile int* abort = &s_abort;
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 10) {
     if (lane == 0) {
-      // ---------------- TMA producer
-      const uint64_t pol_w = l2_policy_evict_first();
-      const uint64_t pol_b = l2_policy_evict_last();
+      // ---------------- TMA producers: warp 0 weights, warp 10 tokens
+      const bool wprod = warp == 0;
+      const int nst = wprod ? kWS : kXS;
+      uint64_t* fb = wprod ? wfull : xfull;
+      uint64_t* eb = wprod ? wempty : xempty;
+      const uint64_t pol = wprod ? l2_policy_evict_first() : l2_policy_evict_last();
       int s = 0;
       uint32_t ph = 0, filled = 0, fill_ph = 0;
       bool ok = true;
+      // tiled weights: tile (row block rb, K block kb) starts at tile row (rb * num_kb + kb) * 128
+      auto row_blocks = [&](const Item& it, int& rb0, int& rb1) {
+        rb0 = it.g * (args.a_rows_per_group / 128) + it.mt * (args.a_mt_stride / 128);
+        rb1 = rb0 + args.a1_offset / 128;
+      };
+      // L2 prefetch cursor (weights only): runs kPfSteps K blocks ahead of the loads
+      int pf_item = blockIdx.x, pf_kb = 0, pf_rb0 = 0, pf_rb1 = 0;
+      long pf_n = 0, ld_n = 0;
+      if (wprod && pf_item < total) row_blocks(decode_item<BN>(pf_item, args.MT, G, s_tb, s_off, s_cnt), pf_rb0, pf_rb1);
       for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
         const Item it = decode_item<BN>(item, args.MT, G, s_tb, s_off, s_cnt);
-        // tiled weights: tile (row block rb, K block kb) starts at tile row (rb * num_kb + kb) * 128
-        const int rb0 = it.g * (args.a_rows_per_group / 128) + it.mt * (args.a_mt_stride / 128);
-        const int rb1 = rb0 + args.a1_offset / 128;
+        int rb0, rb1;
+        row_blocks(it, rb0, rb1);
         const int nbox = (it.nrows + kBBoxRows - 1) / kBBoxRows;
-        const uint32_t bytes = 2 * kATile + nbox * kBBoxRows * kRowBytes;
-        for (int kb = 0; kb < args.num_kb; ++kb) {
-          if (!mbar_wait(&empty[s], ph ^ 1u, abort, args.err)) {
+        const uint32_t bytes = wprod ? (uint32_t)kWTileBytes : (uint32_t)(nbox * kBBoxRows * kRowBytes);
+        for (int kb = 0; kb < args.num_kb; ++kb, ++ld_n) {
+          if (wprod)
+            for (; pf_n <= ld_n + kPfSteps && pf_item < total; ++pf_n) {
+              tma_prefetch_l2_2d(&tmA0, 0, (pf_rb0 * args.num_kb + pf_kb) * 128);
+              tma_prefetch_l2_2d(&tmA1, 0, (pf_rb1 * args.num_kb + pf_kb) * 128);
+              if (++pf_kb == args.num_kb) {
+                pf_kb = 0;
+                pf_item += gridDim.x;
+                if (pf_item < total)
+                  row_blocks(decode_item<BN>(pf_item, args.MT, G, s_tb, s_off, s_cnt), pf_rb0, pf_rb1);
+              }
+            }
+          if (!mbar_wait(&eb[s], ph ^ 1u, abort, args.err)) {
             ok = false;
             break;
           }
-          uint8_t* st = smem + s * kStageBytes;
-          mbar_arrive_expect_tx(&full[s], bytes);
-          tma_load_2d_hint(st, &tmA0, &full[s], 0, (rb0 * args.num_kb + kb) * 128, pol_w);
-          tma_load_2d_hint(st + kATile, &tmA1, &full[s], 0, (rb1 * args.num_kb + kb) * 128, pol_w);
-          for (int b = 0; b < nbox; ++b)
-            tma_load_2d_hint(st + 2 * kATile + b * kBBoxRows * kRowBytes, &tmB, &full[s], kb * 64,
-                             it.row0 + b * kBBoxRows, pol_b);
+          mbar_arrive_expect_tx(&fb[s], bytes);
+          if (wprod) {
+            uint8_t* st = wsm + s * kWTileBytes;
+            tma_load_2d_hint(st, &tmA0, &fb[s], 0, (rb0 * args.num_kb + kb) * 128, pol);
+            tma_load_2d_hint(st + kATile, &tmA1, &fb[s], 0, (rb1 * args.num_kb + kb) * 128, pol);
+          } else {
+            uint8_t* st = xsm + s * kBTile;
+            for (int b = 0; b < nbox; ++b)
+              tma_load_2d_hint(st + b * kBBoxRows * kRowBytes, &tmB, &fb[s], kb * 64, it.row0 + b * kBBoxRows, pol);
+          }
           filled |= 1u << s;
           fill_ph = (fill_ph & ~(1u << s)) | (ph << s);
-          if (++s == kStages) {
+          if (++s == nst) {
             s = 0;
             ph ^= 1u;
           }
         }
       }
       if (!ok)  // let the copies already issued land before the CTA exits
-        for (int q = 0; q < kStages; ++q)
-          if ((filled >> q) & 1u) mbar_wait_cycles(&full[q], (fill_ph >> q) & 1u, kDrainCycles);
+        for (int q = 0; q < nst; ++q)
+          if ((filled >> q) & 1u) mbar_wait_cycles(&fb[q], (fill_ph >> q) & 1u, kDrainCycles);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
-      int s = 0;
-      uint32_t ph = 0, ic = 0;
+      int ws_ = 0, xs = 0;
+      uint32_t wph = 0, xph = 0, ic = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < total; item += gridDim.x, ++ic) {
         const Item it = decode_item<BN>(item, args.MT, G, s_tb, s_off, s_cnt);
@@ -211,25 +254,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d0 = tmem + a * (2u * BN), d1 = d0 + BN;
         for (int kb = 0; kb < args.num_kb; ++kb) {
-          if (!mbar_wait(&full[s], ph, abort, args.err)) {
+          if (!mbar_wait(&wfull[ws_], wph, abort, args.err) || !mbar_wait(&xfull[xs], xph, abort, args.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          uint8_t* st = smem + s * kStageBytes;
+          uint8_t* st = wsm + ws_ * kWTileBytes;
           const uint64_t da0 = sw128_desc(st);
           const uint64_t da1 = sw128_desc(st + kATile);
-          const uint64_t db = sw128_desc(st + 2 * kATile);
+          const uint64_t db = sw128_desc(xsm + xs * kBTile);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {  // 4 x K=16 per 128-byte row
             const uint32_t acc = (kb | kk) ? 1u : 0u;
             mma_f16(d0, da0 + 2 * kk, db + 2 * kk, idesc, acc);
             mma_f16(d1, da1 + 2 * kk, db + 2 * kk, idesc, acc);
           }
-          tc_commit(&empty[s]);
-          if (++s == kStages) {
-            s = 0;
-            ph ^= 1u;
+          tc_commit(&wempty[ws_]);
+          tc_commit(&xempty[xs]);
+          if (++ws_ == kWS) {
+            ws_ = 0;
+            wph ^= 1u;
+          }
+          if (++xs == kXS) {
+            xs = 0;
+            xph ^= 1u;
           }
         }
         if (!ok) break;
@@ -238,9 +286,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit(drain);  // all MMAs issued above complete before TMEM is freed
       mbar_wait_cycles(drain, 0, kDrainCycles);
     }
-  } else {
-    // ---------------- epilogue: warps 2..5
-    const int quad = warp & 3;
+  } else if (warp >= 2 && warp < 2 + kEpiWarps) {
+    // ---------------- epilogue: warps 2..9
+    const int quad = warp & 3, half = (warp - 2) >> 2;
     const int r = quad * 32 + lane;  // row of the 128-row MMA tile
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
     uint32_t ic = 0;
@@ -250,31 +298,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&tfull[a], (ic / kAbuf) & 1u, abort, args.err)) break;
       tc_fence_after();
       const uint32_t t_buf = t_lane + a * (2u * BN);
-      for (int c = 0; c < it.nrows; c += 32) {
+      for (int c = 32 * half; c < it.nrows; c += 64) {
         float d0[32], d1[32];
         tmem_ld_32x32b_x32(t_buf + (uint32_t)c, d0);
         tmem_ld_32x32b_x32(t_buf + (uint32_t)(BN + c), d1);
         tmem_ld_wait();
         const int nn = min(32, it.nrows - c);
-        uint16_t* o = args.out + (size_t)(it.row0 + c) * args.ld_out;
+        // one output row per token: this thread writes column (m tile, r) of rows row0+c .. +nn-1
+        uint16_t* o = args.out + (size_t)(it.row0 + c) * args.ld_out +
+                      (args.mode == 0 ? it.mt * kGemmBM : it.mt * 2 * kGemmBM) + r;
         if (args.mode == 0) {
-          const int col = it.mt * kGemmBM + r;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             if (j < nn) {
               const float g = d0[j];
-              const float hv = g / (1.0f + expf(-g)) * d1[j];
-              o[(size_t)j * args.ld_out + col] = f2bf(hv);
+              *o = f2bf(__fdividef(g, 1.0f + __expf(-g)) * d1[j]);
             }
+            o += args.ld_out;
           }
         } else {
-          const int col = it.mt * 2 * kGemmBM + r;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             if (j < nn) {
-              o[(size_t)j * args.ld_out + col] = f2bf(d0[j]);
-              o[(size_t)j * args.ld_out + col + kGemmBM] = f2bf(d1[j]);
+              o[0] = f2bf(d0[j]);
+              o[kGemmBM] = f2bf(d1[j]);
             }
+            o += args.ld_out;
           }
         }
       }
