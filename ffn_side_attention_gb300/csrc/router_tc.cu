@@ -556,7 +556,7 @@ cudaError_t launch_router_wnorm(const void* wrT, int H, int E, float* wnorm, cud
 int router_tc_splits(const LayerDims& d, int T, int num_sms) {
   const int tiles = ((T + kRBN - 1) / kRBN) * ((d.E + kRBM - 1) / kRBM);
   const int num_kb = d.H / 64;
-  int splits = (num_sms + tiles - 1) / tiles;
+  int splits = num_sms / tiles;  // whole waves: tiles * splits <= SM count
   splits = splits < 1 ? 1 : splits;
   const int max_splits = num_kb / 4 > 0 ? num_kb / 4 : 1;
   if (splits > max_splits) splits = max_splits;

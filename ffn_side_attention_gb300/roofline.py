@@ -67,6 +67,11 @@ def gateup_bytes(cfg, T: int, touched: int) -> float:
     return b
 
 
+def gateup_flops(cfg, T: int) -> int:
+    """FLOPs of one gate/up launch: two H x I products per packed row."""
+    return 4 * T * (cfg.k + cfg.S) * cfg.H * cfg.I
+
+
 def down_bytes(cfg, T: int, touched: int) -> float:
     z = sizes(cfg.dtype)
     rows = T * (cfg.k + cfg.S)
