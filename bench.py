@@ -360,12 +360,12 @@ def run_ours(args, world, rank, local):
     h_in = [x.cpu().pin_memory() for x in inputs[0]]
     h_out = [torch.empty_like(x).pin_memory() for x in h_in]
     for _ in range(max(2, args.warmup // 2)):
-        layer.forward_host(h_in, h_out, stream=stream)
+        layer.forward_host(h_in, h_out, stream=stream, n_micro=args.n_micro)
     e2e_steps = max(3, min(args.steps, 50))
     barrier(world)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
-        layer.forward_host(h_in, h_out, stream=stream)
+        layer.forward_host(h_in, h_out, stream=stream, n_micro=args.n_micro)
     e2e_s = barrier_max(world, time.perf_counter() - t0) / e2e_steps
     io_bytes = T * cfg.H * (4 if cfg.dtype == "fp32" else 2)
 

@@ -62,7 +62,7 @@ def lib():
         L.afd_ffn_forward.restype = ip
         L.afd_ffn_forward_pipelined.argtypes = [vp, vp, ip, vp, vp, ip, vp]
         L.afd_ffn_forward_pipelined.restype = ip
-        L.afd_ffn_forward_host.argtypes = [vp, vp, vp, vp, ip, vp]
+        L.afd_ffn_forward_host.argtypes = [vp, vp, ip, vp, vp, ip, vp]
         L.afd_ffn_forward_host.restype = ip
         L.afd_ffn_debug_routing.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.afd_ffn_debug_routing.restype = ip
@@ -120,8 +120,8 @@ def afd_ffn_forward_pipelined(h, stream, n_micro, src_ptrs, src_counts, out_ptrs
                                                   len(src_counts), _ptr_array(out_ptrs)), h)
 
 
-def afd_ffn_forward_host(h, stream, src_ptrs, src_counts, out_ptrs):
-    return _check(lib().afd_ffn_forward_host(h, stream, _ptr_array(src_ptrs), _int_array(src_counts),
+def afd_ffn_forward_host(h, stream, n_micro, src_ptrs, src_counts, out_ptrs):
+    return _check(lib().afd_ffn_forward_host(h, stream, n_micro, _ptr_array(src_ptrs), _int_array(src_counts),
                                              len(src_counts), _ptr_array(out_ptrs)), h)
 
 
@@ -224,11 +224,13 @@ class MoELayer:
             afd_ffn_forward_pipelined(self.handle, self._stream(stream), n_micro, sp, counts, op)
         return outs
 
-    def forward_host(self, srcs, outs, stream=None):
-        """Host tensors in and out (pinned for asynchronous copies); synchronous."""
+    def forward_host(self, srcs, outs, stream=None, n_micro=1):
+        """Host tensors in and out (pinned for asynchronous copies); synchronous.
+        n_micro > 1 runs the micro-batch pipeline between the copies."""
         sp = [s.data_ptr() if s.shape[0] else 0 for s in srcs]
         op = [o.data_ptr() if o.shape[0] else 0 for o in outs]
-        afd_ffn_forward_host(self.handle, self._stream(stream), sp, [int(s.shape[0]) for s in srcs], op)
+        afd_ffn_forward_host(self.handle, self._stream(stream), int(n_micro), sp, [int(s.shape[0]) for s in srcs],
+                             op)
         return outs
 
     def routing(self, T, stream=None):

@@ -130,6 +130,7 @@ int alloc_workspace(afd_ffn* h, Workspace& ws) {
   if ((rc = dmalloc_t(h, &ws.topk_idx, T * k)) || (rc = dmalloc_t(h, &ws.topk_w, T * k)) ||
       (rc = dmalloc_t(h, &ws.logits, T * E)) ||
       (rc = dmalloc_t(h, &ws.tile_counter, (T + afd::kRouterTokTile - 1) / afd::kRouterTokTile)) ||
+      (rc = dmalloc_t(h, &ws.tok_ticket, T)) ||
       (rc = dmalloc_t(h, &ws.counts, G)) || (rc = dmalloc_t(h, &ws.offsets, G + 1)) ||
       (rc = dmalloc_t(h, &ws.tile_base, G + 1)) || (rc = dmalloc_t(h, &ws.block_hist, ((T + 255) / 256) * E)) ||
       (rc = dmalloc_t(h, &ws.perm, R)) ||
@@ -149,6 +150,7 @@ int alloc_workspace(afd_ffn* h, Workspace& ws) {
   }
   CUDA_TRY(h, cudaMemset(ws.tile_counter, 0, sizeof(int32_t) * ((T + afd::kRouterTokTile - 1) / afd::kRouterTokTile)));
   CUDA_TRY(h, cudaMemset(ws.err, 0, sizeof(int)));
+  CUDA_TRY(h, cudaMemset(ws.tok_ticket, 0, sizeof(int32_t) * T));
   CUDA_TRY(h, cudaMemset(ws.P, 0, R * c.H * ab));
   CUDA_TRY(h, cudaMemset(ws.Hb, 0, R * c.I * (c.dtype == AFD_FP8_E4M3 ? 1 : act_bytes(c))));
   if (c.dtype != AFD_FP32) {
@@ -162,7 +164,7 @@ int alloc_workspace(afd_ffn* h, Workspace& ws) {
 }
 
 void free_workspace(Workspace& ws) {
-  void* ptrs[] = {ws.topk_idx, ws.topk_w, ws.logits, ws.tile_counter, ws.counts, ws.offsets, ws.tile_base,
+  void* ptrs[] = {ws.topk_idx, ws.topk_w, ws.logits, ws.tile_counter, ws.tok_ticket, ws.counts, ws.offsets, ws.tile_base,
                   ws.block_hist, ws.perm, ws.pos, ws.P, ws.P_scale, ws.Hb, ws.H_scale, ws.Y, ws.err,
                   ws.stage, ws.Xc, ws.xnorm, ws.rpart};
   for (void* p : ptrs)
@@ -459,11 +461,13 @@ int afd_ffn_forward_pipelined(afd_ffn_t h, void* stream, int n_micro, const void
   return AFD_OK;
 }
 
-int afd_ffn_forward_host(afd_ffn_t h, void* stream, const void* const* src_ptrs_host, const int* src_counts_host,
-                         int M, void* const* out_ptrs_host) {
+int afd_ffn_forward_host(afd_ffn_t h, void* stream, int n_micro, const void* const* src_ptrs_host,
+                         const int* src_counts_host, int M, void* const* out_ptrs_host) {
   int T = 0;
   int rc = validate_batch(h, src_ptrs_host, src_counts_host, M, out_ptrs_host, &T);
   if (rc) return rc;
+  if (n_micro < 1 || n_micro > AFD_MAX_MICRO)
+    return fail(h, AFD_EINVAL, "n_micro=%d outside [1, %d]", n_micro, AFD_MAX_MICRO);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Workspace& ws = h->ws[0];
   const size_t rowb = (size_t)h->cfg.H * act_bytes(h->cfg);
@@ -481,8 +485,12 @@ int afd_ffn_forward_host(afd_ffn_t h, void* stream, const void* const* src_ptrs_
                                   cudaMemcpyHostToDevice, s));
     r += src_counts_host[m];
   }
-  SrcTable st = make_table(dsrc, src_counts_host, M, dout);
-  if ((rc = run_layer(h, st, ws, s))) return rc;
+  if (n_micro > 1) {
+    if ((rc = afd_ffn_forward_pipelined(h, stream, n_micro, dsrc, src_counts_host, M, dout))) return rc;
+  } else {
+    SrcTable st = make_table(dsrc, src_counts_host, M, dout);
+    if ((rc = run_layer(h, st, ws, s))) return rc;
+  }
   r = 0;
   for (int m = 0; m < M; ++m) {
     if (src_counts_host[m] > 0)

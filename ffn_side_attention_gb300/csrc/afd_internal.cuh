@@ -50,6 +50,7 @@ struct Workspace {
   float* topk_w = nullptr;      // [maxT*k]
   float* logits = nullptr;      // [maxT*E]
   int32_t* tile_counter = nullptr;  // [ceil(maxT/kRouterTokTile)]
+  int32_t* tok_ticket = nullptr;    // [maxT] per-token completion tickets of the small-batch router
   int32_t* counts = nullptr;    // [E+S]
   int32_t* offsets = nullptr;   // [E+S+1]
   int32_t* tile_base = nullptr; // [E+S+1], prefix of ceil(counts / GEMM tile tokens)
@@ -204,6 +205,14 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m
       " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
       : "memory");
+}
+// Contiguous bulk copy global -> shared (both 16-byte aligned, bytes a
+// multiple of 16), completing on `bar` with `bytes` of transaction count.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
 }
 // Prefetch one tile of a tensor map into L2 only (no shared memory, no
 // barrier): lets HBM requests run further ahead than the shared-memory ring.

@@ -17,6 +17,9 @@
 //      L_e <= Lt_e + b_e < m).  The canonical L is then computed for the
 //      candidates only (same order as router.cu), and the top-k and weights
 //      are taken from those exact values.  Over 64 candidates -> all experts.
+// Small batches (a grid of at most kSmallRouterWaves waves of (8 tokens x 8
+// experts) blocks) skip the estimate: one kernel computes every canonical
+// logit and the top-k (latency, not work, bounds them there).
 // Bound: |Lt - exact| + |L - exact| <= (g_tc + g_c) * sum_h |x_h w_h|, and
 // sum |x w| <= ||x|| ||w_e|| (Cauchy-Schwarz, both norms rounded up).
 // g_c = n u / (1 - n u), n = H/32 + 6, u = 2^-24 (the fp32 fma chain and fold);
@@ -34,6 +37,7 @@ namespace {
 
 constexpr int kMaxK = 16;
 constexpr int kMaxCand = 64;
+constexpr int kSmallRouterWaves = 8;  // small-batch path while its grid is at most this many waves
 
 // ---------------------------------------------------------------- 1. stage
 __global__ void __launch_bounds__(256) stage_x_kernel(SrcTable st, int H, uint16_t* __restrict__ Xc,
@@ -265,6 +269,42 @@ __device__ __forceinline__ void warp_best(const float (&v)[PER], const bool (&ta
   }
 }
 
+// Top-k (value desc, id asc) among the entries not marked in tk, then the
+// softmax over the selected: lane 0 writes slots and weights of one token.
+template <int PER>
+__device__ __forceinline__ void write_topk(const float (&lc)[PER], bool (&tk)[PER], int k, int lane,
+                                           int32_t* __restrict__ idx, float* __restrict__ wout) {
+  float sel_v[kMaxK];
+  int sel_i[kMaxK];
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    if (j >= k) break;
+    float bv;
+    int bi;
+    warp_best<PER>(lc, tk, lane, bv, bi);
+    sel_v[j] = bv;
+    sel_i[j] = bi;
+#pragma unroll
+    for (int q = 0; q < PER; ++q)
+      if (lane + 32 * q == bi) tk[q] = true;
+  }
+  if (lane == 0) {
+    float den = 0.0f, ex[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      if (j >= k) break;
+      ex[j] = expf(sel_v[j] - sel_v[0]);
+      den += ex[j];
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      if (j >= k) break;
+      idx[j] = sel_i[j];
+      wout[j] = ex[j] / den;
+    }
+  }
+}
+
 struct SelectArgs {
   const uint16_t* Xc;
   const uint16_t* wrT;  // [E][H]
@@ -360,172 +400,102 @@ __global__ void __launch_bounds__(256) router_select_warp_kernel(const SelectArg
   bool tk[PER];
 #pragma unroll
   for (int q = 0; q < PER; ++q) tk[q] = taken[q] || !(all || ((cmask[q] >> lane) & 1u));
-  float sel_v[kMaxK];
-  int sel_i[kMaxK];
-#pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
-    if (j >= k) break;
-    float bv;
-    int bi;
-    warp_best<PER>(lc, tk, lane, bv, bi);
-    sel_v[j] = bv;
-    sel_i[j] = bi;
-#pragma unroll
-    for (int q = 0; q < PER; ++q)
-      if (lane + 32 * q == bi) tk[q] = true;
-  }
-  if (lane == 0) {
-    float den = 0.0f, ex[kMaxK];
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      if (j >= k) break;
-      ex[j] = expf(sel_v[j] - sel_v[0]);
-      den += ex[j];
-    }
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      if (j >= k) break;
-      a.topk_idx[(size_t)t * k + j] = sel_i[j];
-      a.topk_w[(size_t)t * k + j] = ex[j] / den;
-    }
-  }
+  write_topk<PER>(lc, tk, k, lane, a.topk_idx + (size_t)t * k, a.topk_w + (size_t)t * k);
 }
 
-// Few tokens: eight warps per block, WPT warps per token (8 / WPT tokens per
-// block).  The token's first warp bounds the estimates and lists the
-// candidates; the token's WPT warps compute their canonical logits (round
-// robin); the first warp then selects among the exact values and writes the
-// weights, so the candidate dot products of one token run in parallel.
+// ---------------------------------------------------------------- small batches
+// Few tokens: every logit in the canonical order, straight from the source
+// buffers, in one launch (no staging, no estimate).  Block = 8 warps = 8
+// tokens x one octet of experts: thread 0 copies the octet's 8 router rows
+// (contiguous in W_r) into shared memory with one bulk copy while every warp
+// loads its token's row into registers; lane l then runs the canonical chain
+// over chunks l, l+32, ... for the 8 experts at once (8 independent chains).
+// The last warp to finish a token (atomic ticket per token) selects its top-k
+// from the stored logits and resets the ticket.
 constexpr int kSelWarps = 8;
+constexpr int kOct = 8;               // experts per block
+constexpr int kSmallMaxChunks = 28;   // H <= 7168: chunks of 8 channels per lane
+constexpr int kSmallMaxH = 32 * 8 * kSmallMaxChunks;
+constexpr int kSmallDynSmem = kOct * kSmallMaxH * 2;  // 112 KB
 
-template <int WPT>
-__global__ void __launch_bounds__(32 * kSelWarps) router_select_kernel(const SelectArgs a) {
-  constexpr int PER = (kMaxExperts + 31) / 32;  // 8 entries per lane for E <= 256
-  constexpr int kTok = kSelWarps / WPT;        // tokens per block
-  __shared__ int s_list[kTok][kMaxExperts];
-  __shared__ float s_lc[kTok][kMaxExperts];
-  __shared__ int s_n[kTok];
+__global__ void __launch_bounds__(32 * kSelWarps, 1)
+    router_small_kernel(const SrcTable st, const uint16_t* __restrict__ wrT, const float* __restrict__ bias, int H,
+                        int E, int k, float* __restrict__ logits, int32_t* __restrict__ topk_idx,
+                        float* __restrict__ topk_w, int32_t* __restrict__ ticket, int* err) {
+  constexpr int PER = (kMaxExperts + 31) / 32;
+  extern __shared__ __align__(16) uint4 s_w[];  // [kOct][H/8]
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int s_abort;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int slot = warp / WPT, sub = warp % WPT;
-  const int t = blockIdx.x * kTok + slot;
-  const bool valid = t < a.T;
-  const int E = a.E, k = a.k;
-  const uint16_t* x = a.Xc + (size_t)(valid ? t : 0) * a.H;
-  float est[PER];
-  unsigned cmask[PER];
-  bool taken[PER], all = false;
-  if (sub == 0 && valid) {
-    const float xn = __ldg(a.xnorm + t);
-    float lo[PER], hi[PER];  // bounds of the estimate
-#pragma unroll
-    for (int q = 0; q < PER; ++q) {
-      const int e = lane + 32 * q;
-      taken[q] = e >= E;
-      est[q] = lo[q] = hi[q] = 0.0f;
-      if (e < E) {
-        float sum = 0.0f;
-        for (int sp = 0; sp < a.splits; ++sp) sum += __ldcg(a.part + ((size_t)sp * a.T + t) * E + e);
-        const float bs = a.bias ? __ldg(a.bias + e) : 0.0f;
-        if (a.bias) sum = __fadd_rn(sum, bs);
-        const float b = a.g * xn * __ldg(a.wnorm + e) + 0x1p-22f * (fabsf(sum) + fabsf(bs)) + 0x1p-100f;
-        est[q] = sum;
-        lo[q] = sum - b;
-        hi[q] = sum + b;
-        s_lc[slot][e] = -INFINITY;
-      }
-    }
-    // m = k-th largest lower end
-    float m = 0.0f;
-    {
-      bool tk[PER];
-#pragma unroll
-      for (int q = 0; q < PER; ++q) tk[q] = taken[q];
-      for (int j = 0; j < k; ++j) {
-        float bv;
-        int bi;
-        warp_best<PER>(lo, tk, lane, bv, bi);
-        m = bv;
-#pragma unroll
-        for (int q = 0; q < PER; ++q)
-          if (lane + 32 * q == bi) tk[q] = true;
-      }
-    }
-    // candidates: upper end >= m (every expert when there are too many)
-    int ncand = 0;
-#pragma unroll
-    for (int q = 0; q < PER; ++q) {
-      cmask[q] = __ballot_sync(0xffffffffu, !taken[q] && hi[q] >= m);
-      ncand += __popc(cmask[q]);
-    }
-    all = ncand > kMaxCand;
-    int n = 0;
-#pragma unroll
-    for (int q = 0; q < PER; ++q) {
-      const unsigned msk = all ? __ballot_sync(0xffffffffu, !taken[q]) : cmask[q];
-      if ((msk >> lane) & 1u) s_list[slot][n + __popc(msk & ((1u << lane) - 1u))] = lane + 32 * q;
-      n += __popc(msk);
-    }
-    if (lane == 0) s_n[slot] = n;
+  const int noct = (E + kOct - 1) / kOct;
+  const int oct = blockIdx.x % noct;
+  const int e0 = oct * kOct, ne = min(kOct, E - e0);
+  const int nc = H >> 3;
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&bar, (uint32_t)(ne * nc * 16));
+    bulk_load(s_w, reinterpret_cast<const uint4*>(wrT) + (size_t)e0 * nc, (uint32_t)(ne * nc * 16), &bar);
   }
-  __syncthreads();
-  // canonical logits of the listed experts
-  const int n = valid ? s_n[slot] : 0;
-  for (int i = sub; i < n; i += WPT) {
-    const int e = s_list[slot][i];
-    float v = canonical_dot_warp<8>(x, a.wrT + (size_t)e * a.H, a.H, lane);
-    if (a.bias) v = __fadd_rn(v, __ldg(a.bias + e));
-    if (lane == 0) s_lc[slot][e] = v;
+  const int t = (blockIdx.x / noct) * kSelWarps + warp;
+  const bool valid = t < st.T;
+  uint4 xr[kSmallMaxChunks];
+  if (valid) {
+    const int m = src_of_token(st, t);
+    const uint4* x = reinterpret_cast<const uint4*>(st.src[m]) + (size_t)(t - st.row0[m]) * nc;
+#pragma unroll
+    for (int j = 0; j < kSmallMaxChunks; ++j)
+      if (lane + 32 * j < nc) xr[j] = __ldg(x + lane + 32 * j);
   }
-  __syncthreads();
-  if (sub != 0 || !valid) return;
+  __syncthreads();  // barrier initialised before anyone waits on it
+  const bool ok = mbar_wait(&bar, 0, &s_abort, err);  // every thread: the copy lands before the block exits
+  if (!valid || !ok) return;
+  float p[kOct];
+#pragma unroll
+  for (int i = 0; i < kOct; ++i) p[i] = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kSmallMaxChunks; ++j) {
+    const int c = lane + 32 * j;
+    if (c < nc) {
+      const uint4 a = xr[j];
+#pragma unroll
+      for (int i = 0; i < kOct; ++i)
+        if (i < ne) {
+          const uint4 b = s_w[i * nc + c];
+          p[i] = fma_bf16_lo(a.x, b.x, p[i]); p[i] = fma_bf16_hi(a.x, b.x, p[i]);
+          p[i] = fma_bf16_lo(a.y, b.y, p[i]); p[i] = fma_bf16_hi(a.y, b.y, p[i]);
+          p[i] = fma_bf16_lo(a.z, b.z, p[i]); p[i] = fma_bf16_hi(a.z, b.z, p[i]);
+          p[i] = fma_bf16_lo(a.w, b.w, p[i]); p[i] = fma_bf16_hi(a.w, b.w, p[i]);
+        }
+    }
+  }
+  float v = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kOct; ++i) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) p[i] = p[i] + __shfl_xor_sync(0xffffffffu, p[i], o);
+    if (lane == i) v = p[i];
+  }
+  if (lane < ne) {
+    if (bias) v = __fadd_rn(v, __ldg(bias + e0 + lane));
+    logits[(size_t)t * E + e0 + lane] = v;
+  }
+  __threadfence();
+  int last = 0;
+  if (lane == 0) last = atomicAdd(ticket + t, 1) == noct - 1;
+  if (!__shfl_sync(0xffffffffu, last, 0)) return;
+  __threadfence();
   float lc[PER];
-#pragma unroll
-  for (int q = 0; q < PER; ++q) {
-    const int e = lane + 32 * q;
-    lc[q] = e < E ? s_lc[slot][e] : -INFINITY;
-  }
-  // logits row for inspection: canonical where computed, tensor-core estimate elsewhere
-#pragma unroll
-  for (int q = 0; q < PER; ++q) {
-    const int e = lane + 32 * q;
-    if (e < E) {
-      const bool isc = all || ((cmask[q] >> lane) & 1u);
-      a.logits[(size_t)t * E + e] = isc ? lc[q] : est[q];
-    }
-  }
-  // top-k among the exact values (non-candidates are -inf and never win)
   bool tk[PER];
 #pragma unroll
-  for (int q = 0; q < PER; ++q) tk[q] = taken[q] || !(all || ((cmask[q] >> lane) & 1u));
-  float sel_v[kMaxK];
-  int sel_i[kMaxK];
-#pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
-    if (j >= k) break;
-    float bv;
-    int bi;
-    warp_best<PER>(lc, tk, lane, bv, bi);
-    sel_v[j] = bv;
-    sel_i[j] = bi;
-#pragma unroll
-    for (int q = 0; q < PER; ++q)
-      if (lane + 32 * q == bi) tk[q] = true;
+  for (int q = 0; q < PER; ++q) {
+    const int e = lane + 32 * q;
+    tk[q] = e >= E;
+    lc[q] = e < E ? __ldcg(logits + (size_t)t * E + e) : -INFINITY;
   }
-  if (lane == 0) {
-    float den = 0.0f, ex[kMaxK];
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      if (j >= k) break;
-      ex[j] = expf(sel_v[j] - sel_v[0]);
-      den += ex[j];
-    }
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      if (j >= k) break;
-      a.topk_idx[(size_t)t * k + j] = sel_i[j];
-      a.topk_w[(size_t)t * k + j] = ex[j] / den;
-    }
-  }
+  write_topk<PER>(lc, tk, k, lane, topk_idx + (size_t)t * k, topk_w + (size_t)t * k);
+  if (lane == 0) ticket[t] = 0;
 }
 
 __global__ void wnorm_kernel(const uint16_t* __restrict__ wrT, int H, int E, float* __restrict__ wnorm) {
@@ -545,7 +515,9 @@ __global__ void wnorm_kernel(const uint16_t* __restrict__ wrT, int H, int E, flo
 }  // namespace
 
 cudaError_t router_tc_setup() {
-  return cudaFuncSetAttribute(router_logits_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRDynSmem);
+  cudaError_t e = cudaFuncSetAttribute(router_logits_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRDynSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmallDynSmem);
 }
 
 cudaError_t launch_router_wnorm(const void* wrT, int H, int E, float* wnorm, cudaStream_t s) {
@@ -569,6 +541,13 @@ cudaError_t launch_router_tc(const SrcTable& st, const void* wrT, const float* b
                              cudaStream_t s) {
   const int T = st.T;
   if (T == 0) return cudaSuccess;
+  const int noct = (d.E + kOct - 1) / kOct;
+  if ((long)noct * ((T + kSelWarps - 1) / kSelWarps) <= (long)kSmallRouterWaves * num_sms && d.H <= kSmallMaxH) {
+    router_small_kernel<<<noct * ((T + kSelWarps - 1) / kSelWarps), 32 * kSelWarps,
+                          (size_t)kOct * d.H * 2, s>>>(st, static_cast<const uint16_t*>(wrT), bias, d.H, d.E, d.k,
+                                                       ws.logits, ws.topk_idx, ws.topk_w, ws.tok_ticket, ws.err);
+    return cudaGetLastError();
+  }
   stage_x_kernel<<<(T + 7) / 8, 256, 0, s>>>(st, d.H, static_cast<uint16_t*>(ws.Xc), ws.xnorm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -600,16 +579,7 @@ cudaError_t launch_router_tc(const SrcTable& st, const void* wrT, const float* b
   sa.logits = ws.logits;
   sa.topk_idx = ws.topk_idx;
   sa.topk_w = ws.topk_w;
-  // warps per token: the most (up to 8) that still leaves about one warp per
-  // token once 32 warps per SM are busy
-  int wpt = 8;
-  while (wpt > 1 && (long)T * wpt > 32l * num_sms) wpt >>= 1;
-  const int tok = kSelWarps / wpt;
-  const int blocks = (T + tok - 1) / tok;
-  if (wpt == 8) router_select_kernel<8><<<blocks, 32 * kSelWarps, 0, s>>>(sa);
-  else if (wpt == 4) router_select_kernel<4><<<blocks, 32 * kSelWarps, 0, s>>>(sa);
-  else if (wpt == 2) router_select_kernel<2><<<blocks, 32 * kSelWarps, 0, s>>>(sa);
-  else router_select_warp_kernel<<<blocks, 32 * kSelWarps, 0, s>>>(sa);
+  router_select_warp_kernel<<<(T + kSelWarps - 1) / kSelWarps, 32 * kSelWarps, 0, s>>>(sa);
   return cudaGetLastError();
 }
 

@@ -141,11 +141,13 @@ int afd_ffn_forward_pipelined(afd_ffn_t h, void* stream, int n_micro, const void
                               const int* src_counts_host, int M, void* const* out_ptrs_dev);
 
 /* End-to-end call with HOST buffers: copies each source to the device
- * (one cudaMemcpyAsync per buffer), runs afd_ffn_forward, copies each output
- * back, and synchronises `stream` before returning.  Pinned host memory makes
- * the copies asynchronous DMA; pageable memory works but is slower.  The
- * staging buffers are part of the handle's workspace. */
-int afd_ffn_forward_host(afd_ffn_t h, void* stream, const void* const* src_ptrs_host,
+ * (one cudaMemcpyAsync per buffer), runs afd_ffn_forward (n_micro == 1) or
+ * afd_ffn_forward_pipelined (n_micro in [2, AFD_MAX_MICRO]), copies each
+ * output back, and synchronises `stream` before returning.  Pinned host
+ * memory makes the copies asynchronous DMA; pageable memory works but is
+ * slower.  The staging buffers are part of the handle's workspace.  n_micro
+ * outside [1, AFD_MAX_MICRO] returns AFD_EINVAL. */
+int afd_ffn_forward_host(afd_ffn_t h, void* stream, int n_micro, const void* const* src_ptrs_host,
                          const int* src_counts_host, int M, void* const* out_ptrs_host);
 
 /* Copy the routing of the last forward (workspace 0) into caller device

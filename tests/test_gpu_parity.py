@@ -101,6 +101,13 @@ def test_forward_host_equals_device():
     layer.forward_host(hs, ho)
     for x, y in zip(dev, ho):
         assert torch.equal(x.cpu(), y)
+    # the pipelined path through host buffers equals the single pass bit for bit
+    ho3 = [torch.empty_like(s).pin_memory() for s in hs]
+    layer.forward_host(hs, ho3, n_micro=3)
+    for x, y in zip(dev, ho3):
+        assert torch.equal(x.cpu(), y)
+    with pytest.raises(afd.AfdError):
+        layer.forward_host(hs, ho3, n_micro=0)
 
 
 def test_empty_batch_is_noop():
@@ -174,7 +181,7 @@ def test_qwen3_fp8_full_size_sampled():
     assert_close(c, out_to_f64(outs)[tokens], ref_to_f64(c, ref["out"]))
 
 
-@pytest.mark.parametrize("B", [64, 512])
+@pytest.mark.parametrize("B", [64, 256, 512])
 def test_dsv3_fp8_zipf_sampled(B):
     """DeepSeek-V3 shapes, Zipf-biased routing, shared expert; T = 8 x B."""
     c = synth.CONFIGS["dsv3_fp8"].with_batch(B, 8)
@@ -198,11 +205,22 @@ def test_step3_bf16_three_microbatches_sampled():
         assert torch.equal(x, y)
 
 
+def test_small_batch_router_logits_all_canonical():
+    """Up to 512 tokens the router computes every logit in the canonical order
+    (no tensor-core estimate): all T*E logits equal the oracle's bit for bit."""
+    c = synth.CONFIGS["qwen3_bf16"].with_batch(197, 2)
+    layer, srcs, outs, r, ref = run_case(c, [c.B] * c.M)
+    got = r["logits"].cpu().numpy().reshape(c.T, c.E)
+    assert np.array_equal(got.view(np.uint32), ref["logits"].view(np.uint32))
+    assert_routing_exact(c, r, ref, c.T)
+    assert_close(c, out_to_f64(outs), ref_to_f64(c, ref["out"]))
+
+
 def test_tensor_core_router_error_within_guard_band():
     """The tensor-core logits that are not recomputed exactly must lie within
     the bound the candidate rule assumes, with a wide margin (the model's
     2^-21 per accumulation step is itself conservative)."""
-    c = synth.CONFIGS["qwen3_bf16"].with_batch(197, 2)
+    c = synth.CONFIGS["qwen3_bf16"].with_batch(395, 2)  # T = 790: above the small-batch router
     counts = [c.B] * c.M
     layer, srcs, outs, r, ref = run_case(c, counts)
     T, E = c.T, c.E
