@@ -25,13 +25,13 @@
 // adjacent so concurrently running CTAs share the weight tile in L2.  The
 // kernel is persistent: grid = SM count, CTA c takes items c, c+grid, ...
 //
-// Warp roles (352 threads): warp 0 lane 0 streams weight tiles into their
-// own ring (L2 evict-first); warp 10 lane 0 streams the token tiles into a
+// Warp roles (608 threads): warp 0 lane 0 streams weight tiles into their
+// own ring (L2 evict-first); warp 18 lane 0 streams the token tiles into a
 // second, shallower ring (evict-last); warp 1 owns TMEM and lane 0 issues
-// tcgen05.mma; warps 2-9 are the epilogue (warp w reads TMEM lanes
-// 32*(w%4) .. +31; the two warps of a lane quarter take alternate 32-token
-// chunks).  With one accumulator buffer (256-token tiles) the next item's
-// MMAs wait for the epilogue, so it runs on two warps per SM sub-partition
+// tcgen05.mma; warps 2-17 are the epilogue (warp w reads TMEM lanes
+// 32*(w%4) .. +31; the four warps of a lane quarter take every fourth 32-token
+// chunk).  With one accumulator buffer (256-token tiles) the next item's
+// MMAs wait for the epilogue, so it runs on four warps per SM sub-partition
 // and uses the fast exponential and division for SiLU (their error is far
 // below bf16 rounding).  Separate rings keep more weight bytes in flight than a
 // ring of (weights + tokens) stages would in the same shared memory: the
@@ -49,8 +49,9 @@ namespace {
 constexpr int kRowBytes = 128;               // one 128-byte swizzle row of K
 constexpr int kATile = kGemmBM * kRowBytes;  // 16 KB
 constexpr int kBBoxRows = 32;                // rows per TMA box of B
-constexpr int kThreads = 352;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;
+constexpr int kTokWarp = 2 + kEpiWarps;       // token producer
+constexpr int kThreads = 32 * (kTokWarp + 1);  // 608
 constexpr int kWTileBytes = 2 * kATile;      // one weight stage: two 128-row tiles
 constexpr int kPfSteps = 4;                  // weight K blocks prefetched into L2 ahead of the loads
 
@@ -175,9 +176,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total = args.MT * s_tb[G];
   volatile int* abort = &s_abort;
 
-  if (warp == 0 || warp == 10) {
+  if (warp == 0 || warp == kTokWarp) {
     if (lane == 0) {
-      // ---------------- TMA producers: warp 0 weights, warp 10 tokens
+      // ---------------- TMA producers: warp 0 weights, warp kTokWarp tokens
       const bool wprod = warp == 0;
       const int nst = wprod ? kWS : kXS;
       uint64_t* fb = wprod ? wfull : xfull;
@@ -287,8 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_cycles(drain, 0, kDrainCycles);
     }
   } else if (warp >= 2 && warp < 2 + kEpiWarps) {
-    // ---------------- epilogue: warps 2..9
-    const int quad = warp & 3, half = (warp - 2) >> 2;
+    // ---------------- epilogue: warps 2..17
+    const int quad = warp & 3, part = (warp - 2) >> 2;  // lane quarter; which of every 4 chunks
     const int r = quad * 32 + lane;  // row of the 128-row MMA tile
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
     uint32_t ic = 0;
@@ -298,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&tfull[a], (ic / kAbuf) & 1u, abort, args.err)) break;
       tc_fence_after();
       const uint32_t t_buf = t_lane + a * (2u * BN);
-      for (int c = 32 * half; c < it.nrows; c += 64) {
+      for (int c = 32 * part; c < it.nrows; c += 32 * (kEpiWarps / 4)) {
         float d0[32], d1[32];
         tmem_ld_32x32b_x32(t_buf + (uint32_t)c, d0);
         tmem_ld_32x32b_x32(t_buf + (uint32_t)(BN + c), d1);
