@@ -390,7 +390,7 @@ def run_ours(args, world, rank, local):
         "kernel_ms": k_avg,
         "e2e": {"value": world * T / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": io_bytes,
                 "d2h_bytes_per_step": io_bytes, "api": "afd_ffn_forward_host"},
-        "gpu_launches": args.steps * layer.launches_per_forward * args.n_micro,
+        "gpu_launches": args.steps * sum(layer.launches_per_forward(sz) for sz in sizes),
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

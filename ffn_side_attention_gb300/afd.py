@@ -74,7 +74,7 @@ def lib():
         L.afd_ffn_profile_begin.restype = ip
         L.afd_ffn_profile_end.argtypes = [vp, vp, vp]
         L.afd_ffn_profile_end.restype = ip
-        L.afd_ffn_launches_per_forward.argtypes = [vp]
+        L.afd_ffn_launches_per_forward.argtypes = [vp, ip]
         L.afd_ffn_launches_per_forward.restype = ip
         L.afd_ffn_device_bytes.argtypes = [vp]
         L.afd_ffn_device_bytes.restype = C.c_size_t
@@ -150,8 +150,11 @@ def afd_ffn_profile_end(h):
     return list(ms), n.value
 
 
-def afd_ffn_launches_per_forward(h) -> int:
-    return int(lib().afd_ffn_launches_per_forward(h))
+def afd_ffn_launches_per_forward(h, T) -> int:
+    n = int(lib().afd_ffn_launches_per_forward(h, int(T)))
+    if n < 0:
+        raise AfdError(n, "launches_per_forward: bad handle or T")
+    return n
 
 
 def afd_ffn_device_bytes(h) -> int:
@@ -262,9 +265,9 @@ class MoELayer:
         ms, n = afd_ffn_profile_end(self.handle)
         return dict(zip(KERNEL_NAMES, ms)), n
 
-    @property
-    def launches_per_forward(self):
-        return afd_ffn_launches_per_forward(self.handle)
+    def launches_per_forward(self, T):
+        """Kernel launches one forward of T tokens enqueues."""
+        return afd_ffn_launches_per_forward(self.handle, T)
 
     @property
     def device_bytes(self):

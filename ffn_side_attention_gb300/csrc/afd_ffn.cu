@@ -569,11 +569,14 @@ int afd_ffn_profile_end(afd_ffn_t h, double* ms_per_kernel, int* n_forwards) {
   return AFD_OK;
 }
 
-// router (stage, tensor-core logits, select for bf16/fp8; one kernel for fp32),
-// two routing-table kernels, pack, two GEMMs, combine
-int afd_ffn_launches_per_forward(afd_ffn_t h) {
-  if (!h) return AFD_EINVAL;
-  return AFD_NUM_KERNELS + 1 + (h->cfg.dtype == AFD_FP32 ? 0 : 2);
+// router (one kernel for fp32 and small bf16/fp8 batches; stage, tensor-core
+// logits and select otherwise), two routing-table kernels, pack, two GEMMs,
+// combine
+int afd_ffn_launches_per_forward(afd_ffn_t h, int T) {
+  if (!h || T < 1) return AFD_EINVAL;
+  const afd::LayerDims& d = h->dims;
+  const int router = d.dtype == AFD_FP32 ? 1 : afd::router_tc_launches(d, T, h->num_sms);
+  return router + 2 /* routing tables */ + 1 /* pack */ + 2 /* GEMMs */ + 1 /* combine */;
 }
 
 const char* afd_ffn_last_error(afd_ffn_t h) { return h ? h->err.c_str() : "handle is NULL"; }

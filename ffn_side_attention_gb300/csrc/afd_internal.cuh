@@ -83,6 +83,7 @@ cudaError_t launch_router(const SrcTable& st, const void* wrT, const float* bias
                           Workspace& ws, cudaStream_t s);
 cudaError_t router_setup();  // opt-in shared memory sizes (once per process)
 cudaError_t router_tc_setup();
+int router_tc_launches(const LayerDims& d, int T, int num_sms);  // kernels launch_router_tc enqueues
 cudaError_t launch_router_wnorm(const void* wrT, int H, int E, float* wnorm, cudaStream_t s);
 cudaError_t launch_router_tc(const SrcTable& st, const void* wrT, const float* bias, const float* wnorm,
                              const CUtensorMap* tm_wr, const LayerDims& d, Workspace& ws, int num_sms,

@@ -536,13 +536,20 @@ int router_tc_splits(const LayerDims& d, int T, int num_sms) {
   return splits;
 }
 
+static bool router_small_path(const LayerDims& d, int T, int num_sms) {
+  const int noct = (d.E + kOct - 1) / kOct;
+  return (long)noct * ((T + kSelWarps - 1) / kSelWarps) <= (long)kSmallRouterWaves * num_sms && d.H <= kSmallMaxH;
+}
+
+int router_tc_launches(const LayerDims& d, int T, int num_sms) { return router_small_path(d, T, num_sms) ? 1 : 3; }
+
 cudaError_t launch_router_tc(const SrcTable& st, const void* wrT, const float* bias, const float* wnorm,
                              const CUtensorMap* tm_wr, const LayerDims& d, Workspace& ws, int num_sms,
                              cudaStream_t s) {
   const int T = st.T;
   if (T == 0) return cudaSuccess;
-  const int noct = (d.E + kOct - 1) / kOct;
-  if ((long)noct * ((T + kSelWarps - 1) / kSelWarps) <= (long)kSmallRouterWaves * num_sms && d.H <= kSmallMaxH) {
+  if (router_small_path(d, T, num_sms)) {
+    const int noct = (d.E + kOct - 1) / kOct;
     router_small_kernel<<<noct * ((T + kSelWarps - 1) / kSelWarps), 32 * kSelWarps,
                           (size_t)kOct * d.H * 2, s>>>(st, static_cast<const uint16_t*>(wrT), bias, d.H, d.E, d.k,
                                                        ws.logits, ws.topk_idx, ws.topk_w, ws.tok_ticket, ws.err);

@@ -188,8 +188,10 @@ const char* afd_ffn_last_error(afd_ffn_t h);
 int afd_ffn_profile_begin(afd_ffn_t h);
 int afd_ffn_profile_end(afd_ffn_t h, double* ms_per_kernel, int* n_forwards);
 
-/* Number of kernel launches one afd_ffn_forward of T > 0 tokens enqueues. */
-int afd_ffn_launches_per_forward(afd_ffn_t h);
+/* Number of kernel launches one afd_ffn_forward of T > 0 tokens enqueues
+ * (it depends on T: small batches route in one launch, larger ones in three).
+ * Returns AFD_EINVAL for a NULL handle or T < 1. */
+int afd_ffn_launches_per_forward(afd_ffn_t h, int T);
 
 /* Bytes of device memory the handle holds (weights + workspaces). */
 size_t afd_ffn_device_bytes(afd_ffn_t h);

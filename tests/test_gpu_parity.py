@@ -110,6 +110,18 @@ def test_forward_host_equals_device():
         layer.forward_host(hs, ho3, n_micro=0)
 
 
+def test_launches_per_forward_by_batch():
+    """One router launch for small batches, three (stage, logits, select) for
+    large ones; then 2 routing, pack, 2 GEMMs, combine."""
+    c = synth.CONFIGS["qwen3_bf16"]
+    w = synth.make_weights(c, "cuda")
+    layer = make_layer(c, w, max_tokens=4096, max_sources=8)
+    assert layer.launches_per_forward(6) == 7
+    assert layer.launches_per_forward(3160) == 9
+    with pytest.raises(afd.AfdError):
+        layer.launches_per_forward(0)
+
+
 def test_empty_batch_is_noop():
     c = _small()
     w = synth.make_weights(c, "cuda")
