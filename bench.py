@@ -131,6 +131,10 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ distributed
+# One process per GPU (torchrun), each an independent replica of the layer:
+# the path has no exchange step, so the only collectives are the barrier
+# around the timed region and the max of the ranks' times.  NCCL on GPUs,
+# gloo where there is no GPU (the multi-rank logic is tested that way).
 def dist_setup(n_gpus):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -138,17 +142,27 @@ def dist_setup(n_gpus):
     if world > 1:
         import torch.distributed as dist
 
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
     return world, rank, local
 
 
+def _reduce_device():
+    import torch.distributed as dist
+
+    return "cuda" if dist.get_backend() == "nccl" else "cpu"
+
+
 def barrier_max(world, seconds: float) -> float:
+    """Largest of the ranks' times (every rank gets it)."""
     if world == 1:
         return seconds
     import torch.distributed as dist
 
-    t = torch.tensor([seconds], device="cuda", dtype=torch.float64)
+    t = torch.tensor([seconds], device=_reduce_device(), dtype=torch.float64)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -158,6 +172,11 @@ def barrier(world):
         import torch.distributed as dist
 
         dist.barrier()
+
+
+def job_rate(world, units_per_rank, seconds):
+    """Whole-job throughput: the units all replicas processed / the slowest rank's time."""
+    return world * units_per_rank / seconds
 
 
 # ------------------------------------------------------------------ CPU oracle leg
@@ -370,7 +389,7 @@ def run_ours(args, world, rank, local):
     io_bytes = T * cfg.H * (4 if cfg.dtype == "fp32" else 2)
 
     line = {
-        "metric": METRIC, "value": world * T / step_s, "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": job_rate(world, T, step_s), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": {"fp32": "f32", "bf16": "bf16", "fp8": "e4m3"}[cfg.dtype], "data": "synthetic",
@@ -388,7 +407,7 @@ def run_ours(args, world, rank, local):
                      "peak": rf_peak, "unit": rf_unit, "frac": achieved / rf_peak if achieved else None,
                      "traffic": traffic, "peak_src": peak_src},
         "kernel_ms": k_avg,
-        "e2e": {"value": world * T / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": io_bytes,
+        "e2e": {"value": job_rate(world, T, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": io_bytes,
                 "d2h_bytes_per_step": io_bytes, "api": "afd_ffn_forward_host"},
         "gpu_launches": args.steps * sum(layer.launches_per_forward(sz) for sz in sizes),
         "clocks": clocks,

@@ -1,0 +1,60 @@
+"""bench.py's multi-rank logic (independent replicas: barrier around the
+timed region, max of the ranks' times, whole-job rate) with two gloo ranks on
+the CPU, launched the way torchrun sets the environment."""
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank), CUDA_VISIBLE_DEVICES="")
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import bench
+
+    w, r, local = bench.dist_setup(world)
+    bench.barrier(w)
+    slowest = bench.barrier_max(w, 0.25 + 0.5 * r)  # rank 1 is the slow one
+    rate = bench.job_rate(w, 1000, slowest)
+    q.put((r, w, local, dist.get_backend(), slowest, rate))
+    bench.barrier(w)
+    dist.destroy_process_group()
+
+
+def test_two_gloo_replicas_take_the_slowest_rank():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [o[0] for o in out] == [0, 1]
+    for r, w, local, backend, slowest, rate in out:
+        assert w == 2 and local == r and backend == "gloo"
+        assert slowest == pytest.approx(0.75)       # max over ranks, seen by both
+        assert rate == pytest.approx(2 * 1000 / 0.75)  # both replicas' units over the slowest time
+
+
+def test_single_process_needs_no_process_group():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    assert bench.barrier_max(1, 0.5) == 0.5
+    assert bench.job_rate(1, 300, 0.1) == pytest.approx(3000)
