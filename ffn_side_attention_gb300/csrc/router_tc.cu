@@ -37,6 +37,7 @@ namespace {
 
 constexpr int kMaxK = 16;
 constexpr int kMaxCand = 64;
+constexpr int kPer = 8;  // router entries per lane: E <= 256 routed experts
 constexpr int kSmallRouterWaves = 8;  // small-batch path while its grid is at most this many waves
 
 // ---------------------------------------------------------------- 1. stage
@@ -240,6 +241,37 @@ __device__ __forceinline__ float canonical_dot_warp(const uint16_t* __restrict__
   return p;
 }
 
+// Two canonical dots of one token row against two expert rows: one pass over
+// the chunks loads x once and advances both chains (each in the order above).
+__device__ __forceinline__ float chain8(const uint4& a, const uint4& b, float p) {
+  p = fma_bf16_lo(a.x, b.x, p); p = fma_bf16_hi(a.x, b.x, p);
+  p = fma_bf16_lo(a.y, b.y, p); p = fma_bf16_hi(a.y, b.y, p);
+  p = fma_bf16_lo(a.z, b.z, p); p = fma_bf16_hi(a.z, b.z, p);
+  p = fma_bf16_lo(a.w, b.w, p); p = fma_bf16_hi(a.w, b.w, p);
+  return p;
+}
+__device__ __forceinline__ void canonical_dot2_warp(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w1,
+                                                    const uint16_t* __restrict__ w2, int H, int lane, float& v1,
+                                                    float& v2) {
+  const int nc = H >> 3;
+  const uint4* xa = reinterpret_cast<const uint4*>(x);
+  const uint4* wa = reinterpret_cast<const uint4*>(w1);
+  const uint4* wb = reinterpret_cast<const uint4*>(w2);
+  float p1 = 0.0f, p2 = 0.0f;
+  for (int c = lane; c < nc; c += 32) {
+    const uint4 a = __ldg(xa + c), b = __ldg(wa + c), d = __ldg(wb + c);
+    p1 = chain8(a, b, p1);
+    p2 = chain8(a, d, p2);
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    p1 = p1 + __shfl_xor_sync(0xffffffffu, p1, o);
+    p2 = p2 + __shfl_xor_sync(0xffffffffu, p2, o);
+  }
+  v1 = p1;
+  v2 = p2;
+}
+
 __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
@@ -321,28 +353,33 @@ struct SelectArgs {
 
 // One warp per token (8 tokens per block): for many tokens, every warp runs
 // its token from the bounds to the weights without waiting for the others.
-__global__ void __launch_bounds__(256) router_select_warp_kernel(const SelectArgs a) {
-  constexpr int PER = (kMaxExperts + 31) / 32;  // 8 entries per lane for E <= 256
+// MINB = blocks per SM the register budget is sized for: 2 gives each warp
+// registers for two dot chains at once, 3 fits 50% more tokens per wave (the
+// launcher takes 3 only when that turns a second wave into none).
+template <int MINB>
+__global__ void __launch_bounds__(256, MINB) router_select_warp_kernel(const SelectArgs a) {
+  constexpr int PER = kPer;
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= a.T) return;
   const int E = a.E, k = a.k;
   const uint16_t* x = a.Xc + (size_t)t * a.H;
   const float xn = __ldg(a.xnorm + t);
-  float est[PER], lo[PER], hi[PER];  // estimate and its bounds
+  float* lrow = a.logits + (size_t)t * E;
+  float lo[PER], hi[PER];  // bounds of the estimate (the estimate itself goes to the logits row now)
   bool taken[PER];
 #pragma unroll
   for (int q = 0; q < PER; ++q) {
     const int e = lane + 32 * q;
     taken[q] = e >= E;
-    est[q] = lo[q] = hi[q] = 0.0f;
+    lo[q] = hi[q] = 0.0f;
     if (e < E) {
       float s = 0.0f;
       for (int sp = 0; sp < a.splits; ++sp) s += __ldcg(a.part + ((size_t)sp * a.T + t) * E + e);
       const float bs = a.bias ? __ldg(a.bias + e) : 0.0f;
       if (a.bias) s = __fadd_rn(s, bs);
       const float b = a.g * xn * __ldg(a.wnorm + e) + 0x1p-22f * (fabsf(s) + fabsf(bs)) + 0x1p-100f;
-      est[q] = s;
+      lrow[e] = s;  // replaced by the canonical value below if e is a candidate
       lo[q] = s - b;
       hi[q] = s + b;
     }
@@ -372,29 +409,38 @@ __global__ void __launch_bounds__(256) router_select_warp_kernel(const SelectArg
     ncand += __popc(cmask[q]);
   }
   const bool all = ncand > kMaxCand;
-  // canonical logits of the candidates (all experts when too many)
+  // canonical logits of the candidates (all experts when too many), two at a time
   float lc[PER];
 #pragma unroll
   for (int q = 0; q < PER; ++q) {
     lc[q] = -INFINITY;
     unsigned msk = all ? __ballot_sync(0xffffffffu, !taken[q]) : cmask[q];
     while (msk) {
-      const int src = __ffs(msk) - 1;
+      const int s1 = __ffs(msk) - 1;
       msk &= msk - 1;
-      const int e = src + 32 * q;
-      float v = canonical_dot_warp<1>(x, a.wrT + (size_t)e * a.H, a.H, lane);
-      if (a.bias) v = __fadd_rn(v, __ldg(a.bias + e));
-      if (lane == src) lc[q] = v;
+      const int e1 = s1 + 32 * q;
+      float v1, v2 = 0.0f;
+      int s2 = -1;
+      if (msk) {
+        s2 = __ffs(msk) - 1;
+        msk &= msk - 1;
+        canonical_dot2_warp(x, a.wrT + (size_t)e1 * a.H, a.wrT + (size_t)(s2 + 32 * q) * a.H, a.H, lane, v1, v2);
+      } else {
+        v1 = canonical_dot_warp<1>(x, a.wrT + (size_t)e1 * a.H, a.H, lane);
+      }
+      if (a.bias) v1 = __fadd_rn(v1, __ldg(a.bias + e1));
+      if (lane == s1) lc[q] = v1;
+      if (s2 >= 0) {
+        if (a.bias) v2 = __fadd_rn(v2, __ldg(a.bias + s2 + 32 * q));
+        if (lane == s2) lc[q] = v2;
+      }
     }
   }
-  // logits row for inspection: canonical where computed, tensor-core estimate elsewhere
+  // logits row for inspection: canonical where computed (the estimate stays elsewhere)
 #pragma unroll
   for (int q = 0; q < PER; ++q) {
     const int e = lane + 32 * q;
-    if (e < E) {
-      const bool isc = all || ((cmask[q] >> lane) & 1u);
-      a.logits[(size_t)t * E + e] = isc ? lc[q] : est[q];
-    }
+    if (e < E && (all || ((cmask[q] >> lane) & 1u))) lrow[e] = lc[q];
   }
   // top-k among the exact values (non-candidates are -inf and never win)
   bool tk[PER];
@@ -422,7 +468,7 @@ __global__ void __launch_bounds__(32 * kSelWarps, 1)
     router_small_kernel(const SrcTable st, const uint16_t* __restrict__ wrT, const float* __restrict__ bias, int H,
                         int E, int k, float* __restrict__ logits, int32_t* __restrict__ topk_idx,
                         float* __restrict__ topk_w, int32_t* __restrict__ ticket, int* err) {
-  constexpr int PER = (kMaxExperts + 31) / 32;
+  constexpr int PER = kPer;
   extern __shared__ __align__(16) uint4 s_w[];  // [kOct][H/8]
   __shared__ __align__(8) uint64_t bar;
   __shared__ int s_abort;
@@ -586,7 +632,11 @@ cudaError_t launch_router_tc(const SrcTable& st, const void* wrT, const float* b
   sa.logits = ws.logits;
   sa.topk_idx = ws.topk_idx;
   sa.topk_w = ws.topk_w;
-  router_select_warp_kernel<<<(T + kSelWarps - 1) / kSelWarps, 32 * kSelWarps, 0, s>>>(sa);
+  const int blocks = (T + kSelWarps - 1) / kSelWarps;
+  if (blocks > 2 * num_sms && blocks <= 3 * num_sms)
+    router_select_warp_kernel<3><<<blocks, 32 * kSelWarps, 0, s>>>(sa);
+  else
+    router_select_warp_kernel<2><<<blocks, 32 * kSelWarps, 0, s>>>(sa);
   return cudaGetLastError();
 }
 
