@@ -283,34 +283,38 @@ def run_ours(args, world, rank, local):
             torch.cuda.synchronize()
     torch.cuda.synchronize()
 
-    # Per-kernel times come from CUDA events recorded around each kernel of the
-    # timed steps themselves (one stream).  The library creates those events on
-    # first use, so an untimed pass creates them before the timed region.
+    # The value: K steps with nothing recorded between the kernels (each kernel's
+    # launch overlaps the previous one's tail through programmatic dependent launch).
     n_mb = max(args.n_micro, 1)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    elapsed = barrier_max(world, ev0.elapsed_time(ev1) / 1e3)
+    clocks = sampler.stop() if sampler is not None else None
+    layer.check()
+    ms_step = elapsed / max(args.steps, 1) * 1e3
+
+    # Per-kernel times (the roofline's kernel): K more steps on one stream with CUDA
+    # events recorded around every kernel.  The events serialise the launches, so these
+    # steps run slightly slower than the value's.  The library creates the events on
+    # first use, so an untimed pass creates them first.
     prof_timed = n_mb == 1
     if prof_timed:
         layer.profile_begin()
         for i in range(args.steps):
             step(i)
         layer.profile_end()
-
-    barrier(world)
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    if prof_timed:
+        torch.cuda.synchronize()
         layer.profile_begin()
-    for i in range(args.steps):
-        step(i)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    if prof_timed:
+        for i in range(args.steps):
+            step(i)
         kms, nf = layer.profile_end()
-    barrier(world)
-    elapsed = barrier_max(world, ev0.elapsed_time(ev1) / 1e3)
-    clocks = sampler.stop() if sampler is not None else None
-    layer.check()
-    ms_step = elapsed / max(args.steps, 1) * 1e3
 
 
     # routing statistics of input set 0 (touched experts), per micro-batch:

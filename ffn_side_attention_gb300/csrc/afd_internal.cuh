@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <utility>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -73,6 +74,34 @@ struct Workspace {
   CUtensorMap tm_P, tm_H;       // B operands of the two GEMMs
   bool ready = false;
 };
+
+// ---------------------------------------------------------------- launches
+// Programmatic dependent launch.  Every kernel of a forward starts with
+// pdl_begin(): griddepcontrol.wait returns once the previous kernel of the
+// stream has completed and its writes are visible (a no-op for a normal
+// launch), so nothing upstream is read early; launch_dependents then lets the
+// next kernel's CTAs be scheduled while this one runs, which hides the next
+// launch's latency behind this kernel's tail.  Completion order is unchanged:
+// each kernel waits for its predecessor, hence for every earlier one.
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                            Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------- launchers
 struct LayerDims {

@@ -125,6 +125,7 @@ __device__ __forceinline__ bool epi_sync(uint64_t* bar, uint32_t& phase, int lan
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1,
                     const __grid_constant__ CUtensorMap tmX, const Fp8Args args) {
+  pdl_begin();
   extern __shared__ uint8_t dyn_smem[];
   uint8_t* smem = dyn_smem + ((1024u - (smem_u32(dyn_smem) & 1023u)) & 1023u);
 
@@ -416,7 +417,11 @@ cudaError_t launch_gemm_fp8(const LayerDims& d, int T, const TcWeights& w, Works
     a.mode = 0;
     const long items_ub = tiles_ub * a.MT;
     const int grid = (int)(items_ub < num_sms ? items_ub : num_sms);
-    gemm_fp8_kernel<<<grid, kThreads, kDynSmem, s>>>(*w.tm_wg, *w.tm_wu, ws.tm_P, a);
+    {
+      const cudaError_t e_ = launch_k(gemm_fp8_kernel, dim3(grid), dim3(kThreads), kDynSmem, s, *w.tm_wg,
+                                      *w.tm_wu, ws.tm_P, a);
+      if (e_ != cudaSuccess) return e_;
+    }
     return cudaGetLastError();
   }
   // down: K = I, items of 256 output columns
@@ -435,7 +440,11 @@ cudaError_t launch_gemm_fp8(const LayerDims& d, int T, const TcWeights& w, Works
   a.mode = 1;
   const long items_ub = tiles_ub * a.MT;
   const int grid = (int)(items_ub < num_sms ? items_ub : num_sms);
-  gemm_fp8_kernel<<<grid, kThreads, kDynSmem, s>>>(*w.tm_wd, *w.tm_wd, ws.tm_H, a);
+  {
+    const cudaError_t e_ = launch_k(gemm_fp8_kernel, dim3(grid), dim3(kThreads), kDynSmem, s, *w.tm_wd, *w.tm_wd,
+                                    ws.tm_H, a);
+    if (e_ != cudaSuccess) return e_;
+  }
   return cudaGetLastError();
 }
 

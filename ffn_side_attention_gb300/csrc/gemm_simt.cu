@@ -25,6 +25,7 @@ __device__ __forceinline__ int group_of_row(const int32_t* offsets, int G, int r
 __global__ void __launch_bounds__(128) simt_gateup_kernel(const float* __restrict__ P, const int32_t* __restrict__ offsets,
                                                           int G, int H, int I, const float* __restrict__ wg,
                                                           const float* __restrict__ wu, float* __restrict__ Hb) {
+  pdl_begin();
   const int r = blockIdx.x;
   const int i = blockIdx.y * 128 + threadIdx.x;
   const int e = group_of_row(offsets, G, r);
@@ -45,6 +46,7 @@ __global__ void __launch_bounds__(128) simt_gateup_kernel(const float* __restric
 __global__ void __launch_bounds__(128) simt_down_kernel(const float* __restrict__ Hb, const int32_t* __restrict__ offsets,
                                                         int G, int H, int I, const float* __restrict__ wd,
                                                         float* __restrict__ Y) {
+  pdl_begin();
   const int r = blockIdx.x;
   const int o = blockIdx.y * 128 + threadIdx.x;
   const int e = group_of_row(offsets, G, r);
@@ -119,12 +121,20 @@ cudaError_t launch_gemm_simt(const LayerDims& d, int T, const float* wg, const f
   if (rows == 0) return cudaSuccess;
   const int G = d.E + d.S;
   if (which == 0) {
-    simt_gateup_kernel<<<dim3(rows, (d.I + 127) / 128), 128, 0, s>>>(static_cast<const float*>(ws.P), ws.offsets,
-                                                                     G, d.H, d.I, wg, wu, static_cast<float*>(ws.Hb));
+    {
+      const cudaError_t e_ = launch_k(simt_gateup_kernel, dim3(dim3(rows, (d.I + 127) / 128)), dim3(128), 0, s,
+                                      static_cast<const float*>(ws.P), ws.offsets, G, d.H, d.I, wg, wu,
+                                      static_cast<float*>(ws.Hb));
+      if (e_ != cudaSuccess) return e_;
+    }
     return cudaGetLastError();
   }
-  simt_down_kernel<<<dim3(rows, (d.H + 127) / 128), 128, 0, s>>>(static_cast<const float*>(ws.Hb), ws.offsets, G,
-                                                                 d.H, d.I, wd, static_cast<float*>(ws.Y));
+  {
+    const cudaError_t e_ = launch_k(simt_down_kernel, dim3(dim3(rows, (d.H + 127) / 128)), dim3(128), 0, s,
+                                    static_cast<const float*>(ws.Hb), ws.offsets, G, d.H, d.I, wd,
+                                    static_cast<float*>(ws.Y));
+    if (e_ != cudaSuccess) return e_;
+  }
   return cudaGetLastError();
 }
 

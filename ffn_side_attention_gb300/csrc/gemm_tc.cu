@@ -119,6 +119,7 @@ template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                      const __grid_constant__ CUtensorMap tmB, const TcArgs args) {
+  pdl_begin();
   constexpr int kWS = TileCfg<BN>::kWStages, kXS = TileCfg<BN>::kXStages, kBTile = TileCfg<BN>::kBTile;
   constexpr uint32_t kAbuf = TileCfg<BN>::kAbuf;
   extern __shared__ uint8_t dyn_smem[];
@@ -392,7 +393,11 @@ static cudaError_t launch_bn(const LayerDims& d, int T, const TcWeights& w, Work
   }
   const long items_ub = tiles_ub * a.MT;
   const int grid = (int)(items_ub < num_sms ? items_ub : num_sms);
-  gemm_bf16_kernel<BN><<<grid, kThreads, TileCfg<BN>::kDynSmem, s>>>(*m0, *m1, *mb, a);
+  {
+    const cudaError_t e_ = launch_k(gemm_bf16_kernel<BN>, dim3(grid), dim3(kThreads), TileCfg<BN>::kDynSmem, s,
+                                    *m0, *m1, *mb, a);
+    if (e_ != cudaSuccess) return e_;
+  }
   return cudaGetLastError();
 }
 

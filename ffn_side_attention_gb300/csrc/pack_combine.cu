@@ -53,6 +53,7 @@ __device__ __forceinline__ int packed_rows(const int32_t* __restrict__ pos, int 
 // bf16 / fp32 layers: row copy.
 __global__ void __launch_bounds__(256) pack_copy_kernel(SrcTable st, const int32_t* __restrict__ pos, int T, int k,
                                                         int S, int row_bytes, uint8_t* __restrict__ P) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int nchunk = (row_bytes + 511) >> 9;  // 512 bytes per warp step
   const int nvec = row_bytes >> 4;
@@ -73,6 +74,7 @@ __global__ void __launch_bounds__(256) pack_copy_kernel(SrcTable st, const int32
 __global__ void __launch_bounds__(256) pack_fp8_kernel(SrcTable st, const int32_t* __restrict__ pos, int T, int k,
                                                        int S, int H, uint8_t* __restrict__ P,
                                                        float* __restrict__ P_scale) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int nblk = H >> 7;
   const int nchunk = H >> 8;  // H % 256 == 0: whole warp active
@@ -119,6 +121,7 @@ __global__ void __launch_bounds__(256) combine_bf16_kernel(SrcTable st, const in
                                                            const float* __restrict__ topk_w,
                                                            const uint16_t* __restrict__ Y, int T, int k_rt, int S,
                                                            int H) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int k = KC ? KC : k_rt;
   const int nchunk = H >> 8;
@@ -154,6 +157,7 @@ __global__ void __launch_bounds__(256) combine_bf16_kernel(SrcTable st, const in
 __global__ void __launch_bounds__(256) combine_f32_kernel(SrcTable st, const int32_t* __restrict__ pos,
                                                           const float* __restrict__ topk_w,
                                                           const float* __restrict__ Y, int T, int k, int S, int H) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < T; t += gridDim.x * 8) {
     float4* o = reinterpret_cast<float4*>(out_row(st, t, (size_t)H * 4));
@@ -189,9 +193,17 @@ cudaError_t launch_pack(const SrcTable& st, const LayerDims& d, int T, Workspace
   const int row_bytes = d.H * (d.dtype == AFD_FP32 ? 4 : 2);
   const int grid = grid_for(8, T * ((row_bytes + 511) / 512), num_sms);
   if (d.dtype == AFD_FP8_E4M3)
-    pack_fp8_kernel<<<grid, 256, 0, s>>>(st, ws.pos, T, d.k, d.S, d.H, static_cast<uint8_t*>(ws.P), ws.P_scale);
+    {
+      const cudaError_t e_ = launch_k(pack_fp8_kernel, dim3(grid), dim3(256), 0, s, st, ws.pos, T, d.k, d.S, d.H,
+                                      static_cast<uint8_t*>(ws.P), ws.P_scale);
+      if (e_ != cudaSuccess) return e_;
+    }
   else
-    pack_copy_kernel<<<grid, 256, 0, s>>>(st, ws.pos, T, d.k, d.S, row_bytes, static_cast<uint8_t*>(ws.P));
+    {
+      const cudaError_t e_ = launch_k(pack_copy_kernel, dim3(grid), dim3(256), 0, s, st, ws.pos, T, d.k, d.S,
+                                      row_bytes, static_cast<uint8_t*>(ws.P));
+      if (e_ != cudaSuccess) return e_;
+    }
   return cudaGetLastError();
 }
 
@@ -199,28 +211,26 @@ cudaError_t launch_combine(const SrcTable& st, const LayerDims& d, int T, Worksp
                            cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int grid = grid_for(8, d.dtype == AFD_FP32 ? T : T * (d.H / 256), num_sms);
+  const uint16_t* Y = static_cast<const uint16_t*>(ws.Y);
   if (d.dtype == AFD_FP32)
-    combine_f32_kernel<<<grid, 256, 0, s>>>(st, ws.pos, ws.topk_w, static_cast<const float*>(ws.Y), T, d.k, d.S,
-                                            d.H);
-  else
-    switch (d.k) {
-#define AFD_COMBINE_K(KV)                                                                                      \
-  case KV:                                                                                                     \
-    combine_bf16_kernel<KV><<<grid, 256, 0, s>>>(st, ws.pos, ws.topk_w, static_cast<const uint16_t*>(ws.Y), T, \
-                                                 d.k, d.S, d.H);                                               \
-    break;
-      AFD_COMBINE_K(1)
-      AFD_COMBINE_K(2)
-      AFD_COMBINE_K(3)
-      AFD_COMBINE_K(4)
-      AFD_COMBINE_K(6)
-      AFD_COMBINE_K(8)
-#undef AFD_COMBINE_K
-      default:
-        combine_bf16_kernel<0><<<grid, 256, 0, s>>>(st, ws.pos, ws.topk_w, static_cast<const uint16_t*>(ws.Y), T,
-                                                    d.k, d.S, d.H);
-    }
-  return cudaGetLastError();
+    return launch_k(combine_f32_kernel, dim3(grid), dim3(256), 0, s, st, ws.pos, ws.topk_w,
+                    static_cast<const float*>(ws.Y), T, d.k, d.S, d.H);
+  switch (d.k) {  // k known at compile time keeps a unit's k row loads in flight together
+    case 1:
+      return launch_k(combine_bf16_kernel<1>, dim3(grid), dim3(256), 0, s, st, ws.pos, ws.topk_w, Y, T, d.k, d.S, d.H);
+    case 2:
+      return launch_k(combine_bf16_kernel<2>, dim3(grid), dim3(256), 0, s, st, ws.pos, ws.topk_w, Y, T, d.k, d.S, d.H);
+    case 3:
+      return launch_k(combine_bf16_kernel<3>, dim3(grid), dim3(256), 0, s, st, ws.pos, ws.topk_w, Y, T, d.k, d.S, d.H);
+    case 4:
+      return launch_k(combine_bf16_kernel<4>, dim3(grid), dim3(256), 0, s, st, ws.pos, ws.topk_w, Y, T, d.k, d.S, d.H);
+    case 6:
+      return launch_k(combine_bf16_kernel<6>, dim3(grid), dim3(256), 0, s, st, ws.pos, ws.topk_w, Y, T, d.k, d.S, d.H);
+    case 8:
+      return launch_k(combine_bf16_kernel<8>, dim3(grid), dim3(256), 0, s, st, ws.pos, ws.topk_w, Y, T, d.k, d.S, d.H);
+    default:
+      return launch_k(combine_bf16_kernel<0>, dim3(grid), dim3(256), 0, s, st, ws.pos, ws.topk_w, Y, T, d.k, d.S, d.H);
+  }
 }
 
 }  // namespace afd

@@ -167,6 +167,7 @@ __global__ void __launch_bounds__(Cfg<TA>::kThreads, 1)
     router_kernel(SrcTable st, const TA* __restrict__ wrT, const float* __restrict__ bias, int H, int E, int k,
                   float* __restrict__ logits, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
                   int32_t* __restrict__ ticket) {
+  pdl_begin();
   constexpr int kET = Cfg<TA>::ET, kThreads = Cfg<TA>::kThreads, kStages = Cfg<TA>::kStages;
   constexpr int kEG = kET / kWE;  // expert groups of warps
   extern __shared__ __align__(16) uint8_t router_smem[];
@@ -323,14 +324,20 @@ cudaError_t launch_router(const SrcTable& st, const void* wrT, const float* bias
   if (st.T == 0) return cudaSuccess;
   if (d.dtype == AFD_FP32) {
     dim3 grid((st.T + kTT - 1) / kTT, (d.E + Cfg<float>::ET - 1) / Cfg<float>::ET);
-    router_kernel<float><<<grid, Cfg<float>::kThreads, router_smem_bytes<float>(), s>>>(
-        st, static_cast<const float*>(wrT), bias, d.H, d.E, d.k, ws.logits, ws.topk_idx, ws.topk_w,
-        ws.tile_counter);
+    {
+      const cudaError_t e_ = launch_k(router_kernel<float>, dim3(grid), dim3(Cfg<float>::kThreads),
+                                      router_smem_bytes<float>(), s, st, static_cast<const float*>(wrT), bias,
+                                      d.H, d.E, d.k, ws.logits, ws.topk_idx, ws.topk_w, ws.tile_counter);
+      if (e_ != cudaSuccess) return e_;
+    }
   } else {
     dim3 grid((st.T + kTT - 1) / kTT, (d.E + Cfg<uint16_t>::ET - 1) / Cfg<uint16_t>::ET);
-    router_kernel<uint16_t><<<grid, Cfg<uint16_t>::kThreads, router_smem_bytes<uint16_t>(), s>>>(
-        st, static_cast<const uint16_t*>(wrT), bias, d.H, d.E, d.k, ws.logits, ws.topk_idx, ws.topk_w,
-        ws.tile_counter);
+    {
+      const cudaError_t e_ = launch_k(router_kernel<uint16_t>, dim3(grid), dim3(Cfg<uint16_t>::kThreads),
+                                      router_smem_bytes<uint16_t>(), s, st, static_cast<const uint16_t*>(wrT),
+                                      bias, d.H, d.E, d.k, ws.logits, ws.topk_idx, ws.topk_w, ws.tile_counter);
+      if (e_ != cudaSuccess) return e_;
+    }
   }
   return cudaGetLastError();
 }

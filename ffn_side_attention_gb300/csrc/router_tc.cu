@@ -43,6 +43,7 @@ constexpr int kSmallRouterWaves = 8;  // small-batch path while its grid is at m
 // ---------------------------------------------------------------- 1. stage
 __global__ void __launch_bounds__(256) stage_x_kernel(SrcTable st, int H, uint16_t* __restrict__ Xc,
                                                       float* __restrict__ xnorm) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < st.T; t += gridDim.x * 8) {
     const int m = src_of_token(st, t);
@@ -82,6 +83,7 @@ struct LogitArgs {
 __global__ void __launch_bounds__(192, 1)
     router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                             const LogitArgs args) {
+  pdl_begin();
   extern __shared__ uint8_t dyn_smem[];
   uint8_t* smem = dyn_smem + ((1024u - (smem_u32(dyn_smem) & 1023u)) & 1023u);
   __shared__ __align__(8) uint64_t bars[2 * kRStages + 2];
@@ -358,6 +360,7 @@ struct SelectArgs {
 // launcher takes 3 only when that turns a second wave into none).
 template <int MINB>
 __global__ void __launch_bounds__(256, MINB) router_select_warp_kernel(const SelectArgs a) {
+  pdl_begin();
   constexpr int PER = kPer;
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -468,6 +471,7 @@ __global__ void __launch_bounds__(32 * kSelWarps, 1)
     router_small_kernel(const SrcTable st, const uint16_t* __restrict__ wrT, const float* __restrict__ bias, int H,
                         int E, int k, float* __restrict__ logits, int32_t* __restrict__ topk_idx,
                         float* __restrict__ topk_w, int32_t* __restrict__ ticket, int* err) {
+  pdl_begin();
   constexpr int PER = kPer;
   extern __shared__ __align__(16) uint4 s_w[];  // [kOct][H/8]
   __shared__ __align__(8) uint64_t bar;
@@ -596,12 +600,20 @@ cudaError_t launch_router_tc(const SrcTable& st, const void* wrT, const float* b
   if (T == 0) return cudaSuccess;
   if (router_small_path(d, T, num_sms)) {
     const int noct = (d.E + kOct - 1) / kOct;
-    router_small_kernel<<<noct * ((T + kSelWarps - 1) / kSelWarps), 32 * kSelWarps,
-                          (size_t)kOct * d.H * 2, s>>>(st, static_cast<const uint16_t*>(wrT), bias, d.H, d.E, d.k,
-                                                       ws.logits, ws.topk_idx, ws.topk_w, ws.tok_ticket, ws.err);
+    {
+      const cudaError_t e_ = launch_k(router_small_kernel, dim3(noct * ((T + kSelWarps - 1) / kSelWarps)),
+                                      dim3(32 * kSelWarps), (size_t)kOct * d.H * 2, s, st,
+                                      static_cast<const uint16_t*>(wrT), bias, d.H, d.E, d.k, ws.logits,
+                                      ws.topk_idx, ws.topk_w, ws.tok_ticket, ws.err);
+      if (e_ != cudaSuccess) return e_;
+    }
     return cudaGetLastError();
   }
-  stage_x_kernel<<<(T + 7) / 8, 256, 0, s>>>(st, d.H, static_cast<uint16_t*>(ws.Xc), ws.xnorm);
+  {
+    const cudaError_t e_ = launch_k(stage_x_kernel, dim3((T + 7) / 8), dim3(256), 0, s, st, d.H,
+                                    static_cast<uint16_t*>(ws.Xc), ws.xnorm);
+    if (e_ != cudaSuccess) return e_;
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int splits = router_tc_splits(d, T, num_sms);
@@ -609,7 +621,11 @@ cudaError_t launch_router_tc(const SrcTable& st, const void* wrT, const float* b
   LogitArgs la{T, d.E, num_kb, (num_kb + splits - 1) / splits, ws.rpart, ws.err};
   const int nsplit = (num_kb + la.kb_per_split - 1) / la.kb_per_split;
   dim3 grid((T + kRBN - 1) / kRBN, (d.E + kRBM - 1) / kRBM, nsplit);
-  router_logits_tc_kernel<<<grid, 192, kRDynSmem, s>>>(*tm_wr, ws.tm_X, la);
+  {
+    const cudaError_t e_ = launch_k(router_logits_tc_kernel, dim3(grid), dim3(192), kRDynSmem, s, *tm_wr, ws.tm_X,
+                                    la);
+    if (e_ != cudaSuccess) return e_;
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   SelectArgs sa{};
@@ -634,9 +650,15 @@ cudaError_t launch_router_tc(const SrcTable& st, const void* wrT, const float* b
   sa.topk_w = ws.topk_w;
   const int blocks = (T + kSelWarps - 1) / kSelWarps;
   if (blocks > 2 * num_sms && blocks <= 3 * num_sms)
-    router_select_warp_kernel<3><<<blocks, 32 * kSelWarps, 0, s>>>(sa);
+    {
+      const cudaError_t e_ = launch_k(router_select_warp_kernel<3>, dim3(blocks), dim3(32 * kSelWarps), 0, s, sa);
+      if (e_ != cudaSuccess) return e_;
+    }
   else
-    router_select_warp_kernel<2><<<blocks, 32 * kSelWarps, 0, s>>>(sa);
+    {
+      const cudaError_t e_ = launch_k(router_select_warp_kernel<2>, dim3(blocks), dim3(32 * kSelWarps), 0, s, sa);
+      if (e_ != cudaSuccess) return e_;
+    }
   return cudaGetLastError();
 }
 

@@ -38,6 +38,7 @@ constexpr int kWarpsPerBlock = kTok / 32;  // 8
 __global__ void __launch_bounds__(kTok) block_rank_kernel(const int32_t* __restrict__ idx, int T, int k, int E,
                                                           int32_t* __restrict__ block_hist,
                                                           int32_t* __restrict__ rank, int* err) {
+  pdl_begin();
   extern __shared__ uint32_t bits[];  // [kWarpsPerBlock][E]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kTok + threadIdx.x;
@@ -85,6 +86,7 @@ __global__ void __launch_bounds__(kTok)
     place_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ block_hist, int nblocks, int T, int k,
                  int E, int S, int BN, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                  int32_t* __restrict__ tile_base, int32_t* __restrict__ perm, int32_t* __restrict__ pos) {
+  pdl_begin();
   __shared__ int s_cnt[kMaxExperts + 1], s_base[kMaxExperts], s_off[kMaxExperts + 1], s_tb[kMaxExperts + 1];
   const int G = E + S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -148,12 +150,20 @@ cudaError_t launch_routing(const LayerDims& d, int T, Workspace& ws, cudaStream_
   if (T == 0) return cudaSuccess;
   const int nblocks = (T + kTok - 1) / kTok;
   const int bn = d.dtype == AFD_FP8_E4M3 ? kGemmBNFp8 : bf16_tile_tokens(d, T);  // tokens per GEMM tile
-  block_rank_kernel<<<nblocks, kTok, sizeof(uint32_t) * kWarpsPerBlock * d.E, s>>>(ws.topk_idx, T, d.k, d.E,
-                                                                                  ws.block_hist, ws.pos, ws.err);
+  {
+    const cudaError_t e_ = launch_k(block_rank_kernel, dim3(nblocks), dim3(kTok),
+                                    sizeof(uint32_t) * kWarpsPerBlock * d.E, s, ws.topk_idx, T, d.k, d.E,
+                                    ws.block_hist, ws.pos, ws.err);
+    if (e_ != cudaSuccess) return e_;
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  place_kernel<<<nblocks, kTok, 0, s>>>(ws.topk_idx, ws.block_hist, nblocks, T, d.k, d.E, d.S, bn, ws.counts,
-                                        ws.offsets, ws.tile_base, ws.perm, ws.pos);
+  {
+    const cudaError_t e_ = launch_k(place_kernel, dim3(nblocks), dim3(kTok), 0, s, ws.topk_idx, ws.block_hist,
+                                    nblocks, T, d.k, d.E, d.S, bn, ws.counts, ws.offsets, ws.tile_base, ws.perm,
+                                    ws.pos);
+    if (e_ != cudaSuccess) return e_;
+  }
   return cudaGetLastError();
 }
 
