@@ -119,7 +119,12 @@ template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                      const __grid_constant__ CUtensorMap tmB, const TcArgs args) {
-  pdl_begin();
+  // Dependent launch: this kernel starts only after the previous one (the pack,
+  // or the gate/up GEMM) has passed its own wait, so the routing tables are final
+  // and the weights are constant: the weight producer streams at once, and only
+  // the token producer waits for the previous kernel's output (P or h).  The
+  // epilogue writes (h, Y) are read by nothing that can still be running.
+  pdl_trigger();
   constexpr int kWS = TileCfg<BN>::kWStages, kXS = TileCfg<BN>::kXStages, kBTile = TileCfg<BN>::kBTile;
   constexpr uint32_t kAbuf = TileCfg<BN>::kAbuf;
   extern __shared__ uint8_t dyn_smem[];
@@ -185,6 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t* fb = wprod ? wfull : xfull;
       uint64_t* eb = wprod ? wempty : xempty;
       const uint64_t pol = wprod ? l2_policy_evict_first() : l2_policy_evict_last();
+      if (!wprod) pdl_wait();  // the token operand is the previous kernel's output
       int s = 0;
       uint32_t ph = 0, filled = 0, fill_ph = 0;
       bool ok = true;
