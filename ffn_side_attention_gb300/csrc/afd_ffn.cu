@@ -141,6 +141,7 @@ int alloc_workspace(afd_ffn* h, Workspace& ws) {
   if (c.dtype == AFD_FP8_E4M3) {
     if ((rc = dmalloc_t(h, &ws.P_scale, R * (c.H / 128))) || (rc = dmalloc_t(h, &ws.H_scale, R * (c.I / 128))))
       return rc;
+    ws.scale_ld = (int)R;
   }
   if (c.dtype != AFD_FP32) {
     if ((rc = dmalloc(h, &ws.Xc, T * c.H * 2)) || (rc = dmalloc_t(h, &ws.xnorm, T)) ||

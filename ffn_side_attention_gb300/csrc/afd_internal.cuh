@@ -60,9 +60,10 @@ struct Workspace {
   int32_t* pos = nullptr;       // [maxT*k]  packed row of each (t, j)
   float* row_w = nullptr;       // [max_rows] routing weight of each packed row
   void* P = nullptr;            // [max_rows, H] packed activations
-  float* P_scale = nullptr;     // [max_rows, H/128] (fp8)
+  float* P_scale = nullptr;     // [H/128][scale_ld] (fp8), K-block major: one block's scales are contiguous by row
   void* Hb = nullptr;           // [max_rows, I] SwiGLU output
-  float* H_scale = nullptr;     // [max_rows, I/128] (fp8)
+  float* H_scale = nullptr;     // [I/128][scale_ld] (fp8), same layout
+  int scale_ld = 0;             // row stride of P_scale / H_scale (= max_rows)
   void* Y = nullptr;            // [max_rows, H] weighted expert outputs
   int* err = nullptr;           // device error word
   void* stage = nullptr;        // forward_host staging: [maxT, H] in + [maxT, H] out

@@ -21,10 +21,14 @@
 //     tiles, adjacent in shared memory so one descriptor spans all 256 rows;
 //   * the MMA writes each block's 128 x 256 partial into one of two TMEM
 //     buffers (ping-pong), accumulating only inside the block;
+//   * two loader warps stage each K block's scales (the tile's 128 activation
+//     scales, stored K-block major so they are one coalesced read, and the two
+//     weight blocks' scales) into a 4-slot shared-memory ring ahead of use;
 //   * eight epilogue warps (warp w reads TMEM lanes 32*(w%4) .. +31 and one
 //     half of each 128-column block) read the partial and add it, times the
 //     thread's scale, to fp32 accumulators in registers with packed fp32x2
-//     FMAs (__ffma2_rn); warps whose lanes hold no token skip the math;
+//     FMAs (__ffma2_rn); warps whose lanes hold no token skip the math, and a
+//     TMEM buffer is handed back to the MMA as soon as it has been read;
 //   * after the last block: gate/up -> h = silu(G) * U, re-quantised per
 //     token per 128 channels of I (scale = amax/448, e4m3 RNE, saturating);
 //     down -> Y in bf16.  Each thread stores contiguous 16-byte runs of its
@@ -49,7 +53,8 @@ constexpr int kXBoxRows = 32;
 constexpr int kStageBytes = kXTile + 2 * kWTile;     // 48 KB
 constexpr int kDynSmem = kStages * kStageBytes + 1024;
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 128 + 32 * kEpiWarps;  // 384: warpgroup 0 = producer, MMA, 2 idle; 1-2 = epilogue
+constexpr int kThreads = 128 + 32 * kEpiWarps;  // 384: warpgroup 0 = producer, MMA, 2 scale loaders; 1-2 = epilogue
+constexpr int kSlots = 4;                       // scale ring: one slot per K block
 constexpr int kRegsLow = 56;                    // setmaxnreg of warpgroup 0
 constexpr int kRegsHigh = 224;                  // setmaxnreg of the epilogue warpgroups
 // The split must fit in what the block is launched with:
@@ -57,7 +62,6 @@ constexpr int kRegsHigh = 224;                  // setmaxnreg of the epilogue wa
 constexpr int kRegsNeeded = (128 * kRegsLow + 256 * kRegsHigh + kThreads - 1) / kThreads;  // 168
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kDrainCycles = 400000000ll;  // ~0.2 s
-constexpr int kMaxKb = 56;                        // K blocks per GEMM (K <= 7168)
 
 struct Fp8Args {
   const int32_t* counts;
@@ -72,10 +76,11 @@ struct Fp8Args {
   const float* sW0;      // weight block scales of W0: [G][w_rows_per_group/128][num_kb]
   const float* sW1;
   int sw1_block_offset;  // W1's 128-row block relative to W0's (0: own scale array; 1: next block)
-  const float* sX;       // activation scales [rows][num_kb]
+  const float* sX;       // activation scales [num_kb][scale_ld] (K-block major)
   void* out;             // mode 0: e4m3 codes [rows][ld_out]; mode 1: bf16 [rows][ld_out]
-  float* out_scale;      // mode 0: [rows][ld_out/128]
+  float* out_scale;      // mode 0: [ld_out/128][scale_ld]
   int ld_out;
+  int scale_ld;          // row stride of sX and out_scale
   int mode;
   int* err;
 };
@@ -129,19 +134,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t dyn_smem[];
   uint8_t* smem = dyn_smem + ((1024u - (smem_u32(dyn_smem) & 1023u)) & 1023u);
 
-  __shared__ __align__(8) uint64_t bars[2 * kStages + 6];
+  __shared__ __align__(8) uint64_t bars[2 * kStages + 6 + 2 * kSlots];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_tb[kMaxExperts + 1], s_off[kMaxExperts + 1], s_cnt[kMaxExperts];
-  __shared__ float s_red[2][kBM];                    // per column half, token: |h| maxima
-  __shared__ __align__(16) float s_sc[kMaxKb][kBM];  // this item's activation scales, [kb][token]
-  __shared__ float s_w[2][kMaxKb];                   // this item's weight block scales (W0, W1)
+  __shared__ float s_red[2][2][kBM];  // [item parity][column half][token]: |h| maxima
+  __shared__ float s_xs[kSlots][kBM];  // activation scales of one K block, by token
+  __shared__ float s_xw[kSlots][2];    // the two weight blocks' scales of that K block
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* pfull = bars + 2 * kStages;       // [2] MMA -> epilogue
   uint64_t* pempty = bars + 2 * kStages + 2;  // [2] epilogue -> MMA
   uint64_t* drain = bars + 2 * kStages + 4;
   uint64_t* ebar = bars + 2 * kStages + 5;    // epilogue warps' own barrier
+  uint64_t* sfull = bars + 2 * kStages + 6;   // [kSlots] scale loader -> epilogue
+  uint64_t* sempty = sfull + kSlots;          // [kSlots] epilogue -> scale loader
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = args.G;
@@ -158,6 +165,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&pfull[b], 1);
       mbar_init(&pempty[b], kEpiWarps);
+    }
+    for (int q = 0; q < kSlots; ++q) {
+      mbar_init(&sfull[q], 1);
+      mbar_init(&sempty[q], kEpiWarps);
     }
     mbar_init(drain, 1);
     mbar_init(ebar, kEpiWarps);
@@ -248,6 +259,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_commit(drain);  // all MMAs issued above complete before TMEM is freed
       mbar_wait_cycles(drain, 0, kDrainCycles);
+    } else if (warp >= 2) {
+      // ---------------- scale loaders: warp 2 even K blocks, warp 3 odd ones.  One slot per
+      // K block: the 128 tokens' activation scales sX[kb][row0 ..] (coalesced) and the two
+      // weight blocks' sW[kb], staged ahead so the epilogue never waits on global memory.
+      uint32_t gk = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
+        const Item it = decode_item(item, args.MT, G, s_tb, s_off, s_cnt);
+        const int nkb = args.num_kb;
+        const int blk0 = it.g * (args.w_rows_per_group / 128) + it.mt * (args.w_mt_stride / 128);
+        const float* w0 = args.sW0 + (size_t)blk0 * nkb;
+        const float* w1 = args.sW1 + (size_t)(blk0 + args.sw1_block_offset) * nkb;
+        for (int kb = 0; kb < nkb; ++kb, ++gk) {
+          if ((int)(gk & 1u) != warp - 2) continue;
+          const uint32_t slot = gk % kSlots, use = gk / kSlots;
+          if (!mbar_wait(&sempty[slot], (use & 1u) ^ 1u, abort, args.err)) {
+            ok = false;
+            break;
+          }
+          const float* xs = args.sX + (size_t)kb * args.scale_ld + it.row0;
+          float v[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) v[q] = lane + 32 * q < it.nrows ? __ldg(xs + lane + 32 * q) : 0.0f;
+          const float w = lane == 0 ? __ldg(w0 + kb) : (lane == 1 ? __ldg(w1 + kb) : 0.0f);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) s_xs[slot][lane + 32 * q] = v[q];
+          if (lane < 2) s_xw[slot][lane] = w;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sfull[slot]);
+        }
+      }
     }
   } else {
     regs_inc();
@@ -256,28 +298,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3, half = ew >> 2;
     const int r = quad * 32 + lane;  // token (TMEM lane) of the 128-token tile
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * 64);
-    uint32_t gstep = 0, ephase = 0;
+    uint32_t gstep = 0, ephase = 0, ipar = 0;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
+    for (int item = blockIdx.x; ok && item < total; item += gridDim.x, ipar ^= 1u) {
       const Item it = decode_item(item, args.MT, G, s_tb, s_off, s_cnt);
       const int nkb = args.num_kb;
       const bool active = quad * 32 < it.nrows;  // some lane of this warp holds a token
-      // stage the item's scales in shared memory (the previous item is done with them)
-      if (!epi_sync(ebar, ephase, lane, abort, args.err)) break;
-      {
-        const size_t blk0 = (size_t)it.g * (args.w_rows_per_group / 128) + it.mt * (args.w_mt_stride / 128);
-        const float* sX = args.sX + (size_t)it.row0 * nkb;  // rows row0 .. row0+nrows-1 are contiguous
-        for (int q = ew * 32 + lane; q < it.nrows * nkb; q += 32 * kEpiWarps) {
-          const int tok = q / nkb, kb = q - tok * nkb;
-          s_sc[kb][tok] = __ldg(sX + q);
-        }
-        for (int q = ew * 32 + lane; q < 2 * nkb; q += 32 * kEpiWarps) {
-          const int which = q / nkb, kb = q - which * nkb;
-          s_w[which][kb] =
-              __ldg((which ? args.sW1 + (blk0 + args.sw1_block_offset) * nkb : args.sW0 + blk0 * nkb) + kb);
-        }
-      }
-      if (!epi_sync(ebar, ephase, lane, abort, args.err)) break;
+      const bool mine = r < it.nrows;
       // columns half*64 + 2j, +1 of weight rows 0..127 (acc0) and 128..255 (acc1); packed fp32
       // pairs so the promotion is one fma.rn.f32x2 per two columns
       float2 acc0[32], acc1[32];
@@ -285,14 +312,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < 32; ++j) acc0[j] = acc1[j] = make_float2(0.0f, 0.0f);
       for (int kb = 0; kb < nkb; ++kb, ++gstep) {
         const uint32_t b = gstep & 1u, use = gstep >> 1;
-        if (!mbar_wait(&pfull[b], use & 1u, abort, args.err)) {
+        const uint32_t slot = gstep % kSlots;
+        if (!mbar_wait(&sfull[slot], (gstep / kSlots) & 1u, abort, args.err) ||
+            !mbar_wait(&pfull[b], use & 1u, abort, args.err)) {
           ok = false;
           break;
         }
+        const float sx = s_xs[slot][r], sw0 = sx * s_xw[slot][0], sw1 = sx * s_xw[slot][1];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sempty[slot]);
         tc_fence_after();
         if (active) {
-          const float sx = s_sc[kb][r];
-          const float sw0 = sx * s_w[0][kb], sw1 = sx * s_w[1][kb];
           const float2 s0 = make_float2(sw0, sw0), s1 = make_float2(sw1, sw1);
 #pragma unroll
           for (int cc = 0; cc < 64; cc += 32) {
@@ -301,20 +331,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_32x32b_x32(col, p0);
             tmem_ld_32x32b_x32(col + 128u, p1);
             tmem_ld_wait();
+            if (cc == 32) {  // the buffer is read: hand it back before the last FMAs
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&pempty[b]);
+            }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               acc0[cc / 2 + j] = __ffma2_rn(s0, make_float2(p0[2 * j], p0[2 * j + 1]), acc0[cc / 2 + j]);
               acc1[cc / 2 + j] = __ffma2_rn(s1, make_float2(p1[2 * j], p1[2 * j + 1]), acc1[cc / 2 + j]);
             }
           }
+        } else {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&pempty[b]);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&pempty[b]);
       }
       if (!ok) break;
       // ---- item epilogue (this thread: token row0 + r, 64 columns of each block)
-      const bool mine = r < it.nrows;
       const size_t row = (size_t)(it.row0 + r);
       if (args.mode == 0) {
         // h = silu(G) * U, then e4m3 per token per 128 channels of I (this item's channels)
@@ -326,10 +361,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           h[j] = __fdividef(g, 1.0f + __expf(-g)) * u;  // fast SiLU: error far below e4m3 rounding
           amax = fmaxf(amax, fabsf(h[j]));
         }
-        s_red[half][r] = amax;
+        // s_red alternates by item: a warp writes item i+2's entries only after the barrier of
+        // item i+1, which every warp reaches after reading item i's.
+        s_red[ipar][half][r] = amax;
         if (!epi_sync(ebar, ephase, lane, abort, args.err)) break;
         if (mine) {
-          const float am = fmaxf(s_red[0][r], s_red[1][r]);
+          const float am = fmaxf(s_red[ipar][0][r], s_red[ipar][1][r]);
           const float sc = am == 0.0f ? 1.0f : __fdiv_rn(am, 448.0f);
           uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(args.out) + row * args.ld_out + it.mt * 128 +
                                                 half * 64);
@@ -345,9 +382,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
           }
-          if (half == 0) args.out_scale[row * (args.ld_out / 128) + it.mt] = sc;
+          if (half == 0) args.out_scale[(size_t)it.mt * args.scale_ld + row] = sc;
         }
-        // s_red is reused by the next item: the sync at the next item's start orders it
       } else if (mine) {
         uint16_t* yrow = static_cast<uint16_t*>(args.out) + row * args.ld_out + it.mt * kBN + half * 64;
 #pragma unroll
@@ -414,6 +450,7 @@ cudaError_t launch_gemm_fp8(const LayerDims& d, int T, const TcWeights& w, Works
     a.out = ws.Hb;
     a.out_scale = ws.H_scale;
     a.ld_out = d.I;
+    a.scale_ld = ws.scale_ld;
     a.mode = 0;
     const long items_ub = tiles_ub * a.MT;
     const int grid = (int)(items_ub < num_sms ? items_ub : num_sms);
@@ -437,6 +474,7 @@ cudaError_t launch_gemm_fp8(const LayerDims& d, int T, const TcWeights& w, Works
   a.out = ws.Y;
   a.out_scale = nullptr;
   a.ld_out = d.H;
+  a.scale_ld = ws.scale_ld;
   a.mode = 1;
   const long items_ub = tiles_ub * a.MT;
   const int grid = (int)(items_ub < num_sms ? items_ub : num_sms);

@@ -71,12 +71,13 @@ __global__ void __launch_bounds__(256) pack_copy_kernel(SrcTable st, const int32
 
 // fp8 layer: e4m3 codes + one fp32 scale per 128 channels, computed once per
 // token.  A 256-channel warp step holds two 128-channel blocks of 16 lanes.
+// Scales are stored K-block major (P_scale[block * scale_ld + row]), so the
+// GEMM reads one block's scales of consecutive rows as one coalesced load.
 __global__ void __launch_bounds__(256) pack_fp8_kernel(SrcTable st, const int32_t* __restrict__ pos, int T, int k,
                                                        int S, int H, uint8_t* __restrict__ P,
-                                                       float* __restrict__ P_scale) {
+                                                       float* __restrict__ P_scale, int scale_ld) {
   pdl_begin();
   const int lane = threadIdx.x & 31;
-  const int nblk = H >> 7;
   const int nchunk = H >> 8;  // H % 256 == 0: whole warp active
   const long units = (long)T * nchunk;
   for (long u = (long)blockIdx.x * 8 + (threadIdx.x >> 5); u < units; u += (long)gridDim.x * 8) {
@@ -103,7 +104,7 @@ __global__ void __launch_bounds__(256) pack_fp8_kernel(SrcTable st, const int32_
     }
     for (int r = 0; r < n; ++r) {
       reinterpret_cast<uint2*>(P + (size_t)rows[r] * H)[v] = q;
-      if ((lane & 15) == 0) P_scale[(size_t)rows[r] * nblk + (v >> 4)] = scale;
+      if ((lane & 15) == 0) P_scale[(size_t)(v >> 4) * scale_ld + rows[r]] = scale;
     }
   }
 }
@@ -195,7 +196,7 @@ cudaError_t launch_pack(const SrcTable& st, const LayerDims& d, int T, Workspace
   if (d.dtype == AFD_FP8_E4M3)
     {
       const cudaError_t e_ = launch_k(pack_fp8_kernel, dim3(grid), dim3(256), 0, s, st, ws.pos, T, d.k, d.S, d.H,
-                                      static_cast<uint8_t*>(ws.P), ws.P_scale);
+                                      static_cast<uint8_t*>(ws.P), ws.P_scale, ws.scale_ld);
       if (e_ != cudaSuccess) return e_;
     }
   else
