@@ -23,7 +23,8 @@
 //     buffers (ping-pong), accumulating only inside the block;
 //   * two loader warps stage each K block's scales (the tile's 128 activation
 //     scales, stored K-block major so they are one coalesced read, and the two
-//     weight blocks' scales) into a 4-slot shared-memory ring ahead of use;
+//     weight blocks' scales) into a shared-memory ring of two groups of four
+//     K blocks, one barrier wait per group;
 //   * eight epilogue warps (warp w reads TMEM lanes 32*(w%4) .. +31 and one
 //     half of each 128-column block) read the partial and add it, times the
 //     thread's scale, to fp32 accumulators in registers with packed fp32x2
@@ -31,8 +32,8 @@
 //     TMEM buffer is handed back to the MMA as soon as it has been read;
 //   * after the last block: gate/up -> h = silu(G) * U, re-quantised per
 //     token per 128 channels of I (scale = amax/448, e4m3 RNE, saturating);
-//     down -> Y in bf16.  Each thread stores contiguous 16-byte runs of its
-//     token's row.
+//     down -> Y in bf16.  Each thread stores its token's row in 32-byte
+//     pieces (full L2 sectors).
 // TMA ring of 4 stages x 48 KB.  Same device-side work list, persistent CTAs
 // and bounded waits as the bf16 kernel; the producer warpgroup gives
 // registers up (setmaxnreg) for the epilogue's 128 accumulators.
@@ -54,7 +55,8 @@ constexpr int kStageBytes = kXTile + 2 * kWTile;     // 48 KB
 constexpr int kDynSmem = kStages * kStageBytes + 1024;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 128 + 32 * kEpiWarps;  // 384: warpgroup 0 = producer, MMA, 2 scale loaders; 1-2 = epilogue
-constexpr int kSlots = 4;                       // scale ring: one slot per K block
+constexpr int kGrp = 4;                         // scale ring: groups of 4 K blocks (one slot each),
+constexpr int kSlots = 2 * kGrp;                // two groups, one barrier pair per group
 constexpr int kRegsLow = 56;                    // setmaxnreg of warpgroup 0
 constexpr int kRegsHigh = 224;                  // setmaxnreg of the epilogue warpgroups
 // The split must fit in what the block is launched with:
@@ -113,6 +115,13 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float v0, float v1) {
   return r;
 }
 
+// one 32-byte store (a full L2 sector); p must be 32-byte aligned
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow)); }
 __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh)); }
 
@@ -134,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t dyn_smem[];
   uint8_t* smem = dyn_smem + ((1024u - (smem_u32(dyn_smem) & 1023u)) & 1023u);
 
-  __shared__ __align__(8) uint64_t bars[2 * kStages + 6 + 2 * kSlots];
+  __shared__ __align__(8) uint64_t bars[2 * kStages + 6 + 4];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_tb[kMaxExperts + 1], s_off[kMaxExperts + 1], s_cnt[kMaxExperts];
@@ -147,8 +156,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* pempty = bars + 2 * kStages + 2;  // [2] epilogue -> MMA
   uint64_t* drain = bars + 2 * kStages + 4;
   uint64_t* ebar = bars + 2 * kStages + 5;    // epilogue warps' own barrier
-  uint64_t* sfull = bars + 2 * kStages + 6;   // [kSlots] scale loader -> epilogue
-  uint64_t* sempty = sfull + kSlots;          // [kSlots] epilogue -> scale loader
+  uint64_t* sfull = bars + 2 * kStages + 6;   // [2] scale loader -> epilogue, per group
+  uint64_t* sempty = sfull + 2;               // [2] epilogue -> scale loader
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = args.G;
@@ -166,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&pfull[b], 1);
       mbar_init(&pempty[b], kEpiWarps);
     }
-    for (int q = 0; q < kSlots; ++q) {
+    for (int q = 0; q < 2; ++q) {
       mbar_init(&sfull[q], 1);
       mbar_init(&sempty[q], kEpiWarps);
     }
@@ -260,11 +269,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit(drain);  // all MMAs issued above complete before TMEM is freed
       mbar_wait_cycles(drain, 0, kDrainCycles);
     } else if (warp >= 2) {
-      // ---------------- scale loaders: warp 2 even K blocks, warp 3 odd ones.  One slot per
-      // K block: the 128 tokens' activation scales sX[kb][row0 ..] (coalesced) and the two
-      // weight blocks' sW[kb], staged ahead so the epilogue never waits on global memory.
+      // ---------------- scale loaders: warp 2 even groups of K blocks, warp 3 odd ones.  One
+      // slot per K block: the 128 tokens' activation scales sX[kb][row0 ..] (coalesced) and
+      // the two weight blocks' sW[kb], staged ahead so the epilogue never waits on global
+      // memory; a group's barrier is signalled once its kGrp slots are written.
       uint32_t gk = 0;
-      bool ok = true;
+      bool ok = true, pending = false;
       for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
         const Item it = decode_item(item, args.MT, G, s_tb, s_off, s_cnt);
         const int nkb = args.num_kb;
@@ -272,9 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* w0 = args.sW0 + (size_t)blk0 * nkb;
         const float* w1 = args.sW1 + (size_t)(blk0 + args.sw1_block_offset) * nkb;
         for (int kb = 0; kb < nkb; ++kb, ++gk) {
-          if ((int)(gk & 1u) != warp - 2) continue;
-          const uint32_t slot = gk % kSlots, use = gk / kSlots;
-          if (!mbar_wait(&sempty[slot], (use & 1u) ^ 1u, abort, args.err)) {
+          const uint32_t grp = gk / kGrp;
+          if ((int)(grp & 1u) != warp - 2) continue;
+          const uint32_t slot = gk % kSlots;
+          if (gk % kGrp == 0 && !mbar_wait(&sempty[grp & 1u], ((grp >> 1) & 1u) ^ 1u, abort, args.err)) {
             ok = false;
             break;
           }
@@ -286,9 +297,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) s_xs[slot][lane + 32 * q] = v[q];
           if (lane < 2) s_xw[slot][lane] = w;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sfull[slot]);
+          pending = gk % kGrp != kGrp - 1;
+          if (!pending) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sfull[grp & 1u]);
+          }
         }
+      }
+      if (ok && pending) {  // the last group is partial
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfull[((gk - 1) / kGrp) & 1u]);
       }
     }
   } else {
@@ -312,15 +330,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < 32; ++j) acc0[j] = acc1[j] = make_float2(0.0f, 0.0f);
       for (int kb = 0; kb < nkb; ++kb, ++gstep) {
         const uint32_t b = gstep & 1u, use = gstep >> 1;
-        const uint32_t slot = gstep % kSlots;
-        if (!mbar_wait(&sfull[slot], (gstep / kSlots) & 1u, abort, args.err) ||
+        const uint32_t slot = gstep % kSlots, grp = gstep / kGrp;
+        if ((gstep % kGrp == 0 && !mbar_wait(&sfull[grp & 1u], (grp >> 1) & 1u, abort, args.err)) ||
             !mbar_wait(&pfull[b], use & 1u, abort, args.err)) {
           ok = false;
           break;
         }
         const float sx = s_xs[slot][r], sw0 = sx * s_xw[slot][0], sw1 = sx * s_xw[slot][1];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sempty[slot]);
+        if (gstep % kGrp == kGrp - 1) {  // the group's slots are read
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sempty[grp & 1u]);
+        }
         tc_fence_after();
         if (active) {
           const float2 s0 = make_float2(sw0, sw0), s1 = make_float2(sw1, sw1);
@@ -368,19 +388,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (mine) {
           const float am = fmaxf(s_red[ipar][0][r], s_red[ipar][1][r]);
           const float sc = am == 0.0f ? 1.0f : __fdiv_rn(am, 448.0f);
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(args.out) + row * args.ld_out + it.mt * 128 +
-                                                half * 64);
+          // 32-byte aligned: ld_out is a multiple of 128 and the offset of 64 codes
+          uint8_t* dst = static_cast<uint8_t*>(args.out) + row * args.ld_out + it.mt * 128 + half * 64;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint32_t w[4];
+          for (int v = 0; v < 2; ++v) {
+            uint32_t w[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int j = 16 * v + 4 * q;
+            for (int q = 0; q < 8; ++q) {
+              const int j = 32 * v + 4 * q;
               const uint32_t lo = am == 0.0f ? 0u : cvt_e4m3x2(__fdiv_rn(h[j], sc), __fdiv_rn(h[j + 1], sc));
               const uint32_t hi = am == 0.0f ? 0u : cvt_e4m3x2(__fdiv_rn(h[j + 2], sc), __fdiv_rn(h[j + 3], sc));
               w[q] = lo | (hi << 16);
             }
-            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+            st_global_v8(dst + 32 * v, w);
           }
           if (half == 0) args.out_scale[(size_t)it.mt * args.scale_ld + row] = sc;
         }
@@ -389,16 +409,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
           const float2* acc = part ? acc1 : acc0;
-          uint4* dst = reinterpret_cast<uint4*>(yrow + part * 128);
+          uint16_t* dst = yrow + part * 128;  // 32-byte aligned: ld_out % 256 == 0
 #pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            uint32_t w[4];
+          for (int v = 0; v < 4; ++v) {
+            uint32_t w[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const __nv_bfloat162 y = __float22bfloat162_rn(acc[4 * v + q]);
+            for (int q = 0; q < 8; ++q) {
+              const __nv_bfloat162 y = __float22bfloat162_rn(acc[8 * v + q]);
               w[q] = *reinterpret_cast<const uint32_t*>(&y);
             }
-            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+            st_global_v8(dst + 16 * v, w);
           }
         }
       }
