@@ -22,7 +22,7 @@ AFD_NUM_KERNELS = 6
 KERNEL_NAMES = ["router", "routing", "pack", "gemm_gateup", "gemm_down", "combine"]
 
 EXPORTS = ["afd_ffn_create", "afd_ffn_create_error", "afd_ffn_forward", "afd_ffn_forward_pipelined",
-           "afd_ffn_forward_host", "afd_ffn_debug_routing", "afd_ffn_check", "afd_ffn_last_error",
+           "afd_ffn_forward_host", "afd_ffn_forward_host_async", "afd_ffn_host_wait", "afd_ffn_debug_routing", "afd_ffn_check", "afd_ffn_last_error",
            "afd_ffn_profile_begin", "afd_ffn_profile_end", "afd_ffn_launches_per_forward",
            "afd_ffn_device_bytes", "afd_ffn_router_noalloc", "afd_ffn_destroy"]
 
@@ -64,6 +64,10 @@ def lib():
         L.afd_ffn_forward_pipelined.restype = ip
         L.afd_ffn_forward_host.argtypes = [vp, vp, ip, vp, vp, ip, vp]
         L.afd_ffn_forward_host.restype = ip
+        L.afd_ffn_forward_host_async.argtypes = [vp, ip, vp, vp, ip, vp]
+        L.afd_ffn_forward_host_async.restype = ip
+        L.afd_ffn_host_wait.argtypes = [vp]
+        L.afd_ffn_host_wait.restype = ip
         L.afd_ffn_debug_routing.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.afd_ffn_debug_routing.restype = ip
         L.afd_ffn_check.argtypes = [vp, vp]
@@ -123,6 +127,15 @@ def afd_ffn_forward_pipelined(h, stream, n_micro, src_ptrs, src_counts, out_ptrs
 def afd_ffn_forward_host(h, stream, n_micro, src_ptrs, src_counts, out_ptrs):
     return _check(lib().afd_ffn_forward_host(h, stream, n_micro, _ptr_array(src_ptrs), _int_array(src_counts),
                                              len(src_counts), _ptr_array(out_ptrs)), h)
+
+
+def afd_ffn_forward_host_async(h, n_micro, src_ptrs, src_counts, out_ptrs):
+    return _check(lib().afd_ffn_forward_host_async(h, n_micro, _ptr_array(src_ptrs), _int_array(src_counts),
+                                                   len(src_counts), _ptr_array(out_ptrs)), h)
+
+
+def afd_ffn_host_wait(h):
+    return _check(lib().afd_ffn_host_wait(h), h)
 
 
 def afd_ffn_debug_routing(h, stream, topk_idx, topk_w, counts, offsets, perm_token, pos, logits):
@@ -235,6 +248,19 @@ class MoELayer:
         afd_ffn_forward_host(self.handle, self._stream(stream), int(n_micro), sp, [int(s.shape[0]) for s in srcs],
                              op)
         return outs
+
+    def forward_host_async(self, srcs, outs, n_micro=1):
+        """Host tensors in and out (pinned), asynchronous: returns once the copies and the
+        layer are enqueued on the library's streams; consecutive calls overlap one batch's
+        transfers with another's compute.  Outputs are valid after host_wait()."""
+        sp = [s.data_ptr() if s.shape[0] else 0 for s in srcs]
+        op = [o.data_ptr() if o.shape[0] else 0 for o in outs]
+        afd_ffn_forward_host_async(self.handle, int(n_micro), sp, [int(s.shape[0]) for s in srcs], op)
+        return outs
+
+    def host_wait(self):
+        """Wait for every forward_host_async call so far."""
+        return afd_ffn_host_wait(self.handle)
 
     def routing(self, T, stream=None):
         """Routing tables of the last forward (workspace 0) as int32/fp32 tensors."""

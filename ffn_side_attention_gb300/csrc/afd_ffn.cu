@@ -47,6 +47,13 @@ struct afd_ffn {
   cudaStream_t mstream[AFD_MAX_MICRO] = {};
   cudaEvent_t ev_fork = nullptr;
   cudaEvent_t ev_join[AFD_MAX_MICRO] = {};
+  // afd_ffn_forward_host_async: copy-in, compute and copy-out streams, two device
+  // staging slots (sources + outputs) and, per slot, the events that order reuse
+  cudaStream_t astream[3] = {};
+  void* astage[2] = {};
+  cudaEvent_t ev_in[2] = {}, ev_done[2] = {}, ev_out[2] = {};
+  unsigned long long async_calls = 0;
+  int async_rc = 0;  // first error of an enqueued call, reported by afd_ffn_host_wait
   // per-kernel timing: AFD_NUM_KERNELS + 1 events per recorded forward
   bool prof_on = false;
   std::vector<cudaEvent_t> prof_events;
@@ -503,6 +510,76 @@ int afd_ffn_forward_host(afd_ffn_t h, void* stream, int n_micro, const void* con
   return AFD_OK;
 }
 
+int afd_ffn_forward_host_async(afd_ffn_t h, int n_micro, const void* const* src_ptrs_host,
+                               const int* src_counts_host, int M, void* const* out_ptrs_host) {
+  int T = 0;
+  int rc = validate_batch(h, src_ptrs_host, src_counts_host, M, out_ptrs_host, &T);
+  if (rc) return rc;
+  if (n_micro < 1 || n_micro > AFD_MAX_MICRO)
+    return fail(h, AFD_EINVAL, "n_micro=%d outside [1, %d]", n_micro, AFD_MAX_MICRO);
+  const size_t rowb = (size_t)h->cfg.H * act_bytes(h->cfg);
+  const size_t slot_bytes = 2 * (size_t)h->cfg.max_tokens * rowb;
+  for (int i = 0; i < 3; ++i)
+    if (!h->astream[i]) CUDA_TRY(h, cudaStreamCreateWithFlags(&h->astream[i], cudaStreamNonBlocking));
+  for (int q = 0; q < 2; ++q) {
+    if (!h->astage[q] && (rc = dmalloc(h, &h->astage[q], slot_bytes))) return rc;
+    for (cudaEvent_t* e : {&h->ev_in[q], &h->ev_done[q], &h->ev_out[q]})
+      if (!*e) CUDA_TRY(h, cudaEventCreateWithFlags(e, cudaEventDisableTiming));
+  }
+  cudaStream_t cin = h->astream[0], comp = h->astream[1], cout = h->astream[2];
+  const int q = (int)(h->async_calls++ & 1u);
+  uint8_t* in = static_cast<uint8_t*>(h->astage[q]);
+  uint8_t* outb = in + (size_t)h->cfg.max_tokens * rowb;
+  const void* dsrc[AFD_MAX_SOURCES];
+  void* dout[AFD_MAX_SOURCES];
+  // copy-in: the slot's sources are free once the layer two calls back has finished
+  CUDA_TRY(h, cudaStreamWaitEvent(cin, h->ev_done[q], 0));
+  size_t r = 0;
+  for (int m = 0; m < M; ++m) {
+    dsrc[m] = in + r * rowb;
+    dout[m] = outb + r * rowb;
+    if (src_counts_host[m] > 0)
+      CUDA_TRY(h, cudaMemcpyAsync(in + r * rowb, src_ptrs_host[m], src_counts_host[m] * rowb,
+                                  cudaMemcpyHostToDevice, cin));
+    r += src_counts_host[m];
+  }
+  CUDA_TRY(h, cudaEventRecord(h->ev_in[q], cin));
+  // compute: after this call's copy-in and after the slot's outputs two calls back went out
+  CUDA_TRY(h, cudaStreamWaitEvent(comp, h->ev_in[q], 0));
+  CUDA_TRY(h, cudaStreamWaitEvent(comp, h->ev_out[q], 0));
+  if (n_micro > 1) {
+    rc = afd_ffn_forward_pipelined(h, comp, n_micro, dsrc, src_counts_host, M, dout);
+  } else {
+    SrcTable st = make_table(dsrc, src_counts_host, M, dout);
+    rc = run_layer(h, st, h->ws[0], comp);
+  }
+  if (rc) {
+    if (!h->async_rc) h->async_rc = rc;
+    return rc;
+  }
+  CUDA_TRY(h, cudaEventRecord(h->ev_done[q], comp));
+  // copy-out
+  CUDA_TRY(h, cudaStreamWaitEvent(cout, h->ev_done[q], 0));
+  r = 0;
+  for (int m = 0; m < M; ++m) {
+    if (src_counts_host[m] > 0)
+      CUDA_TRY(h, cudaMemcpyAsync(out_ptrs_host[m], outb + r * rowb, src_counts_host[m] * rowb,
+                                  cudaMemcpyDeviceToHost, cout));
+    r += src_counts_host[m];
+  }
+  CUDA_TRY(h, cudaEventRecord(h->ev_out[q], cout));
+  return AFD_OK;
+}
+
+int afd_ffn_host_wait(afd_ffn_t h) {
+  if (!h) return AFD_EINVAL;
+  for (cudaStream_t s : h->astream)
+    if (s) CUDA_TRY(h, cudaStreamSynchronize(s));
+  const int rc = h->async_rc;
+  h->async_rc = 0;
+  return rc;
+}
+
 int afd_ffn_debug_routing(afd_ffn_t h, void* stream, int* topk_idx, float* topk_w, int* counts, int* offsets,
                           int* perm_token, int* pos, float* logits) {
   if (!h) return AFD_EINVAL;
@@ -593,6 +670,13 @@ void afd_ffn_destroy(afd_ffn_t h) {
     if (p) cudaFree(p);
   for (auto s : h->mstream)
     if (s) cudaStreamDestroy(s);
+  for (auto s : h->astream)
+    if (s) cudaStreamDestroy(s);
+  for (int q = 0; q < 2; ++q) {
+    if (h->astage[q]) cudaFree(h->astage[q]);
+    for (cudaEvent_t e : {h->ev_in[q], h->ev_done[q], h->ev_out[q]})
+      if (e) cudaEventDestroy(e);
+  }
   for (auto e : h->ev_join)
     if (e) cudaEventDestroy(e);
   if (h->ev_fork) cudaEventDestroy(h->ev_fork);

@@ -150,6 +150,28 @@ int afd_ffn_forward_pipelined(afd_ffn_t h, void* stream, int n_micro, const void
 int afd_ffn_forward_host(afd_ffn_t h, void* stream, int n_micro, const void* const* src_ptrs_host,
                          const int* src_counts_host, int M, void* const* out_ptrs_host);
 
+/* HOST buffers for a stream of batches, asynchronous: the FFN daemon's loop
+ * with each batch's transfers hidden under another batch's compute (the dual
+ * batch overlap of the FastAFD blog, section 4).  Enqueues the host->device
+ * copy of the sources, the layer (as afd_ffn_forward_host with the same
+ * n_micro) and the device->host copy of the outputs on three library streams
+ * (copy-in, compute, copy-out) and returns without waiting.  Consecutive calls
+ * alternate between two device staging slots; events order them on the
+ * device, so the sources of call i+1 cross the host link while call i
+ * computes and call i-1's outputs return.  Calls run in order.  Host buffers
+ * must stay valid until afd_ffn_host_wait returns, and be pinned for the
+ * copies to be asynchronous.  While calls are in flight, issue no other
+ * forward on this handle.  Argument errors return at once (nothing is
+ * enqueued); the staging slots (2 x 2 x max_tokens x H activations) are
+ * allocated on first use. */
+int afd_ffn_forward_host_async(afd_ffn_t h, int n_micro, const void* const* src_ptrs_host,
+                               const int* src_counts_host, int M, void* const* out_ptrs_host);
+
+/* Blocks until every afd_ffn_forward_host_async call so far has its outputs
+ * in host memory.  Returns AFD_OK, or the first error met since the last
+ * wait. */
+int afd_ffn_host_wait(afd_ffn_t h);
+
 /* Copy the routing of the last forward (workspace 0) into caller device
  * buffers, each may be NULL to skip:
  *   topk_idx [T*k] int32, topk_w [T*k] fp32 (slot order: descending logit,

@@ -110,6 +110,33 @@ def test_forward_host_equals_device():
         layer.forward_host(hs, ho3, n_micro=0)
 
 
+@pytest.mark.parametrize("n_micro", [1, 3])
+def test_forward_host_async_stream_of_batches(n_micro):
+    """Consecutive asynchronous host-buffer calls (staging slots reused every other
+    call, batch sizes changing) give, call by call, the device forward's outputs."""
+    c = _small(E=16, k=4, H=256, I=256, S=1)
+    w = synth.make_weights(c, "cuda")
+    layer = make_layer(c, w, max_tokens=96, max_sources=4)
+    batches = [[20, 9], [33, 0, 40], [5], [48, 48], [1, 2, 3]]
+    expect, hin, hout = [], [], []
+    for i, counts in enumerate(batches):
+        srcs = synth.make_sources(c, "cuda", seed=10 + i, counts=counts)
+        expect.append([o.cpu() for o in layer.forward(srcs)])
+        torch.cuda.synchronize()
+        hin.append([x.cpu().pin_memory() for x in srcs])
+        hout.append([torch.full_like(x, float("nan")).pin_memory() for x in hin[-1]])
+    for i in range(len(batches)):
+        layer.forward_host_async(hin[i], hout[i], n_micro=n_micro)
+    layer.host_wait()
+    for i in range(len(batches)):
+        for x, y in zip(expect[i], hout[i]):
+            assert torch.equal(x, y), f"call {i}"
+    with pytest.raises(afd.AfdError):
+        layer.forward_host_async(hin[0], hout[0], n_micro=0)
+    layer.host_wait()
+    layer.check()
+
+
 def test_launches_per_forward_by_batch():
     """One router launch for small batches, three (stage, logits, select) for
     large ones; then 2 routing, pack, 2 GEMMs, combine."""
