@@ -200,8 +200,6 @@ int validate_config(const afd_ffn_config* c) {
   } else {
     if (c->H % 256) return fail(nullptr, AFD_EINVAL, "bf16/fp8 layer needs H %% 256 == 0 (H=%d)", c->H);
     if (c->I % 128) return fail(nullptr, AFD_EINVAL, "bf16/fp8 layer needs I %% 128 == 0 (I=%d)", c->I);
-    if (c->dtype == AFD_FP8_E4M3 && (c->H > 7168 || c->I > 7168))
-      return fail(nullptr, AFD_EUNSUPPORTED, "fp8 layer supports H, I <= 7168 (56 scale blocks)");
   }
   return AFD_OK;
 }

@@ -73,8 +73,7 @@ typedef enum {
  *   (1 <= k <= E <= 256); n_shared 0 or 1 always-on shared expert of the
  *   same shape, added with weight 1; max_sources bound on M per forward
  *   (<= AFD_MAX_SOURCES); max_tokens bound on T = sum of src_counts.
- *   bf16/fp8 need H % 256 == 0 and I % 128 == 0; fp8 also H, I <= 7168;
- *   fp32 needs H % 8 == 0. */
+ *   bf16/fp8 need H % 256 == 0 and I % 128 == 0; fp32 needs H % 8 == 0. */
 typedef struct {
   int H, I, E, k, n_shared, max_sources, max_tokens;
   afd_dtype dtype;

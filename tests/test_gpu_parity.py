@@ -197,6 +197,8 @@ def test_fp32_router_edges(shape, counts):
     (dict(dtype="fp8", S=1), [17, 0, 40]),
     (dict(dtype="fp8", E=4, k=2, H=512, I=384), [300, 301]),       # > 128 rows per expert: several N tiles
     (dict(dtype="fp8", E=48, k=3, H=768, I=640, S=1), [2, 5]),
+    (dict(dtype="fp8", E=4, k=2, H=7424, I=256), [40]),            # 58 K blocks in gate/up
+    (dict(dtype="fp8", E=4, k=2, H=256, I=7296, S=1), [40]),       # 57 K blocks in down
 ])
 def test_fp8_shapes(shape, counts):
     c = _small(**shape)
