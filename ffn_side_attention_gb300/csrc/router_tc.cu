@@ -274,6 +274,37 @@ __device__ __forceinline__ void canonical_dot2_warp(const uint16_t* __restrict__
   v2 = p2;
 }
 
+// The same two dots with the token row in shared memory (xs: this warp's copy).
+__device__ __forceinline__ void canonical_dot2_xs(const uint4* xs, const uint16_t* __restrict__ w1,
+                                                  const uint16_t* __restrict__ w2, int H, int lane, float& v1,
+                                                  float& v2) {
+  const int nc = H >> 3;
+  const uint4* wa = reinterpret_cast<const uint4*>(w1);
+  const uint4* wb = reinterpret_cast<const uint4*>(w2);
+  float p1 = 0.0f, p2 = 0.0f;
+  for (int c = lane; c < nc; c += 32) {
+    const uint4 a = xs[c], b = __ldg(wa + c), d = __ldg(wb + c);
+    p1 = chain8(a, b, p1);
+    p2 = chain8(a, d, p2);
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    p1 = p1 + __shfl_xor_sync(0xffffffffu, p1, o);
+    p2 = p2 + __shfl_xor_sync(0xffffffffu, p2, o);
+  }
+  v1 = p1;
+  v2 = p2;
+}
+__device__ __forceinline__ float canonical_dot_xs(const uint4* xs, const uint16_t* __restrict__ w, int H, int lane) {
+  const int nc = H >> 3;
+  const uint4* wa = reinterpret_cast<const uint4*>(w);
+  float p = 0.0f;
+  for (int c = lane; c < nc; c += 32) p = chain8(xs[c], __ldg(wa + c), p);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) p = p + __shfl_xor_sync(0xffffffffu, p, o);
+  return p;
+}
+
 __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
@@ -339,6 +370,11 @@ __device__ __forceinline__ void write_topk(const float (&lc)[PER], bool (&tk)[PE
   }
 }
 
+// Token rows of one select block in shared memory: used up to H = 4096.  At H = 7168
+// (112 KB per block) the router was slower (DeepSeek-V3 T=4096: 150 -> 199 us).
+constexpr int kSelXsMaxBytes = 8 * 4096 * 2;
+constexpr int kSelXsThreeBytes = 220 * 1024;  // three such blocks per SM
+
 struct SelectArgs {
   const uint16_t* Xc;
   const uint16_t* wrT;  // [E][H]
@@ -357,14 +393,23 @@ struct SelectArgs {
 // its token from the bounds to the weights without waiting for the others.
 // MINB = blocks per SM the register budget is sized for: 2 gives each warp
 // registers for two dot chains at once, 3 fits 50% more tokens per wave (the
-// launcher takes 3 only when that turns a second wave into none).
-template <int MINB>
+// launcher takes 3 only when that turns a second wave into none).  XS: each
+// warp first copies its token row into shared memory, so the candidate dots
+// read only the expert rows from L2 (the row is reused by every candidate).
+template <int MINB, bool XS>
 __global__ void __launch_bounds__(256, MINB) router_select_warp_kernel(const SelectArgs a) {
   pdl_begin();
   constexpr int PER = kPer;
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= a.T) return;
+  extern __shared__ uint4 sel_xs[];  // XS: [8 warps][H / 8]
+  uint4* xs = sel_xs + (size_t)(threadIdx.x >> 5) * (a.H >> 3);
+  if (XS) {
+    const uint4* xg = reinterpret_cast<const uint4*>(a.Xc + (size_t)t * a.H);
+    for (int c = lane; c < (a.H >> 3); c += 32) xs[c] = __ldg(xg + c);
+    __syncwarp();
+  }
   const int E = a.E, k = a.k;
   const uint16_t* x = a.Xc + (size_t)t * a.H;
   const float xn = __ldg(a.xnorm + t);
@@ -427,9 +472,15 @@ __global__ void __launch_bounds__(256, MINB) router_select_warp_kernel(const Sel
       if (msk) {
         s2 = __ffs(msk) - 1;
         msk &= msk - 1;
-        canonical_dot2_warp(x, a.wrT + (size_t)e1 * a.H, a.wrT + (size_t)(s2 + 32 * q) * a.H, a.H, lane, v1, v2);
+        const uint16_t* w1 = a.wrT + (size_t)e1 * a.H;
+        const uint16_t* w2 = a.wrT + (size_t)(s2 + 32 * q) * a.H;
+        if (XS)
+          canonical_dot2_xs(xs, w1, w2, a.H, lane, v1, v2);
+        else
+          canonical_dot2_warp(x, w1, w2, a.H, lane, v1, v2);
       } else {
-        v1 = canonical_dot_warp<1>(x, a.wrT + (size_t)e1 * a.H, a.H, lane);
+        v1 = XS ? canonical_dot_xs(xs, a.wrT + (size_t)e1 * a.H, a.H, lane)
+                : canonical_dot_warp<1>(x, a.wrT + (size_t)e1 * a.H, a.H, lane);
       }
       if (a.bias) v1 = __fadd_rn(v1, __ldg(a.bias + e1));
       if (lane == s1) lc[q] = v1;
@@ -567,6 +618,12 @@ __global__ void wnorm_kernel(const uint16_t* __restrict__ wrT, int H, int E, flo
 cudaError_t router_tc_setup() {
   cudaError_t e = cudaFuncSetAttribute(router_logits_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRDynSmem);
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(router_select_warp_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSelXsMaxBytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(router_select_warp_kernel<3, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSelXsMaxBytes);
+  if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmallDynSmem);
 }
 
@@ -649,16 +706,17 @@ cudaError_t launch_router_tc(const SrcTable& st, const void* wrT, const float* b
   sa.topk_idx = ws.topk_idx;
   sa.topk_w = ws.topk_w;
   const int blocks = (T + kSelWarps - 1) / kSelWarps;
-  if (blocks > 2 * num_sms && blocks <= 3 * num_sms)
-    {
-      const cudaError_t e_ = launch_k(router_select_warp_kernel<3>, dim3(blocks), dim3(32 * kSelWarps), 0, s, sa);
-      if (e_ != cudaSuccess) return e_;
-    }
-  else
-    {
-      const cudaError_t e_ = launch_k(router_select_warp_kernel<2>, dim3(blocks), dim3(32 * kSelWarps), 0, s, sa);
-      if (e_ != cudaSuccess) return e_;
-    }
+  // token rows in shared memory when 8 of them fit the opt-in size; 3 blocks per SM
+  // only if their rows fit the SM's shared memory too
+  const size_t xs_bytes = (size_t)kSelWarps * d.H * 2;
+  const bool xs = xs_bytes <= (size_t)kSelXsMaxBytes;
+  const bool three = blocks > 2 * num_sms && blocks <= 3 * num_sms && (!xs || 3 * xs_bytes <= kSelXsThreeBytes);
+  void (*kern)(const SelectArgs) = three ? (xs ? router_select_warp_kernel<3, true> : router_select_warp_kernel<3, false>)
+                                         : (xs ? router_select_warp_kernel<2, true> : router_select_warp_kernel<2, false>);
+  {
+    const cudaError_t e_ = launch_k(kern, dim3(blocks), dim3(32 * kSelWarps), xs ? xs_bytes : 0, s, sa);
+    if (e_ != cudaSuccess) return e_;
+  }
   return cudaGetLastError();
 }
 
