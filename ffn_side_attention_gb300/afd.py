@@ -19,10 +19,13 @@ AFD_OK, AFD_EINVAL, AFD_ECUDA, AFD_ECAPACITY, AFD_EUNSUPPORTED, AFD_EDEVICE = 0,
 AFD_MAX_SOURCES, AFD_MAX_MICRO = 64, 4
 
 AFD_NUM_KERNELS = 6
+INJECT_TIMEOUT = 1
+INJECT_RANGE = 2
 KERNEL_NAMES = ["router", "routing", "pack", "gemm_gateup", "gemm_down", "combine"]
 
 EXPORTS = ["afd_ffn_create", "afd_ffn_create_error", "afd_ffn_forward", "afd_ffn_forward_pipelined",
-           "afd_ffn_forward_host", "afd_ffn_forward_host_async", "afd_ffn_host_wait", "afd_ffn_debug_routing", "afd_ffn_check", "afd_ffn_last_error",
+           "afd_ffn_forward_host", "afd_ffn_forward_host_async", "afd_ffn_host_wait", "afd_ffn_debug_routing",
+           "afd_ffn_debug_inject", "afd_ffn_check", "afd_ffn_last_error",
            "afd_ffn_profile_begin", "afd_ffn_profile_end", "afd_ffn_launches_per_forward",
            "afd_ffn_device_bytes", "afd_ffn_router_noalloc", "afd_ffn_destroy"]
 
@@ -68,6 +71,8 @@ def lib():
         L.afd_ffn_forward_host_async.restype = ip
         L.afd_ffn_host_wait.argtypes = [vp]
         L.afd_ffn_host_wait.restype = ip
+        L.afd_ffn_debug_inject.argtypes = [vp, vp, ip, C.c_longlong]
+        L.afd_ffn_debug_inject.restype = ip
         L.afd_ffn_debug_routing.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.afd_ffn_debug_routing.restype = ip
         L.afd_ffn_check.argtypes = [vp, vp]
@@ -136,6 +141,10 @@ def afd_ffn_forward_host_async(h, n_micro, src_ptrs, src_counts, out_ptrs):
 
 def afd_ffn_host_wait(h):
     return _check(lib().afd_ffn_host_wait(h), h)
+
+
+def afd_ffn_debug_inject(h, stream, kind, arg):
+    return _check(lib().afd_ffn_debug_inject(h, stream, kind, arg), h)
 
 
 def afd_ffn_debug_routing(h, stream, topk_idx, topk_w, counts, offsets, perm_token, pos, logits):
@@ -279,6 +288,12 @@ class MoELayer:
                                                                    ("idx", "w", "counts", "offsets", "perm", "pos",
                                                                     "logits")])
         return r
+
+    def debug_inject(self, kind, arg=0, stream=None):
+        """Make a device-side check fire (INJECT_TIMEOUT: a bounded wait that runs out after
+        ``arg`` cycles; INJECT_RANGE: an out-of-range expert id in the routing tables); the
+        next check() reports it."""
+        return afd_ffn_debug_inject(self.handle, self._stream(stream), int(kind), int(arg))
 
     def check(self, stream=None):
         return afd_ffn_check(self.handle, self._stream(stream))

@@ -603,6 +603,29 @@ int afd_ffn_debug_routing(afd_ffn_t h, void* stream, int* topk_idx, float* topk_
   return AFD_OK;
 }
 
+int afd_ffn_debug_inject(afd_ffn_t h, void* stream, int kind, long long arg) {
+  if (!h) return AFD_EINVAL;
+  if (kind != AFD_INJECT_TIMEOUT && kind != AFD_INJECT_RANGE)
+    return fail(h, AFD_EINVAL, "unknown injection kind %d", kind);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Workspace& ws = h->ws[0];
+  int rc = alloc_workspace(h, ws);
+  if (rc) return rc;
+  if (kind == AFD_INJECT_TIMEOUT) {
+    const long long limit = arg < 1000 ? 1000 : (arg > 4000000000ll ? 4000000000ll : arg);
+    afd::wait_probe_kernel<<<1, 32, 0, s>>>(ws.err, limit);
+    CUDA_TRY(h, cudaGetLastError());
+    return AFD_OK;
+  }
+  // one token whose first expert id is E; the others valid
+  std::vector<int32_t> idx(h->cfg.k);
+  for (int j = 0; j < h->cfg.k; ++j) idx[j] = j == 0 ? h->cfg.E : j - 1;
+  CUDA_TRY(h, cudaMemcpyAsync(ws.topk_idx, idx.data(), idx.size() * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+  CUDA_TRY(h, cudaStreamSynchronize(s));  // idx is a host temporary
+  CUDA_TRY(h, afd::launch_routing(h->dims, 1, ws, s));
+  return AFD_OK;
+}
+
 int afd_ffn_check(afd_ffn_t h, void* stream) {
   if (!h) return AFD_EINVAL;
   CUDA_TRY(h, cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
@@ -616,7 +639,10 @@ int afd_ffn_check(afd_ffn_t h, void* stream) {
     CUDA_TRY(h, cudaMemset(ws.err, 0, sizeof(int)));
     word |= v;
   }
-  if (word) return fail(h, AFD_EDEVICE, "device error word 0x%x (1 = bounded wait timed out, 2 = routing value out of range)", word);
+  if (word)
+    return fail(h, AFD_EDEVICE, "device error word 0x%x:%s%s", word,
+                (word & afd::kErrTimeout) ? " a bounded wait timed out;" : "",
+                (word & afd::kErrRange) ? " a routing value was out of range;" : "");
   return AFD_OK;
 }
 

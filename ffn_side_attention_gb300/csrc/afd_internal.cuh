@@ -218,6 +218,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// A block that waits on a barrier nothing arrives on, through mbar_wait with a
+// limit of `limit` cycles: the fault-path test of the bounded waits (sets the
+// kErrTimeout bit and returns).
+__global__ void wait_probe_kernel(int* err, long long limit);
+
 // Bounded wait without the abort flag (drains in-flight copies and MMAs).
 __device__ __forceinline__ bool mbar_wait_cycles(uint64_t* bar, uint32_t parity, long long limit_cycles) {
   const long long t0 = clock64();

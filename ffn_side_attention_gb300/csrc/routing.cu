@@ -146,6 +146,18 @@ __global__ void __launch_bounds__(kTok)
 
 }  // namespace
 
+__global__ void wait_probe_kernel(int* err, long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  mbar_wait(&bar, 0, &abort, err, limit);  // phase 0 never completes
+}
+
 cudaError_t launch_routing(const LayerDims& d, int T, Workspace& ws, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int nblocks = (T + kTok - 1) / kTok;

@@ -195,6 +195,20 @@ int afd_ffn_debug_routing(afd_ffn_t h, void* stream, int* topk_idx, float* topk_
  * abandoned its work and returned), 2 = a routing value out of range. */
 int afd_ffn_check(afd_ffn_t h, void* stream);
 
+/* Fault-path hook for tests: makes one of the device-side checks fire without
+ * faulting or hanging the GPU, so that afd_ffn_check() can be seen to report it.
+ *   AFD_INJECT_TIMEOUT: one block waits on a barrier that nothing arrives on,
+ *     through the bounded wait every kernel uses, and gives up after `arg` SM
+ *     clock cycles (clamped to [1e3, 4e9]), setting bit 1 of the error word.
+ *   AFD_INJECT_RANGE: runs the routing-table kernels on a one-token batch whose
+ *     first expert id is E (out of range); their range check skips it and sets
+ *     bit 2.  This overwrites the routing afd_ffn_debug_routing() returns.
+ * Enqueued on `stream`.  The handle stays usable once afd_ffn_check() has read
+ * and cleared the word.  Any other kind returns AFD_EINVAL. */
+#define AFD_INJECT_TIMEOUT 1
+#define AFD_INJECT_RANGE 2
+int afd_ffn_debug_inject(afd_ffn_t h, void* stream, int kind, long long arg);
+
 /* Last error text of the handle ("" if none). */
 const char* afd_ffn_last_error(afd_ffn_t h);
 

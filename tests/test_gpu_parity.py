@@ -137,6 +137,30 @@ def test_forward_host_async_stream_of_batches(n_micro):
     layer.check()
 
 
+@pytest.mark.parametrize("kind,text", [(afd.INJECT_TIMEOUT, r"word 0x1: a bounded wait timed out;$"),
+                                       (afd.INJECT_RANGE, r"word 0x2: a routing value was out of range;$")])
+def test_device_checks_report_and_the_handle_recovers(kind, text):
+    """A bounded wait that runs out (nothing ever arrives; the wait gives up after ~1 ms)
+    and an out-of-range expert id in the routing tables each set the device error word,
+    afd_ffn_check reports it, and the next forward on the same handle is clean and
+    unchanged."""
+    c = _small(E=16, k=4, H=256, I=256)
+    counts = [20, 9]
+    srcs = synth.make_sources(c, "cuda", counts=counts)
+    w = synth.make_weights(c, "cuda")
+    layer = make_layer(c, w, max_tokens=64, max_sources=4)
+    before = torch.cat(layer.forward(srcs)).clone()
+    layer.check()
+    layer.debug_inject(kind, 2_000_000)
+    with pytest.raises(afd.AfdError, match=text):
+        layer.check()
+    after = torch.cat(layer.forward(srcs))
+    layer.check()
+    assert torch.equal(before, after)
+    with pytest.raises(afd.AfdError):
+        layer.debug_inject(7)
+
+
 def test_launches_per_forward_by_batch():
     """One router launch for small batches, three (stage, logits, select) for
     large ones; then 2 routing, pack, 2 GEMMs, combine."""
