@@ -48,24 +48,39 @@ __device__ __forceinline__ int packed_rows(const int32_t* __restrict__ pos, int 
   return n;
 }
 
-// Work unit = (token, 512-byte chunk of its row): one warp, 16 bytes per lane;
-// units spread over the grid keep many rows' copies in flight at once.
+// Work unit = (token, kPackG consecutive 512-byte chunks of its row): one warp,
+// 16 bytes per lane per chunk; the unit's kPackG loads are all issued before its
+// stores, and units spread over the grid keep many rows' copies in flight.
+constexpr int kPackG = 4;
+
 // bf16 / fp32 layers: row copy.
 __global__ void __launch_bounds__(256) pack_copy_kernel(SrcTable st, const int32_t* __restrict__ pos, int T, int k,
                                                         int S, int row_bytes, uint8_t* __restrict__ P) {
   pdl_begin();
   const int lane = threadIdx.x & 31;
   const int nchunk = (row_bytes + 511) >> 9;  // 512 bytes per warp step
+  const int ngroup = (nchunk + kPackG - 1) / kPackG;
   const int nvec = row_bytes >> 4;
-  const long units = (long)T * nchunk;
+  const long units = (long)T * ngroup;
   for (long u = (long)blockIdx.x * 8 + (threadIdx.x >> 5); u < units; u += (long)gridDim.x * 8) {
-    const int t = (int)(u / nchunk), c = (int)(u - (long)t * nchunk);
-    const int v = c * 32 + lane;
-    if (v >= nvec) continue;
+    const int t = (int)(u / ngroup), c0 = (int)(u - (long)t * ngroup) * kPackG;
     int rows[kMaxCopies];
     const int n = packed_rows(pos, t, T, k, S, rows);
-    const uint4 x = __ldg(reinterpret_cast<const uint4*>(src_row(st, t, row_bytes)) + v);
-    for (int q = 0; q < n; ++q) reinterpret_cast<uint4*>(P + (size_t)rows[q] * row_bytes)[v] = x;
+    const uint4* src = reinterpret_cast<const uint4*>(src_row(st, t, row_bytes));
+    uint4 x[kPackG];
+#pragma unroll
+    for (int g = 0; g < kPackG; ++g) {
+      const int v = (c0 + g) * 32 + lane;
+      if (v < nvec) x[g] = __ldg(src + v);
+    }
+    for (int q = 0; q < n; ++q) {
+      uint4* dst = reinterpret_cast<uint4*>(P + (size_t)rows[q] * row_bytes);
+#pragma unroll
+      for (int g = 0; g < kPackG; ++g) {
+        const int v = (c0 + g) * 32 + lane;
+        if (v < nvec) dst[v] = x[g];
+      }
+    }
   }
 }
 
@@ -79,32 +94,41 @@ __global__ void __launch_bounds__(256) pack_fp8_kernel(SrcTable st, const int32_
   pdl_begin();
   const int lane = threadIdx.x & 31;
   const int nchunk = H >> 8;  // H % 256 == 0: whole warp active
-  const long units = (long)T * nchunk;
+  const int ngroup = (nchunk + kPackG - 1) / kPackG;
+  const long units = (long)T * ngroup;
   for (long u = (long)blockIdx.x * 8 + (threadIdx.x >> 5); u < units; u += (long)gridDim.x * 8) {
-    const int t = (int)(u / nchunk), c = (int)(u - (long)t * nchunk);
-    const int v = c * 32 + lane;
+    const int t = (int)(u / ngroup), c0 = (int)(u - (long)t * ngroup) * kPackG;
     int rows[kMaxCopies];
     const int n = packed_rows(pos, t, T, k, S, rows);
-    const uint4 x8 = __ldg(reinterpret_cast<const uint4*>(src_row(st, t, (size_t)H * 2)) + v);
-    const float x[8] = {bf16_lo(x8.x), bf16_hi(x8.x), bf16_lo(x8.y), bf16_hi(x8.y),
-                        bf16_lo(x8.z), bf16_hi(x8.z), bf16_lo(x8.w), bf16_hi(x8.w)};
-    float amax = 0.0f;
+    const uint4* src = reinterpret_cast<const uint4*>(src_row(st, t, (size_t)H * 2));
+    uint4 x8[kPackG];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(x[q]));
+    for (int g = 0; g < kPackG; ++g)
+      if (c0 + g < nchunk) x8[g] = __ldg(src + (c0 + g) * 32 + lane);
 #pragma unroll
-    for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float scale = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
-    uint2 q = make_uint2(0u, 0u);
-    if (amax != 0.0f) {
-      const uint32_t q01 = cvt_e4m3x2(__fdiv_rn(x[1], scale), __fdiv_rn(x[0], scale));
-      const uint32_t q23 = cvt_e4m3x2(__fdiv_rn(x[3], scale), __fdiv_rn(x[2], scale));
-      const uint32_t q45 = cvt_e4m3x2(__fdiv_rn(x[5], scale), __fdiv_rn(x[4], scale));
-      const uint32_t q67 = cvt_e4m3x2(__fdiv_rn(x[7], scale), __fdiv_rn(x[6], scale));
-      q = make_uint2(q01 | (q23 << 16), q45 | (q67 << 16));
-    }
-    for (int r = 0; r < n; ++r) {
-      reinterpret_cast<uint2*>(P + (size_t)rows[r] * H)[v] = q;
-      if ((lane & 15) == 0) P_scale[(size_t)(v >> 4) * scale_ld + rows[r]] = scale;
+    for (int g = 0; g < kPackG; ++g) {
+      if (c0 + g >= nchunk) break;
+      const int v = (c0 + g) * 32 + lane;
+      const float x[8] = {bf16_lo(x8[g].x), bf16_hi(x8[g].x), bf16_lo(x8[g].y), bf16_hi(x8[g].y),
+                          bf16_lo(x8[g].z), bf16_hi(x8[g].z), bf16_lo(x8[g].w), bf16_hi(x8[g].w)};
+      float amax = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(x[q]));
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const float scale = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+      uint2 q = make_uint2(0u, 0u);
+      if (amax != 0.0f) {
+        const uint32_t q01 = cvt_e4m3x2(__fdiv_rn(x[1], scale), __fdiv_rn(x[0], scale));
+        const uint32_t q23 = cvt_e4m3x2(__fdiv_rn(x[3], scale), __fdiv_rn(x[2], scale));
+        const uint32_t q45 = cvt_e4m3x2(__fdiv_rn(x[5], scale), __fdiv_rn(x[4], scale));
+        const uint32_t q67 = cvt_e4m3x2(__fdiv_rn(x[7], scale), __fdiv_rn(x[6], scale));
+        q = make_uint2(q01 | (q23 << 16), q45 | (q67 << 16));
+      }
+      for (int r = 0; r < n; ++r) {
+        reinterpret_cast<uint2*>(P + (size_t)rows[r] * H)[v] = q;
+        if ((lane & 15) == 0) P_scale[(size_t)(v >> 4) * scale_ld + rows[r]] = scale;
+      }
     }
   }
 }
@@ -192,7 +216,7 @@ cudaError_t launch_pack(const SrcTable& st, const LayerDims& d, int T, Workspace
                         cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int row_bytes = d.H * (d.dtype == AFD_FP32 ? 4 : 2);
-  const int grid = grid_for(8, T * ((row_bytes + 511) / 512), num_sms);
+  const int grid = grid_for(8, T * (((row_bytes + 511) / 512 + kPackG - 1) / kPackG), num_sms);
   if (d.dtype == AFD_FP8_E4M3)
     {
       const cudaError_t e_ = launch_k(pack_fp8_kernel, dim3(grid), dim3(256), 0, s, st, ws.pos, T, d.k, d.S, d.H,
