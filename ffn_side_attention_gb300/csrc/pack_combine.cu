@@ -48,10 +48,13 @@ __device__ __forceinline__ int packed_rows(const int32_t* __restrict__ pos, int 
   return n;
 }
 
-// Work unit = (token, kPackG consecutive 512-byte chunks of its row): one warp,
-// 16 bytes per lane per chunk; the unit's kPackG loads are all issued before its
-// stores, and units spread over the grid keep many rows' copies in flight.
-constexpr int kPackG = 4;
+// Work unit = (token, G consecutive 512-byte chunks of its row): one warp, 16
+// bytes per lane per chunk; the unit's G loads are all issued before its stores,
+// and units spread over the grid keep many rows' copies in flight.  G was
+// measured: 8 for the plain copy, 4 where the unit also quantises (8 made the
+// DeepSeek-V3 fp8 pack slower).
+constexpr int kPackGCopy = 8;
+constexpr int kPackGFp8 = 4;
 
 // bf16 / fp32 layers: row copy.
 __global__ void __launch_bounds__(256) pack_copy_kernel(SrcTable st, const int32_t* __restrict__ pos, int T, int k,
@@ -59,24 +62,24 @@ __global__ void __launch_bounds__(256) pack_copy_kernel(SrcTable st, const int32
   pdl_begin();
   const int lane = threadIdx.x & 31;
   const int nchunk = (row_bytes + 511) >> 9;  // 512 bytes per warp step
-  const int ngroup = (nchunk + kPackG - 1) / kPackG;
+  const int ngroup = (nchunk + kPackGCopy - 1) / kPackGCopy;
   const int nvec = row_bytes >> 4;
   const long units = (long)T * ngroup;
   for (long u = (long)blockIdx.x * 8 + (threadIdx.x >> 5); u < units; u += (long)gridDim.x * 8) {
-    const int t = (int)(u / ngroup), c0 = (int)(u - (long)t * ngroup) * kPackG;
+    const int t = (int)(u / ngroup), c0 = (int)(u - (long)t * ngroup) * kPackGCopy;
     int rows[kMaxCopies];
     const int n = packed_rows(pos, t, T, k, S, rows);
     const uint4* src = reinterpret_cast<const uint4*>(src_row(st, t, row_bytes));
-    uint4 x[kPackG];
+    uint4 x[kPackGCopy];
 #pragma unroll
-    for (int g = 0; g < kPackG; ++g) {
+    for (int g = 0; g < kPackGCopy; ++g) {
       const int v = (c0 + g) * 32 + lane;
       if (v < nvec) x[g] = __ldg(src + v);
     }
     for (int q = 0; q < n; ++q) {
       uint4* dst = reinterpret_cast<uint4*>(P + (size_t)rows[q] * row_bytes);
 #pragma unroll
-      for (int g = 0; g < kPackG; ++g) {
+      for (int g = 0; g < kPackGCopy; ++g) {
         const int v = (c0 + g) * 32 + lane;
         if (v < nvec) dst[v] = x[g];
       }
@@ -94,19 +97,19 @@ __global__ void __launch_bounds__(256) pack_fp8_kernel(SrcTable st, const int32_
   pdl_begin();
   const int lane = threadIdx.x & 31;
   const int nchunk = H >> 8;  // H % 256 == 0: whole warp active
-  const int ngroup = (nchunk + kPackG - 1) / kPackG;
+  const int ngroup = (nchunk + kPackGFp8 - 1) / kPackGFp8;
   const long units = (long)T * ngroup;
   for (long u = (long)blockIdx.x * 8 + (threadIdx.x >> 5); u < units; u += (long)gridDim.x * 8) {
-    const int t = (int)(u / ngroup), c0 = (int)(u - (long)t * ngroup) * kPackG;
+    const int t = (int)(u / ngroup), c0 = (int)(u - (long)t * ngroup) * kPackGFp8;
     int rows[kMaxCopies];
     const int n = packed_rows(pos, t, T, k, S, rows);
     const uint4* src = reinterpret_cast<const uint4*>(src_row(st, t, (size_t)H * 2));
-    uint4 x8[kPackG];
+    uint4 x8[kPackGFp8];
 #pragma unroll
-    for (int g = 0; g < kPackG; ++g)
+    for (int g = 0; g < kPackGFp8; ++g)
       if (c0 + g < nchunk) x8[g] = __ldg(src + (c0 + g) * 32 + lane);
 #pragma unroll
-    for (int g = 0; g < kPackG; ++g) {
+    for (int g = 0; g < kPackGFp8; ++g) {
       if (c0 + g >= nchunk) break;
       const int v = (c0 + g) * 32 + lane;
       const float x[8] = {bf16_lo(x8[g].x), bf16_hi(x8[g].x), bf16_lo(x8[g].y), bf16_hi(x8[g].y),
@@ -216,7 +219,8 @@ cudaError_t launch_pack(const SrcTable& st, const LayerDims& d, int T, Workspace
                         cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int row_bytes = d.H * (d.dtype == AFD_FP32 ? 4 : 2);
-  const int grid = grid_for(8, T * (((row_bytes + 511) / 512 + kPackG - 1) / kPackG), num_sms);
+  const int G = d.dtype == AFD_FP8_E4M3 ? kPackGFp8 : kPackGCopy;
+  const int grid = grid_for(8, T * (((row_bytes + 511) / 512 + G - 1) / G), num_sms);
   if (d.dtype == AFD_FP8_E4M3)
     {
       const cudaError_t e_ = launch_k(pack_fp8_kernel, dim3(grid), dim3(256), 0, s, st, ws.pos, T, d.k, d.S, d.H,
