@@ -274,6 +274,28 @@ __device__ __forceinline__ void canonical_dot2_warp(const uint16_t* __restrict__
   v2 = p2;
 }
 
+// Four canonical dots in one pass (x read once for four expert rows).
+__device__ __forceinline__ void canonical_dot4_warp(const uint16_t* __restrict__ x, const uint16_t* const (&w)[4],
+                                                    int H, int lane, float (&v)[4]) {
+  const int nc = H >> 3;
+  const uint4* xa = reinterpret_cast<const uint4*>(x);
+  float p[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  for (int c = lane; c < nc; c += 32) {
+    const uint4 a = __ldg(xa + c);
+    uint4 b[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) b[i] = __ldg(reinterpret_cast<const uint4*>(w[i]) + c);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[i] = chain8(a, b[i], p[i]);
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[i] = p[i] + __shfl_xor_sync(0xffffffffu, p[i], o);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = p[i];
+}
+
 // The same two dots with the token row in shared memory (xs: this warp's copy).
 __device__ __forceinline__ void canonical_dot2_xs(const uint4* xs, const uint16_t* __restrict__ w1,
                                                   const uint16_t* __restrict__ w2, int H, int lane, float& v1,
@@ -457,37 +479,85 @@ __global__ void __launch_bounds__(256, MINB) router_select_warp_kernel(const Sel
     ncand += __popc(cmask[q]);
   }
   const bool all = ncand > kMaxCand;
-  // canonical logits of the candidates (all experts when too many), two at a time
+  // canonical logits of the candidates (all experts when too many)
   float lc[PER];
+  if (XS) {  // token row in shared memory: two candidates of a group of 32 per pass
 #pragma unroll
-  for (int q = 0; q < PER; ++q) {
-    lc[q] = -INFINITY;
-    unsigned msk = all ? __ballot_sync(0xffffffffu, !taken[q]) : cmask[q];
-    while (msk) {
-      const int s1 = __ffs(msk) - 1;
-      msk &= msk - 1;
-      const int e1 = s1 + 32 * q;
-      float v1, v2 = 0.0f;
-      int s2 = -1;
-      if (msk) {
-        s2 = __ffs(msk) - 1;
+    for (int q = 0; q < PER; ++q) {
+      lc[q] = -INFINITY;
+      unsigned msk = all ? __ballot_sync(0xffffffffu, !taken[q]) : cmask[q];
+      while (msk) {
+        const int s1 = __ffs(msk) - 1;
         msk &= msk - 1;
-        const uint16_t* w1 = a.wrT + (size_t)e1 * a.H;
-        const uint16_t* w2 = a.wrT + (size_t)(s2 + 32 * q) * a.H;
-        if (XS)
-          canonical_dot2_xs(xs, w1, w2, a.H, lane, v1, v2);
-        else
-          canonical_dot2_warp(x, w1, w2, a.H, lane, v1, v2);
-      } else {
-        v1 = XS ? canonical_dot_xs(xs, a.wrT + (size_t)e1 * a.H, a.H, lane)
-                : canonical_dot_warp<1>(x, a.wrT + (size_t)e1 * a.H, a.H, lane);
+        const int e1 = s1 + 32 * q;
+        float v1, v2 = 0.0f;
+        int s2 = -1;
+        if (msk) {
+          s2 = __ffs(msk) - 1;
+          msk &= msk - 1;
+          canonical_dot2_xs(xs, a.wrT + (size_t)e1 * a.H, a.wrT + (size_t)(s2 + 32 * q) * a.H, a.H, lane, v1, v2);
+        } else {
+          v1 = canonical_dot_xs(xs, a.wrT + (size_t)e1 * a.H, a.H, lane);
+        }
+        if (a.bias) v1 = __fadd_rn(v1, __ldg(a.bias + e1));
+        if (lane == s1) lc[q] = v1;
+        if (s2 >= 0) {
+          if (a.bias) v2 = __fadd_rn(v2, __ldg(a.bias + s2 + 32 * q));
+          if (lane == s2) lc[q] = v2;
+        }
       }
-      if (a.bias) v1 = __fadd_rn(v1, __ldg(a.bias + e1));
-      if (lane == s1) lc[q] = v1;
-      if (s2 >= 0) {
-        if (a.bias) v2 = __fadd_rn(v2, __ldg(a.bias + s2 + 32 * q));
-        if (lane == s2) lc[q] = v2;
+    }
+  } else {  // token row from L2: up to four candidates (from any group) per pass over it
+    unsigned cm[PER];  // candidates still to compute, per group of 32 experts (warp-uniform)
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      lc[q] = -INFINITY;
+      cm[q] = all ? __ballot_sync(0xffffffffu, !taken[q]) : cmask[q];
+    }
+    // the value of expert e goes to lane e % 32 of group e / 32
+    auto put = [&](int e, float v) {
+      if (a.bias) v = __fadd_rn(v, __ldg(a.bias + e));
+#pragma unroll
+      for (int q = 0; q < PER; ++q)
+        if (q == (e >> 5) && lane == (e & 31)) lc[q] = v;
+    };
+    auto next = [&]() {  // lowest remaining candidate
+      int e = -1;
+#pragma unroll
+      for (int q = PER - 1; q >= 0; --q)
+        if (cm[q]) e = 32 * q + __ffs(cm[q]) - 1;
+#pragma unroll
+      for (int q = 0; q < PER; ++q)
+        if (q == (e >> 5)) cm[q] &= cm[q] - 1;
+      return e;
+    };
+    int left = 0;
+#pragma unroll
+    for (int q = 0; q < PER; ++q) left += __popc(cm[q]);
+    for (; left >= 4; left -= 4) {
+      int e4[4];
+      const uint16_t* w4[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        e4[i] = next();
+        w4[i] = a.wrT + (size_t)e4[i] * a.H;
       }
+      float v4[4];
+      canonical_dot4_warp(x, w4, a.H, lane, v4);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) put(e4[i], v4[i]);
+    }
+    if (left >= 2) {
+      const int e1 = next(), e2 = next();
+      float v1, v2;
+      canonical_dot2_warp(x, a.wrT + (size_t)e1 * a.H, a.wrT + (size_t)e2 * a.H, a.H, lane, v1, v2);
+      put(e1, v1);
+      put(e2, v2);
+      left -= 2;
+    }
+    if (left) {
+      const int e1 = next();
+      put(e1, canonical_dot_warp<1>(x, a.wrT + (size_t)e1 * a.H, a.H, lane));
     }
   }
   // logits row for inspection: canonical where computed (the estimate stays elsewhere)
