@@ -37,7 +37,9 @@
  *   - The caller owns every buffer it passes in; the library owns its copies
  *     of the weights and its workspaces, freed by afd_ffn_destroy().
  *   - One handle runs one forward at a time: calls on one handle must not
- *     overlap on the GPU (use afd_ffn_forward_pipelined for concurrency).
+ *     overlap on the GPU.  afd_ffn_forward_pipelined (micro-batches) and
+ *     afd_ffn_forward_host_async (a stream of batches) order their own
+ *     concurrency on library streams.
  */
 #ifndef AFD_FFN_H_
 #define AFD_FFN_H_
@@ -203,7 +205,8 @@ int afd_ffn_check(afd_ffn_t h, void* stream);
  *   AFD_INJECT_RANGE: runs the routing-table kernels on a one-token batch whose
  *     first expert id is E (out of range); their range check skips it and sets
  *     bit 2.  This overwrites the routing afd_ffn_debug_routing() returns.
- * Enqueued on `stream`.  The handle stays usable once afd_ffn_check() has read
+ * Enqueued on `stream` (AFD_INJECT_RANGE first synchronises it once, for its
+ * host-side token).  The handle stays usable once afd_ffn_check() has read
  * and cleared the word.  Any other kind returns AFD_EINVAL. */
 #define AFD_INJECT_TIMEOUT 1
 #define AFD_INJECT_RANGE 2
