@@ -88,6 +88,27 @@ def test_pipelined_equals_single_and_deterministic():
     layer.check()
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_outputs_follow_their_tokens(dtype):
+    """Per-token independence on the GPU: permuting tokens within and across the source
+    buffers (and changing how many buffers carry them) permutes the outputs bit for bit."""
+    c = _small(dtype=dtype, E=16, k=4, H=256, I=256, S=1)
+    counts = [37, 0, 91]
+    srcs = synth.make_sources(c, "cuda", seed=5, counts=counts)
+    w = synth.make_weights(c, "cuda", seed=5)
+    layer = make_layer(c, w, max_tokens=160, max_sources=4)
+    x = torch.cat(srcs)
+    y = torch.cat(layer.forward(srcs)).clone()
+    torch.cuda.synchronize()
+    perm = torch.randperm(x.shape[0], generator=torch.Generator().manual_seed(11)).to(x.device)
+    xp = x[perm]
+    regrouped = [xp[:50].contiguous(), xp[50:51].contiguous(), xp[51:].contiguous()]
+    yp = torch.cat(layer.forward(regrouped))
+    torch.cuda.synchronize()
+    layer.check()
+    assert torch.equal(yp, y[perm])
+
+
 def test_forward_host_equals_device():
     c = _small(E=16, k=4, H=256, I=256)
     counts = [20, 9]
