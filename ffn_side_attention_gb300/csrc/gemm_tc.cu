@@ -53,6 +53,7 @@ constexpr int kEpiWarps = 16;
 constexpr int kTokWarp = 2 + kEpiWarps;       // token producer
 constexpr int kThreads = 32 * (kTokWarp + 1);  // 608
 constexpr int kWTileBytes = 2 * kATile;      // one weight stage: two 128-row tiles
+constexpr int kEvenRounds = 4;  // launches of at most this many item rounds share them out evenly
 constexpr int kPfSteps = 4;                  // weight K blocks prefetched into L2 ahead of the loads
 
 // Tile shape per token-tile width BN: 128 -> 5 weight + 3 token stages and
@@ -180,6 +181,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   const int total = args.MT * s_tb[G];
+  // Equal rounds for short launches: with R = ceil(total / grid) <= kEvenRounds rounds, only
+  // ceil(total / R) CTAs take items, R (or R - 1) each, instead of a last round where a few
+  // SMs stream one more item each at the rate one SM reaches alone.  With more rounds that
+  // tail is a small share and the SMs left idle would cost more than it.
+  const int rounds = total > 0 ? (total + (int)gridDim.x - 1) / (int)gridDim.x : 1;
+  const int nact = rounds <= kEvenRounds ? (total + rounds - 1) / rounds : (int)gridDim.x;
+  const int first = (int)blockIdx.x < nact ? (int)blockIdx.x : total;  // idle CTAs take none
   volatile int* abort = &s_abort;
 
   if (warp == 0 || warp == kTokWarp) {
@@ -200,10 +208,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         rb1 = rb0 + args.a1_offset / 128;
       };
       // L2 prefetch cursor (weights only): runs kPfSteps K blocks ahead of the loads
-      int pf_item = blockIdx.x, pf_kb = 0, pf_rb0 = 0, pf_rb1 = 0;
+      int pf_item = first, pf_kb = 0, pf_rb0 = 0, pf_rb1 = 0;
       long pf_n = 0, ld_n = 0;
       if (wprod && pf_item < total) row_blocks(decode_item<BN>(pf_item, args.MT, G, s_tb, s_off, s_cnt), pf_rb0, pf_rb1);
-      for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
+      for (int item = first; ok && item < total; item += nact) {
         const Item it = decode_item<BN>(item, args.MT, G, s_tb, s_off, s_cnt);
         int rb0, rb1;
         row_blocks(it, rb0, rb1);
@@ -216,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_prefetch_l2_2d(&tmA1, 0, (pf_rb1 * args.num_kb + pf_kb) * 128);
               if (++pf_kb == args.num_kb) {
                 pf_kb = 0;
-                pf_item += gridDim.x;
+                pf_item += nact;
                 if (pf_item < total)
                   row_blocks(decode_item<BN>(pf_item, args.MT, G, s_tb, s_off, s_cnt), pf_rb0, pf_rb1);
               }
@@ -253,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int ws_ = 0, xs = 0;
       uint32_t wph = 0, xph = 0, ic = 0;
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < total; item += gridDim.x, ++ic) {
+      for (int item = first; ok && item < total; item += nact, ++ic) {
         const Item it = decode_item<BN>(item, args.MT, G, s_tb, s_off, s_cnt);
         const int N = (it.nrows + 15) & ~15;
         const uint32_t idesc = mma_idesc(1u, kGemmBM, N);
@@ -300,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quad * 32 + lane;  // row of the 128-row MMA tile
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
     uint32_t ic = 0;
-    for (int item = blockIdx.x; item < total; item += gridDim.x, ++ic) {
+    for (int item = first; item < total; item += nact, ++ic) {
       const Item it = decode_item<BN>(item, args.MT, G, s_tb, s_off, s_cnt);
       const uint32_t a = ic % kAbuf;
       if (!mbar_wait(&tfull[a], (ic / kAbuf) & 1u, abort, args.err)) break;
