@@ -139,7 +139,7 @@ int alloc_workspace(afd_ffn* h, Workspace& ws) {
       (rc = dmalloc_t(h, &ws.tile_counter, (T + afd::kRouterTokTile - 1) / afd::kRouterTokTile)) ||
       (rc = dmalloc_t(h, &ws.tok_ticket, T)) ||
       (rc = dmalloc_t(h, &ws.counts, G)) || (rc = dmalloc_t(h, &ws.offsets, G + 1)) ||
-      (rc = dmalloc_t(h, &ws.tile_base, G + 1)) || (rc = dmalloc_t(h, &ws.block_hist, ((T + 255) / 256) * E)) ||
+      (rc = dmalloc_t(h, &ws.tile_base, G + 1)) || (rc = dmalloc_t(h, &ws.gu_done, G)) || (rc = dmalloc_t(h, &ws.block_hist, ((T + 255) / 256) * E)) ||
       (rc = dmalloc_t(h, &ws.perm, R)) ||
       (rc = dmalloc_t(h, &ws.pos, T * k)) || (rc = dmalloc(h, &ws.P, R * c.H * ab)) ||
       (rc = dmalloc(h, &ws.Hb, R * c.I * (c.dtype == AFD_FP8_E4M3 ? 1 : act_bytes(c)))) ||

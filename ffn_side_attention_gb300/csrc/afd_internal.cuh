@@ -55,6 +55,7 @@ struct Workspace {
   int32_t* counts = nullptr;    // [E+S]
   int32_t* offsets = nullptr;   // [E+S+1]
   int32_t* tile_base = nullptr; // [E+S+1], prefix of ceil(counts / GEMM tile tokens)
+  int32_t* gu_done = nullptr;   // [E+S] gate/up items finished per group (bf16 GEMMs; zeroed by the routing)
   int32_t* block_hist = nullptr; // [ceil(maxT/256)][E] per-block expert counts of the routing kernels
   int32_t* perm = nullptr;      // [max_rows] token of each packed row
   int32_t* pos = nullptr;       // [maxT*k]  packed row of each (t, j)
@@ -93,6 +94,14 @@ __device__ __forceinline__ void pdl_begin() {
 // before waiting.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Order this thread's earlier generic-proxy accesses (an acquire that saw another CTA's
+// data) before its later async-proxy ones (TMA reads of that data).
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                             Args&&... args) {

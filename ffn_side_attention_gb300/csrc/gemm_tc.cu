@@ -85,6 +85,12 @@ struct TcArgs {
   int ld_out;
   int mode;              // 0: SwiGLU(D0, D1) ; 1: D0 | D1 as two column blocks
   int* err;
+  // Per-group progress of the gate/up launch: mode 0 adds one per epilogue warp per item
+  // once that warp's h stores are visible; mode 1 (down) loads a group's h rows once the
+  // count reaches kEpiWarps * done_mt * (its token tiles), instead of waiting for the
+  // whole gate/up grid.  Null: mode 1 waits for the previous grid.
+  int32_t* done;
+  int done_mt;           // gate/up items per token tile (I / 128)
 };
 
 struct Item {
@@ -110,6 +116,24 @@ __device__ __forceinline__ Item decode_item(int item, int MT, int G, const int* 
   return it;
 }
 
+
+// Wait until *p >= target (acquire), with the same bound and abort flag as mbar_wait.
+__device__ __forceinline__ bool wait_count(const int* p, int target, volatile int* abort, int* err) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(p) >= target) return true;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (clock64() - t0 > 4000000000ll) {
+        *abort = 1;
+        atomicOr(err, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
 
 __device__ __forceinline__ uint16_t f2bf(float v) {
   __nv_bfloat16 b = __float2bfloat16_rn(v);
@@ -198,7 +222,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t* fb = wprod ? wfull : xfull;
       uint64_t* eb = wprod ? wempty : xempty;
       const uint64_t pol = wprod ? l2_policy_evict_first() : l2_policy_evict_last();
-      if (!wprod) pdl_wait();  // the token operand is the previous kernel's output
+      // the token operand is the previous kernel's output: the whole grid (gate/up, after the
+      // pack) or, for down with progress counters, each group's gate/up items (below)
+      const bool per_group = args.mode == 1 && args.done != nullptr;
+      if (!wprod && !per_group) pdl_wait();
+      int ready_g = -1;
       int s = 0;
       uint32_t ph = 0, filled = 0, fill_ph = 0;
       bool ok = true;
@@ -217,6 +245,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         row_blocks(it, rb0, rb1);
         const int nbox = (it.nrows + kBBoxRows - 1) / kBBoxRows;
         const uint32_t bytes = wprod ? (uint32_t)kWTileBytes : (uint32_t)(nbox * kBBoxRows * kRowBytes);
+        if (!wprod && per_group && it.g != ready_g) {
+          const int target = kEpiWarps * args.done_mt * (s_tb[it.g + 1] - s_tb[it.g]);
+          if (!wait_count(args.done + it.g, target, abort, args.err)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();  // the TMA reads below see the h rows the count covers
+          ready_g = it.g;
+        }
         for (int kb = 0; kb < args.num_kb; ++kb, ++ld_n) {
           if (wprod)
             for (; pf_n <= ld_n + kPfSteps && pf_item < total; ++pf_n) {
@@ -346,6 +383,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[a]);
+      if (args.mode == 0 && args.done != nullptr) {  // this warp's h stores of the item are out
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(args.done + it.g, 1);
+      }
     }
   }
 
@@ -389,6 +431,7 @@ static cudaError_t launch_bn(const LayerDims& d, int T, const TcWeights& w, Work
     a.out = static_cast<uint16_t*>(ws.Hb);
     a.ld_out = d.I;
     a.mode = 0;
+    a.done = ws.gu_done;
     m0 = w.tm_wg;
     m1 = w.tm_wu;
     mb = &ws.tm_P;
@@ -401,6 +444,8 @@ static cudaError_t launch_bn(const LayerDims& d, int T, const TcWeights& w, Work
     a.out = static_cast<uint16_t*>(ws.Y);
     a.ld_out = d.H;
     a.mode = 1;
+    a.done = ws.gu_done;
+    a.done_mt = d.I / kGemmBM;
     m0 = w.tm_wd;
     m1 = w.tm_wd;
     mb = &ws.tm_H;

@@ -85,7 +85,8 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
 __global__ void __launch_bounds__(kTok)
     place_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ block_hist, int nblocks, int T, int k,
                  int E, int S, int BN, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                 int32_t* __restrict__ tile_base, int32_t* __restrict__ perm, int32_t* __restrict__ pos) {
+                 int32_t* __restrict__ tile_base, int32_t* __restrict__ perm, int32_t* __restrict__ pos,
+                 int32_t* __restrict__ gu_done) {
   pdl_begin();
   __shared__ int s_cnt[kMaxExperts + 1], s_base[kMaxExperts], s_off[kMaxExperts + 1], s_tb[kMaxExperts + 1];
   const int G = E + S;
@@ -128,7 +129,10 @@ __global__ void __launch_bounds__(kTok)
     for (int g = threadIdx.x; g <= G; g += kTok) {
       offsets[g] = s_off[g];
       tile_base[g] = s_tb[g];
-      if (g < G) counts[g] = s_cnt[g];
+      if (g < G) {
+        counts[g] = s_cnt[g];
+        gu_done[g] = 0;  // this forward's gate/up GEMM counts its finished items here
+      }
     }
   const int t = blockIdx.x * kTok + threadIdx.x;
   if (t < T) {
@@ -173,7 +177,7 @@ cudaError_t launch_routing(const LayerDims& d, int T, Workspace& ws, cudaStream_
   {
     const cudaError_t e_ = launch_k(place_kernel, dim3(nblocks), dim3(kTok), 0, s, ws.topk_idx, ws.block_hist,
                                     nblocks, T, d.k, d.E, d.S, bn, ws.counts, ws.offsets, ws.tile_base, ws.perm,
-                                    ws.pos);
+                                    ws.pos, ws.gu_done);
     if (e_ != cudaSuccess) return e_;
   }
   return cudaGetLastError();
