@@ -232,6 +232,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 // kErrTimeout bit and returns).
 __global__ void wait_probe_kernel(int* err, long long limit);
 
+// Wait until *p >= target (acquire), with the same bound and abort flag as mbar_wait.
+__device__ __forceinline__ bool wait_count(const int* p, int target, volatile int* abort, int* err) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(p) >= target) return true;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (clock64() - t0 > 4000000000ll) {
+        *abort = 1;
+        atomicOr(err, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
 // Bounded wait without the abort flag (drains in-flight copies and MMAs).
 __device__ __forceinline__ bool mbar_wait_cycles(uint64_t* bar, uint32_t parity, long long limit_cycles) {
   const long long t0 = clock64();

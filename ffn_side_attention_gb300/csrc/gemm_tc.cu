@@ -117,24 +117,6 @@ __device__ __forceinline__ Item decode_item(int item, int MT, int G, const int* 
 }
 
 
-// Wait until *p >= target (acquire), with the same bound and abort flag as mbar_wait.
-__device__ __forceinline__ bool wait_count(const int* p, int target, volatile int* abort, int* err) {
-  if (ld_acquire_gpu(p) >= target) return true;
-  const long long t0 = clock64();
-  for (uint32_t it = 1;; ++it) {
-    __nanosleep(64);
-    if (ld_acquire_gpu(p) >= target) return true;
-    if ((it & 63u) == 0) {
-      if (*abort) return false;
-      if (clock64() - t0 > 4000000000ll) {
-        *abort = 1;
-        atomicOr(err, kErrTimeout);
-        return false;
-      }
-    }
-  }
-}
-
 __device__ __forceinline__ uint16_t f2bf(float v) {
   __nv_bfloat16 b = __float2bfloat16_rn(v);
   return *reinterpret_cast<uint16_t*>(&b);
