@@ -101,11 +101,6 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
 }
 // Order this thread's earlier generic-proxy accesses (an acquire that saw another CTA's
 // data) before its later async-proxy ones (TMA reads of that data).
-// *p += v with release semantics at GPU scope (cumulative: covers what this thread
-// observed through an earlier CTA barrier)
-__device__ __forceinline__ void red_release_add(int* p, int v) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
