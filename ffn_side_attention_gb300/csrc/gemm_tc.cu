@@ -24,6 +24,12 @@
 // the device from tile_base (no host sync); items of one (g, m tile) are
 // adjacent so concurrently running CTAs share the weight tile in L2.  The
 // kernel is persistent: grid = SM count, CTA c takes items c, c+grid, ...
+// (launches of at most four rounds spread them evenly over fewer CTAs).
+//
+// The down launch starts before the gate/up launch ends: the gate/up epilogue
+// warps count each expert's finished items (after a fence on their h stores)
+// and the down token producer loads an expert's h rows once its count is
+// complete, so experts whose gate/up is done proceed during the gate/up tail.
 //
 // Warp roles (608 threads): warp 0 lane 0 streams weight tiles into their
 // own ring (L2 evict-first); warp 18 lane 0 streams the token tiles into a
