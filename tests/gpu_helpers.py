@@ -73,12 +73,14 @@ def assert_routing_exact(c: synth.LayerConfig, r: dict, ref: dict, T: int):
     assert np.array_equal(r["pos"].cpu().numpy(), pos)
 
 
-def run_case(c: synth.LayerConfig, counts, seed=0, tokens=None, n_micro=1, weights=None, max_tokens=None):
+def run_case(c: synth.LayerConfig, counts, seed=0, tokens=None, n_micro=1, weights=None, max_tokens=None,
+             max_sources=None):
     """Run the CUDA layer and the oracle; returns (layer, srcs, outs, routing, ref)."""
     T = sum(counts)
     srcs = synth.make_sources(c, "cuda", seed=seed, counts=counts)
     w = weights if weights is not None else synth.make_weights(c, "cuda", seed=seed)
-    layer = make_layer(c, w, max_tokens=max_tokens or max(T, 1), max_sources=max(len(counts), 1))
+    layer = make_layer(c, w, max_tokens=max_tokens or max(T, 1),
+                       max_sources=max_sources or max(len(counts), 1))
     outs = layer.forward(srcs, n_micro=n_micro)
     torch.cuda.synchronize()
     layer.check()

@@ -38,6 +38,20 @@ def test_bf16_shapes(shape, counts):
     assert_close(c, out_to_f64(outs), ref_to_f64(c, ref["out"]))
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_largest_router_and_source_table(dtype):
+    """The configuration limits at once: E = 256 experts plus a shared one (257 groups),
+    k = 16 slots, and M = 64 source buffers with empty ones among them; batches on both
+    router paths (small-batch kernel, and the tensor-core estimate with exact candidates)."""
+    c = _small(dtype=dtype, E=256, k=16, H=256, I=128, S=1)
+    rng = np.random.default_rng(3)
+    for counts in ([int(v) for v in rng.integers(0, 3, 64)], [int(v) for v in rng.integers(0, 40, 64)]):
+        layer, srcs, outs, r, ref = run_case(c, counts, max_sources=64)
+        assert_routing_exact(c, r, ref, sum(counts))
+        assert_close(c, out_to_f64(outs), ref_to_f64(c, ref["out"]))
+        layer.close()
+
+
 def test_bf16_zipf_bias_imbalance():
     """Zipf(1.2) log-bias on the logits: a few experts take most tokens."""
     c = _small(E=64, k=8, H=512, I=256, zipf=1.2)
