@@ -15,6 +15,8 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "afd_internal.cuh"
 
 using afd::LayerDims;
@@ -254,24 +256,44 @@ int prof_mark(afd_ffn* h, int i, cudaStream_t s) {
 }
 
 // The launch sequence of one forward on one workspace.
+// NVTX range around the enqueue of one stage (a trace tool maps it onto the stage's
+// kernels; without a tool attached the calls return at once)
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 int run_layer(afd_ffn* h, const SrcTable& st, Workspace& ws, cudaStream_t s) {
   const LayerDims& d = h->dims;
   const int T = st.T;
   ws.last_T = T;
   if (T == 0) return AFD_OK;
+  NvtxRange range_layer("afd.forward");
   int rc;
   afd::TcWeights w{&h->tm_wg, &h->tm_wu, &h->tm_wd, h->sgT, h->suT, h->sdT};
   if ((rc = prof_mark(h, 0, s))) return rc;
-  if (d.dtype == AFD_FP32)
-    CUDA_TRY(h, afd::launch_router(st, h->wrT, h->bias, d, ws, s));
-  else
-    CUDA_TRY(h, afd::launch_router_tc(st, h->wrT, h->bias, h->wnorm, &h->tm_wr, d, ws, h->num_sms, s));
+  {
+    NvtxRange r("afd.router");
+    if (d.dtype == AFD_FP32)
+      CUDA_TRY(h, afd::launch_router(st, h->wrT, h->bias, d, ws, s));
+    else
+      CUDA_TRY(h, afd::launch_router_tc(st, h->wrT, h->bias, h->wnorm, &h->tm_wr, d, ws, h->num_sms, s));
+  }
   if ((rc = prof_mark(h, 1, s))) return rc;
-  CUDA_TRY(h, afd::launch_routing(d, T, ws, s));
+  {
+    NvtxRange r("afd.routing");
+    CUDA_TRY(h, afd::launch_routing(d, T, ws, s));
+  }
   if ((rc = prof_mark(h, 2, s))) return rc;
-  CUDA_TRY(h, afd::launch_pack(st, d, T, ws, h->num_sms, s));
+  {
+    NvtxRange r("afd.pack");
+    CUDA_TRY(h, afd::launch_pack(st, d, T, ws, h->num_sms, s));
+  }
   if ((rc = prof_mark(h, 3, s))) return rc;
   for (int which = 0; which < 2; ++which) {
+    NvtxRange r(which ? "afd.gemm_down" : "afd.gemm_gateup");
     if (d.dtype == AFD_FP32)
       CUDA_TRY(h, afd::launch_gemm_simt(d, T, h->wg32, h->wu32, h->wd32, ws, s, which));
     else if (d.dtype == AFD_FP8_E4M3)
@@ -280,7 +302,10 @@ int run_layer(afd_ffn* h, const SrcTable& st, Workspace& ws, cudaStream_t s) {
       CUDA_TRY(h, afd::launch_gemm_tc(d, T, w, ws, h->num_sms, s, which));
     if ((rc = prof_mark(h, 4 + which, s))) return rc;
   }
-  CUDA_TRY(h, afd::launch_combine(st, d, T, ws, h->num_sms, s));
+  {
+    NvtxRange r("afd.combine");
+    CUDA_TRY(h, afd::launch_combine(st, d, T, ws, h->num_sms, s));
+  }
   return prof_mark(h, 6, s);
 }
 
