@@ -266,6 +266,18 @@ def test_fp8_shapes(shape, counts):
     assert_close(c, out_to_f64(outs), ref_to_f64(c, ref["out"]))
 
 
+@pytest.mark.parametrize("T", [1, 32, 33, 64, 65, 127, 160, 193])
+def test_fp8_tile_fill_at_the_short_tile_bounds(T):
+    """k = E: every expert (and the shared one) gets all T tokens, so the last tile of each
+    group holds T mod 128 rows (128 when that is 0) and crosses the 32- and 64-row bounds
+    between the swapped short-tile MMA and the 128-token one."""
+    c = _small(dtype="fp8", E=8, k=8, H=512, I=256, S=1)
+    layer, srcs, outs, r, ref = run_case(c, [T])
+    assert_routing_exact(c, r, ref, T)
+    assert np.all(r["counts"].cpu().numpy() == T)
+    assert_close(c, out_to_f64(outs), ref_to_f64(c, ref["out"]))
+
+
 def _sampled(c, n_random=12, seed=13):
     T = c.T
     rng = np.random.default_rng(seed)
