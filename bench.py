@@ -302,6 +302,20 @@ def run_ours(args, world, rank, local):
     layer.check()
     ms_step = elapsed / max(args.steps, 1) * 1e3
 
+    # Step-time spread: K more steps with an event between consecutive forwards (the
+    # event keeps the next forward's first kernel from launching during the previous
+    # one's last), for the median and p10 / p90 of single steps.
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    evs[0].record(stream)
+    for i in range(args.steps):
+        step(i)
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per_step = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps))
+
+    def pct(q):
+        return per_step[min(len(per_step) - 1, int(q * (len(per_step) - 1) + 0.5))] if per_step else None
+
     # Per-kernel times (the roofline's kernel): K more steps on one stream with CUDA
     # events recorded around every kernel.  The events serialise the launches, so these
     # steps run slightly slower than the value's.  The library creates the events on
@@ -418,6 +432,8 @@ def run_ours(args, world, rank, local):
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs > L2: expert weights streamed every step; 4 rotating input sets"},
         "tflops": flops / step_s / 1e12,
+        "step_ms": {"p10": pct(0.1), "p50": pct(0.5), "p90": pct(0.9), "n": len(per_step),
+                    "how": "CUDA events between consecutive forwards (separate pass)"},
         "layer_roofline": {"t_roof_ms": t_roof * 1e3, "bound": bound, "frac": t_roof / step_s,
                            "flops": flops, "bytes": lbytes, "touched_experts": touched,
                            "peak_tflops": ptc, "peak_gbs": peaks["hbm_gbs"], "peaks": peak_src},
@@ -441,6 +457,13 @@ def run_ours(args, world, rank, local):
         dt, n, cores, *_ = oracle_sample(cfg, inputs[0], w, n)
         line["cpu_baseline"] = {"value": n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": f"first {n} of {T} tokens, whole layer (routing + experts + combine)"}
+        if T <= 64:  # small batches: the oracle on one core as well
+            import oracle
+
+            oracle.set_num_threads(1)
+            dt1, n1, *_ = oracle_sample(cfg, inputs[0], w, n)
+            oracle.set_num_threads(cores)
+            line["cpu_baseline"]["one_core"] = {"value": n1 / dt1, "unit": "tokens/s", "cores": 1}
     if rank == 0:
         print(json.dumps(line), flush=True)
     layer.close()

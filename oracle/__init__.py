@@ -83,6 +83,8 @@ def lib():
                                              C.c_void_p, C.c_int, C.c_void_p, C.c_int, C.c_void_p,
                                              C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
             L.oracle_num_threads.restype = C.c_int
+            L.oracle_set_num_threads.restype = None
+            L.oracle_set_num_threads.argtypes = [C.c_int]
             _lib = L
     return _lib
 
@@ -97,6 +99,11 @@ def _c(a, dtype):
 
 def num_threads() -> int:
     return lib().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    """Thread count of the oracle's parallel loops (timing only)."""
+    lib().oracle_set_num_threads(int(n))
 
 
 # ---------------------------------------------------------------- formats

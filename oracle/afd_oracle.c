@@ -460,3 +460,13 @@ int oracle_num_threads(void) {
   return 1;
 #endif
 }
+
+/* Threads for the parallel loops that follow (n >= 1); timing only, results do not
+ * depend on it (every parallel loop writes disjoint outputs or sums integers). */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}

@@ -339,6 +339,24 @@ def test_token_order_and_buffer_split_invariance(orc):
     assert np.array_equal(sub["out"], base["out"][[63, 0, 17]])
 
 
+def test_thread_count_does_not_change_results(orc):
+    """The bench times the oracle on one core and on all of them; each parallel loop
+    writes its own tokens' results, so the thread count changes nothing."""
+    c = _tiny(S=1)
+    src = [s.numpy() for s in synth.make_sources(c)]
+    w = synth.weights_numpy(synth.make_weights(c))
+    n = orc.num_threads()
+    try:
+        orc.set_num_threads(1)
+        one = orc.moe_forward(_cfgd(c), src, w)
+    finally:
+        orc.set_num_threads(n)
+    many = orc.moe_forward(_cfgd(c), src, w)
+    for key in ("out", "idx", "w", "logits"):
+        assert np.array_equal(one[key], many[key]), key
+    assert one["fma"] == many["fma"]
+
+
 def test_flop_count(orc):
     for S in (0, 1):
         c = _tiny(S=S)
