@@ -54,24 +54,22 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def recorded_traffic(kernel_file: str):
-    """dram bytes of the gate/up GEMM launch from the committed ncu summary of
-    that kernel, or None when its source changed since the capture."""
+def recorded_traffic(kernel_file: str, cfg):
+    """ncu capture records of the gate/up GEMM launch for the layer's shapes (H, I,
+    dtype), from the committed summaries of that kernel; empty when its source changed
+    since the captures."""
     import hashlib
 
     p = os.path.join(ROOT, "profiles", "traffic.json")
     src = os.path.join(ROOT, "ffn_side_attention_gb300", "csrc", kernel_file)
     if not (os.path.exists(p) and os.path.exists(src)):
-        return None
+        return []
     with open(p) as f:
-        rec = json.load(f).get(kernel_file)
-    if not rec:
-        return None
+        recs = json.load(f).get(kernel_file) or []
     with open(src, "rb") as f:
         h = hashlib.sha256(f.read()).hexdigest()
-    if rec.get("source_sha256") != h:
-        return None
-    return rec
+    return [r for r in recs if r.get("source_sha256") == h and
+            (r.get("H"), r.get("I"), r.get("dtype")) == (cfg.H, cfg.I, cfg.dtype)]
 
 
 def tc_peak(peaks, dtype):
@@ -385,15 +383,18 @@ def run_ours(args, world, rank, local):
     else:
         achieved = gu_bytes / gu_s / 1e9 if gu_s > 0 else None
         rf_peak, rf_unit = peaks["hbm_gbs"], "GB/s"
-    rec = recorded_traffic("gemm_fp8.cu" if cfg.dtype == "fp8" else "gemm_tc.cu")
+    recs = recorded_traffic("gemm_fp8.cu" if cfg.dtype == "fp8" else "gemm_tc.cu", cfg)
+    exact = [r for r in recs if r.get("workload") == cfg.name and r.get("T") == sizes[0]]
+    scaled = [r for r in recs if r.get("dram_bytes_per_touched_expert")]
     traffic = None
     if args.traffic is not None:
         traffic = args.traffic
-    elif rec and rec.get("workload") == cfg.name and rec.get("T") == sizes[0]:
-        traffic = rec.get("dram_bytes_per_launch")
-    elif rec and rec.get("dram_bytes_per_touched_expert"):
-        # capture on a smaller case, scaled by the touched experts (traffic is weight-dominated)
-        traffic = rec["dram_bytes_per_touched_expert"] * (touched_list[0] + cfg.S)
+    elif exact:
+        traffic = exact[0]["dram_bytes_per_launch"]
+    elif scaled:
+        # a capture of the same shapes on fewer experts, scaled by the touched experts
+        # (the bf16 gate/up traffic is weight-dominated)
+        traffic = scaled[0]["dram_bytes_per_touched_expert"] * (touched_list[0] + cfg.S)
 
     # End to end through the host-buffer entry points (pinned memory, two input sets
     # alternating).  Every step copies its sources in and its outputs out inside the
