@@ -272,7 +272,8 @@ class MoELayer:
         return afd_ffn_host_wait(self.handle)
 
     def routing(self, T, stream=None):
-        """Routing tables of the last forward (workspace 0) as int32/fp32 tensors."""
+        """Routing tables of the last forward (of its first micro-batch when it was
+        micro-batched) as int32/fp32 tensors."""
         torch = self.torch
         dev = torch.device("cuda")
         r = {

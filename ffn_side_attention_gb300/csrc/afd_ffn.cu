@@ -49,12 +49,14 @@ struct afd_ffn {
   cudaStream_t mstream[AFD_MAX_MICRO] = {};
   cudaEvent_t ev_fork = nullptr;
   cudaEvent_t ev_join[AFD_MAX_MICRO] = {};
-  // afd_ffn_forward_host_async: copy-in, compute and copy-out streams, two device
-  // staging slots (sources + outputs) and, per slot, the events that order reuse
-  cudaStream_t astream[3] = {};
+  // afd_ffn_forward_host_async: copy-in and copy-out streams, one compute stream per
+  // staging slot (sources + outputs), and per slot the events that order reuse
+  cudaStream_t astream[4] = {};  // copy-in, compute slot 0, copy-out, compute slot 1
   void* astage[2] = {};
   cudaEvent_t ev_in[2] = {}, ev_done[2] = {}, ev_out[2] = {};
   unsigned long long async_calls = 0;
+  int async_last_micro = 1;  // n_micro of the previous asynchronous call
+  int route_ws = 0;          // workspace holding the last forward's routing
   int async_rc = 0;  // first error of an enqueued call, reported by afd_ffn_host_wait
   // per-kernel timing: AFD_NUM_KERNELS + 1 events per recorded forward
   bool prof_on = false;
@@ -442,6 +444,7 @@ int afd_ffn_forward(afd_ffn_t h, void* stream, const void* const* src_ptrs_dev, 
   int rc = validate_batch(h, src_ptrs_dev, src_counts_host, M, out_ptrs_dev, &T);
   if (rc) return rc;
   SrcTable st = make_table(src_ptrs_dev, src_counts_host, M, out_ptrs_dev);
+  h->route_ws = 0;
   return run_layer(h, st, h->ws[0], static_cast<cudaStream_t>(stream));
 }
 
@@ -453,6 +456,7 @@ int afd_ffn_forward_pipelined(afd_ffn_t h, void* stream, int n_micro, const void
   if (n_micro < 1 || n_micro > AFD_MAX_MICRO)
     return fail(h, AFD_EINVAL, "n_micro=%d outside [1, %d]", n_micro, AFD_MAX_MICRO);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  h->route_ws = 0;
   if (!h->ev_fork) CUDA_TRY(h, cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming));
   for (int i = 0; i < n_micro; ++i) {
     if (!h->mstream[i]) CUDA_TRY(h, cudaStreamCreateWithFlags(&h->mstream[i], cudaStreamNonBlocking));
@@ -520,6 +524,7 @@ int afd_ffn_forward_host(afd_ffn_t h, void* stream, int n_micro, const void* con
     if ((rc = afd_ffn_forward_pipelined(h, stream, n_micro, dsrc, src_counts_host, M, dout))) return rc;
   } else {
     SrcTable st = make_table(dsrc, src_counts_host, M, dout);
+    h->route_ws = 0;
     if ((rc = run_layer(h, st, ws, s))) return rc;
   }
   r = 0;
@@ -542,15 +547,21 @@ int afd_ffn_forward_host_async(afd_ffn_t h, int n_micro, const void* const* src_
     return fail(h, AFD_EINVAL, "n_micro=%d outside [1, %d]", n_micro, AFD_MAX_MICRO);
   const size_t rowb = (size_t)h->cfg.H * act_bytes(h->cfg);
   const size_t slot_bytes = 2 * (size_t)h->cfg.max_tokens * rowb;
-  for (int i = 0; i < 3; ++i)
+  for (int i = 0; i < 4; ++i)
     if (!h->astream[i]) CUDA_TRY(h, cudaStreamCreateWithFlags(&h->astream[i], cudaStreamNonBlocking));
   for (int q = 0; q < 2; ++q) {
     if (!h->astage[q] && (rc = dmalloc(h, &h->astage[q], slot_bytes))) return rc;
     for (cudaEvent_t* e : {&h->ev_in[q], &h->ev_done[q], &h->ev_out[q]})
       if (!*e) CUDA_TRY(h, cudaEventCreateWithFlags(e, cudaEventDisableTiming));
   }
-  cudaStream_t cin = h->astream[0], comp = h->astream[1], cout = h->astream[2];
-  const int q = (int)(h->async_calls++ & 1u);
+  const int q = (int)(h->async_calls & 1u);
+  // Single-pass calls alternate between two compute streams and workspaces, so one
+  // batch's router and pack can run while the previous batch's last kernels finish.
+  // A micro-batched call uses workspaces 0..n_micro-1 and follows the other slot's call.
+  cudaStream_t cin = h->astream[0], comp = h->astream[q ? 3 : 1], cout = h->astream[2];
+  Workspace& wsq = h->ws[q];
+  if (n_micro == 1 && (rc = alloc_workspace(h, wsq))) return rc;
+  ++h->async_calls;
   uint8_t* in = static_cast<uint8_t*>(h->astage[q]);
   uint8_t* outb = in + (size_t)h->cfg.max_tokens * rowb;
   const void* dsrc[AFD_MAX_SOURCES];
@@ -570,11 +581,15 @@ int afd_ffn_forward_host_async(afd_ffn_t h, int n_micro, const void* const* src_
   // compute: after this call's copy-in and after the slot's outputs two calls back went out
   CUDA_TRY(h, cudaStreamWaitEvent(comp, h->ev_in[q], 0));
   CUDA_TRY(h, cudaStreamWaitEvent(comp, h->ev_out[q], 0));
+  if (n_micro > 1 || h->async_last_micro > 1)  // workspaces shared with the other slot's call
+    CUDA_TRY(h, cudaStreamWaitEvent(comp, h->ev_done[q ^ 1], 0));
+  h->async_last_micro = n_micro;
   if (n_micro > 1) {
     rc = afd_ffn_forward_pipelined(h, comp, n_micro, dsrc, src_counts_host, M, dout);
   } else {
     SrcTable st = make_table(dsrc, src_counts_host, M, dout);
-    rc = run_layer(h, st, h->ws[0], comp);
+    rc = run_layer(h, st, wsq, comp);
+    h->route_ws = q;
   }
   if (rc) {
     if (!h->async_rc) h->async_rc = rc;
@@ -607,7 +622,7 @@ int afd_ffn_debug_routing(afd_ffn_t h, void* stream, int* topk_idx, float* topk_
                           int* perm_token, int* pos, float* logits) {
   if (!h) return AFD_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const Workspace& ws = h->ws[0];
+  const Workspace& ws = h->ws[h->route_ws];
   const size_t T = ws.last_T, k = h->cfg.k, E = h->cfg.E;
   auto cp = [&](void* dst, const void* src, size_t n) -> cudaError_t {
     if (!dst || n == 0) return cudaSuccess;

@@ -155,16 +155,20 @@ int afd_ffn_forward_host(afd_ffn_t h, void* stream, int n_micro, const void* con
  * with each batch's transfers hidden under another batch's compute (the dual
  * batch overlap of the FastAFD blog, section 4).  Enqueues the host->device
  * copy of the sources, the layer (as afd_ffn_forward_host with the same
- * n_micro) and the device->host copy of the outputs on three library streams
- * (copy-in, compute, copy-out) and returns without waiting.  Consecutive calls
- * alternate between two device staging slots; events order them on the
- * device, so the sources of call i+1 cross the host link while call i
- * computes and call i-1's outputs return.  Calls run in order.  Host buffers
+ * n_micro) and the device->host copy of the outputs on library streams
+ * (copy-in, copy-out, and one compute stream per slot) and returns without
+ * waiting.  Consecutive calls alternate between two device staging slots;
+ * events order them on the device, so the sources of call i+1 cross the host
+ * link while call i computes and call i-1's outputs return.  Single-pass calls
+ * (n_micro == 1) also alternate between two compute streams and workspaces, so
+ * one call's first kernels may run while the previous call's last ones finish;
+ * a micro-batched call waits for the previous call.  Each call's outputs are
+ * those of afd_ffn_forward_host on the same batch.  Host buffers
  * must stay valid until afd_ffn_host_wait returns, and be pinned for the
  * copies to be asynchronous.  While calls are in flight, issue no other
  * forward on this handle.  Argument errors return at once (nothing is
  * enqueued); the staging slots (2 x 2 x max_tokens x H activations) are
- * allocated on first use. */
+ * allocated on first use, and so is a second workspace. */
 int afd_ffn_forward_host_async(afd_ffn_t h, int n_micro, const void* const* src_ptrs_host,
                                const int* src_counts_host, int M, void* const* out_ptrs_host);
 
@@ -173,7 +177,8 @@ int afd_ffn_forward_host_async(afd_ffn_t h, int n_micro, const void* const* src_
  * wait. */
 int afd_ffn_host_wait(afd_ffn_t h);
 
-/* Copy the routing of the last forward (workspace 0) into caller device
+/* Copy the routing of the last forward (for a micro-batched forward, that of
+ * its first micro-batch) into caller device
  * buffers, each may be NULL to skip:
  *   topk_idx [T*k] int32, topk_w [T*k] fp32 (slot order: descending logit,
  *   ties to the lower expert id), counts [E] int32, offsets [E+1] int32

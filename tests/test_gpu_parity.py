@@ -145,10 +145,12 @@ def test_forward_host_equals_device():
         layer.forward_host(hs, ho3, n_micro=0)
 
 
-@pytest.mark.parametrize("n_micro", [1, 3])
+@pytest.mark.parametrize("n_micro", [[1] * 5, [3] * 5, [1, 3, 1, 1, 2]])
 def test_forward_host_async_stream_of_batches(n_micro):
     """Consecutive asynchronous host-buffer calls (staging slots reused every other
-    call, batch sizes changing) give, call by call, the device forward's outputs."""
+    call, single-pass calls alternating compute streams and workspaces, batch sizes
+    and micro-batch counts changing) give, call by call, the device forward's outputs;
+    afterwards the routing read-out is the last call's."""
     c = _small(E=16, k=4, H=256, I=256, S=1)
     w = synth.make_weights(c, "cuda")
     layer = make_layer(c, w, max_tokens=96, max_sources=4)
@@ -160,12 +162,19 @@ def test_forward_host_async_stream_of_batches(n_micro):
         torch.cuda.synchronize()
         hin.append([x.cpu().pin_memory() for x in srcs])
         hout.append([torch.full_like(x, float("nan")).pin_memory() for x in hin[-1]])
+    T_last = sum(batches[-1])
+    r_expect = {k: v.clone() for k, v in layer.routing(T_last).items()}
+    torch.cuda.synchronize()  # the library streams do not wait for torch's stream
     for i in range(len(batches)):
-        layer.forward_host_async(hin[i], hout[i], n_micro=n_micro)
+        layer.forward_host_async(hin[i], hout[i], n_micro=n_micro[i])
     layer.host_wait()
     for i in range(len(batches)):
         for x, y in zip(expect[i], hout[i]):
             assert torch.equal(x, y), f"call {i}"
+    if n_micro[-1] == 1:
+        r = layer.routing(T_last)
+        for k in ("idx", "w", "counts", "offsets", "perm", "pos"):
+            assert torch.equal(r[k], r_expect[k]), k
     with pytest.raises(afd.AfdError):
         layer.forward_host_async(hin[0], hout[0], n_micro=0)
     layer.host_wait()
