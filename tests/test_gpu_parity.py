@@ -29,6 +29,8 @@ def test_tiny_fp32_layer():
     (dict(E=4, k=2, H=512, I=384), [300, 301]),              # experts with > 256 rows: several N tiles
     (dict(E=64, k=8, H=768, I=640, S=1), [5, 3, 0, 9]),      # many experts, few tokens
     (dict(E=8, k=8, H=256, I=128), [33]),                    # k = E: every expert on every token
+    (dict(E=8, k=1), [40, 3]),                               # k = 1: one slot, weight 1
+    (dict(E=1, k=1, S=1), [20]),                             # one routed expert (and the shared one)
 ])
 def test_bf16_shapes(shape, counts):
     c = _small(**shape)
@@ -265,6 +267,7 @@ def test_fp32_router_edges(shape, counts):
     (dict(dtype="fp8", S=1), [17, 0, 40]),
     (dict(dtype="fp8", E=4, k=2, H=512, I=384), [300, 301]),       # > 128 rows per expert: several N tiles
     (dict(dtype="fp8", E=48, k=3, H=768, I=640, S=1), [2, 5]),
+    (dict(dtype="fp8", E=8, k=1), [50]),                          # k = 1
     (dict(dtype="fp8", E=4, k=2, H=7424, I=256), [40]),            # 58 K blocks in gate/up
     (dict(dtype="fp8", E=4, k=2, H=256, I=7296, S=1), [40]),       # 57 K blocks in down
 ])
