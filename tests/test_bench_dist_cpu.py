@@ -58,3 +58,31 @@ def test_single_process_needs_no_process_group():
 
     assert bench.barrier_max(1, 0.5) == 0.5
     assert bench.job_rate(1, 300, 0.1) == pytest.approx(3000)
+
+
+def test_traffic_records_match_source_and_shapes(tmp_path, monkeypatch):
+    """roofline.traffic comes only from an ncu record of the same kernel source (sha256)
+    and the same layer shapes; anything else gives no record (null traffic)."""
+    import hashlib
+    import json
+
+    sys.path.insert(0, ROOT)
+    import bench
+    from ffn_side_attention_gb300 import synth
+
+    src_dir = tmp_path / "ffn_side_attention_gb300" / "csrc"
+    src_dir.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    (src_dir / "gemm_tc.cu").write_bytes(b"kernel v1")
+    sha = hashlib.sha256(b"kernel v1").hexdigest()
+    recs = [dict(source_sha256=sha, H=4096, I=1536, dtype="bf16", workload="a", T=1),
+            dict(source_sha256=sha, H=7168, I=5120, dtype="bf16", workload="b", T=2),
+            dict(source_sha256="0" * 64, H=4096, I=1536, dtype="bf16", workload="c", T=3)]
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"gemm_tc.cu": recs}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    got = bench.recorded_traffic("gemm_tc.cu", synth.CONFIGS["qwen3_bf16"])
+    assert [r["workload"] for r in got] == ["a"]
+    assert [r["workload"] for r in bench.recorded_traffic("gemm_tc.cu", synth.CONFIGS["step3_bf16"])] == ["b"]
+    assert bench.recorded_traffic("gemm_fp8.cu", synth.CONFIGS["qwen3_fp8"]) == []
+    (src_dir / "gemm_tc.cu").write_bytes(b"kernel v2")  # the kernel changed since the capture
+    assert bench.recorded_traffic("gemm_tc.cu", synth.CONFIGS["qwen3_bf16"]) == []
