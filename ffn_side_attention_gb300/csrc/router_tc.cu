@@ -304,6 +304,9 @@ __device__ __forceinline__ void canonical_dot2_xs(const uint4* xs, const uint16_
   const uint4* wa = reinterpret_cast<const uint4*>(w1);
   const uint4* wb = reinterpret_cast<const uint4*>(w2);
   float p1 = 0.0f, p2 = 0.0f;
+  // unrolled so that several chunks' router-row loads are in flight ahead of the
+  // chains; each lane's chain still runs over its chunks in ascending order
+#pragma unroll 8
   for (int c = lane; c < nc; c += 32) {
     const uint4 a = xs[c], b = __ldg(wa + c), d = __ldg(wb + c);
     p1 = chain8(a, b, p1);
@@ -321,6 +324,7 @@ __device__ __forceinline__ float canonical_dot_xs(const uint4* xs, const uint16_
   const int nc = H >> 3;
   const uint4* wa = reinterpret_cast<const uint4*>(w);
   float p = 0.0f;
+#pragma unroll 8
   for (int c = lane; c < nc; c += 32) p = chain8(xs[c], __ldg(wa + c), p);
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) p = p + __shfl_xor_sync(0xffffffffu, p, o);
