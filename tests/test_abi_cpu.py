@@ -84,3 +84,14 @@ def test_null_handle_calls(lib):
     assert L.afd_ffn_check(None, None) == -1
     assert L.afd_ffn_device_bytes(None) == 0
     L.afd_ffn_destroy(None)
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    """No fallback: with the shared library absent the binding raises instead of
+    running anything else."""
+    from ffn_side_attention_gb300 import afd
+
+    monkeypatch.setattr(afd, "_lib", None)
+    monkeypatch.setattr(afd, "LIB_PATH", str(tmp_path / "libafd_ffn.so"))
+    with pytest.raises(RuntimeError, match="is not built"):
+        afd.lib()
