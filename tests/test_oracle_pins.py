@@ -180,6 +180,74 @@ def test_router_planted_logits(orc):
     assert np.allclose(w[1], 1 / 3, atol=1e-7)
 
 
+def test_router_bias_added_last_hand_value(orc):
+    """The bias enters as one fp32 addition after the fold ("MoE 大规模分布式推理工程实战",
+    section 4.1: logits of the linear gate, then + the bias, then top-k).  Hand value:
+    lane 0 holds 1 (channel 0), lanes 8 and 24 hold 2^-24 (channels 64 and 192); the fold
+    gives s = 1 + 2^-23 (level 16: 2^-24 + 2^-24 = 2^-23 exactly; level 8: 1 + 2^-23).
+    With bias 2^-24, s + b = 1 + 3*2^-24 lies half-way between 1 + 2^-23 (odd mantissa) and
+    1 + 2^-22 (even), so the logit is 1 + 2^-22.  Each wrong placement gives another value:
+    no bias 1 + 2^-23; bias subtracted: 1 + 2^-24 ties to 1; bias added to lane 0 before
+    the fold: 1 + 2^-24 ties to 1 there, and the fold then gives 1 + 2^-23."""
+    H = 256
+    x = np.zeros((1, H), np.float32)
+    x[0, 0], x[0, 64], x[0, 192] = 1.0, 2.0 ** -24, 2.0 ** -24
+    w = np.ones((H, 1), np.float32)
+    got = float(orc.router_logits(x, w, "fp32", np.array([2.0 ** -24], np.float32))[0, 0])
+    assert got == 1.0 + 2.0 ** -22
+    assert float(orc.router_logits(x, w, "fp32")[0, 0]) == 1.0 + 2.0 ** -23
+    # bf16 activations take the same route: all values above are bf16-exact
+    xb = orc.bf16_bits(x)
+    wb = orc.bf16_bits(w)
+    assert float(orc.router_logits(xb, wb, "bf16", np.array([2.0 ** -24], np.float32))[0, 0]) == 1.0 + 2.0 ** -22
+
+
+def test_router_bias_reorders_planted_topk(orc):
+    """One-hot router columns plant logits c_e * x[e] (exact); a bias then moves experts
+    in and out of the top-k.  Expected sets by hand: logits 1..8 plus bias
+    (+10, 0, 0, 0, 0, -0.5, 0, -10) = (11, 2, 3, 4, 5, 5.5, 7, -2) -> top-3 = 0, 6, 5;
+    without the bias (or with it subtracted) the top-3 would be 7, 6, 5.  A bias that
+    makes two logits equal sends the tie to the lower id: (1..8) + (0, 0, 0, 0, 0, 0, 1, 0)
+    = (..., 6, 8, 8) -> 6, 7, 5.  Weights are the softmax of the biased selected logits."""
+    H, E, k = 16, 8, 3
+    Wr = np.zeros((H, E), np.float32)
+    for e in range(E):
+        Wr[e, e] = float(e + 1)
+    x = np.zeros((2, H), np.float32)
+    x[:, :E] = 1.0
+    b1 = np.array([10, 0, 0, 0, 0, -0.5, 0, -10], np.float32)
+    idx, w = orc.topk(orc.router_logits(x, Wr, "fp32", b1), k)
+    assert idx.tolist() == [[0, 6, 5]] * 2
+    sel = np.array([11.0, 7.0, 5.5])
+    p = np.exp(sel - sel.max())
+    assert np.allclose(w[0], p / p.sum(), rtol=1e-6, atol=0)
+    b2 = np.array([0, 0, 0, 0, 0, 0, 1, 0], np.float32)
+    idx2, w2 = orc.topk(orc.router_logits(x, Wr, "fp32", b2), k)
+    assert idx2.tolist() == [[6, 7, 5]] * 2
+    p2 = np.exp(np.array([8.0, 8.0, 6.0]) - 8.0)
+    assert np.allclose(w2[0], p2 / p2.sum(), rtol=1e-6, atol=0)
+
+
+def test_router_bias_k_equals_E_is_softmax_of_biased_logits(orc):
+    """k = E with a Zipf(1.2) log-bias: the weights are the full softmax of (x W + b),
+    computed here in float64 from the matrix product (closed form), and the slots are the
+    experts in descending biased-logit order.  The bias is ~ -6.7 .. 0, far above the
+    canonical sum's rounding, so dropping or flipping it fails by orders of magnitude."""
+    from scipy.special import softmax
+
+    T, H, E = 40, 256, 16
+    rng = np.random.default_rng(21)
+    x = _bf16_vals(rng, (T, H))
+    Wr = _bf16_vals(rng, (H, E), 1 / math.sqrt(H))
+    b = synth.zipf_bias(E, 1.2).numpy()
+    idx, w = orc.topk(orc.router_logits(orc.bf16_bits(x), orc.bf16_bits(Wr), "bf16", b), E)
+    z = x.astype(np.float64) @ Wr.astype(np.float64) + b.astype(np.float64)
+    p = softmax(z, axis=1)
+    for t in range(T):
+        assert idx[t].tolist() == sorted(range(E), key=lambda e: (-z[t, e], e))
+        assert np.allclose(w[t], p[t, idx[t]], rtol=1e-5, atol=1e-7)
+
+
 def test_topk_brute_force(orc):
     rng = np.random.default_rng(4)
     T, E, k = 300, 40, 6
@@ -307,6 +375,25 @@ def test_k_equals_E_is_full_softmax_mixture(orc):
     ref = sum(p[:, e:e + 1] * _np_swiglu(x, w["w_gate"][e].astype(np.float64), w["w_up"][e].astype(np.float64),
                                          w["w_down"][e].astype(np.float64)) for e in range(c.E))
     assert np.linalg.norm(r["out"] - ref) / np.linalg.norm(ref) < 1e-5
+
+
+def test_k_equals_E_with_bias_is_biased_softmax_mixture(orc):
+    """The layer passes the router bias through to routing: with k = E and a bias, the
+    output is the mixture weighted by softmax(x W_r + b) (closed form in float64)."""
+    from scipy.special import softmax
+
+    c = _tiny(E=4, k=4)
+    src = [s.numpy() for s in synth.make_sources(c)]
+    w = synth.weights_numpy(synth.make_weights(c))
+    w["router_bias"] = np.array([1.5, -2.0, 0.25, 0.0], np.float32)
+    r = orc.moe_forward(_cfgd(c), src, w)
+    x = np.concatenate(src).astype(np.float64)
+    p = softmax(x @ w["w_router"].astype(np.float64) + w["router_bias"].astype(np.float64), axis=1)
+    ref = sum(p[:, e:e + 1] * _np_swiglu(x, w["w_gate"][e].astype(np.float64), w["w_up"][e].astype(np.float64),
+                                         w["w_down"][e].astype(np.float64)) for e in range(c.E))
+    assert np.linalg.norm(r["out"] - ref) / np.linalg.norm(ref) < 1e-5
+    no_bias = orc.moe_forward(_cfgd(c), src, {k_: v for k_, v in w.items() if k_ != "router_bias"})
+    assert np.linalg.norm(no_bias["out"] - ref) / np.linalg.norm(ref) > 1e-2
 
 
 def test_shared_expert_adds_unweighted(orc):
