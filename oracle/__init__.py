@@ -82,6 +82,9 @@ def lib():
             L.oracle_moe_forward.argtypes = [C.POINTER(_Cfg), C.POINTER(_Weights), C.c_void_p,
                                              C.c_void_p, C.c_int, C.c_void_p, C.c_int, C.c_void_p,
                                              C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
+            L.oracle_expert_hidden.restype = C.c_int
+            L.oracle_expert_hidden.argtypes = [C.POINTER(_Cfg), C.POINTER(_Weights), C.c_void_p, C.c_void_p,
+                                               C.c_int, C.c_void_p]
             L.oracle_num_threads.restype = C.c_int
             L.oracle_set_num_threads.restype = None
             L.oracle_set_num_threads.argtypes = [C.c_int]
@@ -233,3 +236,24 @@ def moe_forward(cfg: dict, srcs: list, weights: dict, tokens=None):
     if rc != 0:
         raise ValueError("oracle_moe_forward rejected its arguments")
     return {"out": out, "idx": idx, "w": w, "logits": logits, "fma": int(fma.value)}
+
+
+def expert_hidden(cfg: dict, weights: dict, x, experts) -> np.ndarray:
+    """fp32 SwiGLU hidden rows silu(a Wg) * (a Wu) of (token row, expert) pairs, before
+    the down projection's operand rounding (bf16) or quantisation (fp8).
+
+    x: [n, H] token rows (fp32, or bf16 bits for the bf16/fp8 layers); experts: [n]
+    expert ids, -1 for the shared expert.  Returns [n, I] fp32."""
+    dtype = cfg["dtype"]
+    H, I = cfg["H"], cfg["I"]
+    c = _Cfg(H, I, cfg["E"], cfg["k"], int(cfg.get("S", 0)), DTYPES[dtype])
+    keep = {key: _np_weight(key, weights.get(key), dtype) for key in _WKEYS}
+    wst = _Weights(*[_p(keep[key]) for key in _WKEYS])
+    x = _c(x, np.float32 if dtype == "fp32" else np.uint16).reshape(-1, H)
+    ex = _c(experts, np.int32).reshape(-1)
+    if ex.shape[0] != x.shape[0]:
+        raise ValueError("one expert id per token row")
+    out = np.zeros((x.shape[0], I), np.float32)
+    if lib().oracle_expert_hidden(C.byref(c), C.byref(wst), _p(x), _p(ex), x.shape[0], _p(out)) != 0:
+        raise ValueError("oracle_expert_hidden rejected an expert id")
+    return out

@@ -319,17 +319,14 @@ static void operand_row(const float* v, int n, int dtype, double* out, const dou
   }
 }
 
-/* y[H] = SwiGLU expert applied to one operand row a[H] (double).  Returns the
- * number of multiply-adds performed (3*H*I). */
-static long long expert_ffn(const oracle_cfg* cfg, const void* wg, const void* wu, const void* wd,
-                            const float* sg, const float* su, const float* sd, int e, const double* a,
-                            double* y, const double* e4m3_table) {
+/* First half of one SwiGLU expert on an operand row a[H] (double):
+ * G = a Wg, U = a Wu accumulated in double, hf[i] = silu(G_i) * U_i rounded
+ * once to fp32 -- the value the down projection's operand is made from. */
+static void expert_hidden(const oracle_cfg* cfg, const void* wg, const void* wu, const float* sg,
+                          const float* su, int e, const double* a, float* hf, const double* e4m3_table) {
   int H = cfg->H, I = cfg->I;
-  long long fmas = 0;
   double* G = (double*)calloc((size_t)I, sizeof(double));
   double* U = (double*)calloc((size_t)I, sizeof(double));
-  float* hf = (float*)malloc(sizeof(float) * (size_t)I);
-  double* hd = (double*)malloc(sizeof(double) * (size_t)I);
   long gbase = (long)e * H * I;
   for (int h = 0; h < H; ++h) {
     double ah = a[h];
@@ -338,12 +335,26 @@ static long long expert_ffn(const oracle_cfg* cfg, const void* wg, const void* w
       U[i] += ah * weight_at(wu, su, cfg->dtype, gbase, H, I, h, i, e4m3_table);
     }
   }
-  fmas += 2LL * H * I;
   for (int i = 0; i < I; ++i) {
     double g = G[i];
     double silu = g / (1.0 + exp(-g));
     hf[i] = (float)(silu * U[i]);
   }
+  free(G);
+  free(U);
+}
+
+/* y[H] = SwiGLU expert applied to one operand row a[H] (double).  Returns the
+ * number of multiply-adds performed (3*H*I). */
+static long long expert_ffn(const oracle_cfg* cfg, const void* wg, const void* wu, const void* wd,
+                            const float* sg, const float* su, const float* sd, int e, const double* a,
+                            double* y, const double* e4m3_table) {
+  int H = cfg->H, I = cfg->I;
+  long long fmas = 0;
+  float* hf = (float*)malloc(sizeof(float) * (size_t)I);
+  double* hd = (double*)malloc(sizeof(double) * (size_t)I);
+  expert_hidden(cfg, wg, wu, sg, su, e, a, hf, e4m3_table);
+  fmas += 2LL * H * I;
   operand_row(hf, I, cfg->dtype, hd, e4m3_table);
   for (int c = 0; c < H; ++c) y[c] = 0.0;
   long dbase = (long)e * I * H;
@@ -352,11 +363,47 @@ static long long expert_ffn(const oracle_cfg* cfg, const void* wg, const void* w
     for (int c = 0; c < H; ++c) y[c] += hi * weight_at(wd, sd, cfg->dtype, dbase, I, H, i, c, e4m3_table);
   }
   fmas += (long long)I * H;
-  free(G);
-  free(U);
   free(hf);
   free(hd);
   return fmas;
+}
+
+/* The fp32 SwiGLU hidden rows (before the down projection's rounding or
+ * quantisation) of n (token, expert) pairs, for tests that compare the
+ * layer's intermediate operand.
+ *   x      : [n, H] token rows in the activation dtype (fp32 values, or bf16
+ *            bits for the bf16/fp8 layers)
+ *   expert : [n] expert ids; -1 selects the shared expert
+ *   hf     : [n, I] fp32 output
+ * The activation operand is formed as in the full layer (bf16 values, or the
+ * per-128-channel e4m3 quantisation for the fp8 layer).  Returns 0, or -1 on
+ * a bad expert id. */
+int oracle_expert_hidden(const oracle_cfg* cfg, const oracle_weights* w, const void* x, const int32_t* expert,
+                         int n, float* hf) {
+  int H = cfg->H, I = cfg->I;
+  int act_dtype = cfg->dtype == ORC_FP32 ? ORC_FP32 : ORC_BF16;
+  double e4m3_table[256];
+  for (int c = 0; c < 256; ++c) e4m3_table[c] = oracle_e4m3_decode((uint8_t)c);
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int i = 0; i < n; ++i) {
+    int e = expert[i];
+    if (e < -1 || e >= cfg->E || (e == -1 && !cfg->n_shared)) {
+      bad = 1;
+      continue;
+    }
+    float* xf = (float*)malloc(sizeof(float) * H);
+    double* a = (double*)malloc(sizeof(double) * H);
+    for (int h = 0; h < H; ++h) xf[h] = load_act(x, act_dtype, (long)i * H + h);
+    operand_row(xf, H, cfg->dtype, a, e4m3_table);
+    if (e < 0)
+      expert_hidden(cfg, w->sh_gate, w->sh_up, w->sh_s_gate, w->sh_s_up, 0, a, hf + (size_t)i * I, e4m3_table);
+    else
+      expert_hidden(cfg, w->w_gate, w->w_up, w->s_gate, w->s_up, e, a, hf + (size_t)i * I, e4m3_table);
+    free(xf);
+    free(a);
+  }
+  return bad ? -1 : 0;
 }
 
 /*

@@ -524,3 +524,48 @@ def test_fp8_layer_matches_float64_reference(orc):
             ref[t] += wj * (h @ wd)
     got = f(r["out"]).astype(np.float64)
     assert np.linalg.norm(got - ref) / np.linalg.norm(ref) < 4e-3
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp8"])
+def test_expert_hidden_matches_float64_swiglu(orc, dtype):
+    """The hidden-row export (silu(a Wg) * (a Wu) rounded once to fp32, per (token,
+    expert)) against a float64 numpy evaluation: a = the token in the layer's operand
+    format (fp32 / bf16 values / torch's e4m3 cast per 128 channels), weights dequantised
+    block-wise for fp8.  The two sums differ only in float64 rounding order, so after the
+    fp32 rounding they agree to one fp32 ulp.  The shared expert is selected by id -1."""
+    c = _tiny(dtype=dtype, H=256, I=256, E=4, k=2, S=1)
+    src = synth.make_sources(c)
+    x = np.concatenate([synth.to_numpy_bits(s) for s in src])[:24]
+    w = synth.weights_numpy(synth.make_weights(c))
+    experts = np.array([t % c.E for t in range(23)] + [-1], np.int32)
+    got = orc.expert_hidden(_cfgd(c), w, x, experts)
+    xf = x.astype(np.float32) if dtype == "fp32" else orc.bf16_to_f32(x)
+
+    def wmat(key, e):
+        if dtype == "fp32":
+            return w[key][e].astype(np.float64) if e >= 0 else w["sh_" + key[2:]].astype(np.float64)
+        q = w[key][e] if e >= 0 else w["sh_" + key[2:]]
+        if dtype == "bf16":
+            return orc.bf16_to_f32(q).astype(np.float64)
+        s = w["s_" + key[2:]][e] if e >= 0 else w["sh_s_" + key[2:]]
+        v = torch.from_numpy(q.copy()).view(torch.float8_e4m3fn).double().numpy()
+        return v * np.kron(s.astype(np.float64), np.ones((128, 128)))
+
+    def operand(row):
+        if dtype != "fp8":
+            return row.astype(np.float64)
+        out = np.zeros(row.shape, np.float64)
+        for b in range(0, row.shape[0], 128):
+            blk = row[b:b + 128].astype(np.float32)
+            sc = np.float32(np.abs(blk).max()) / np.float32(448)
+            out[b:b + 128] = torch.from_numpy(blk / sc).to(torch.float8_e4m3fn).double().numpy() * float(sc)
+        return out
+
+    for i, e in enumerate(experts):
+        a = operand(xf[i])
+        g = a @ wmat("w_gate", e)
+        ref = (g / (1 + np.exp(-g)) * (a @ wmat("w_up", e))).astype(np.float32)
+        ulp = np.spacing(np.abs(ref)).astype(np.float64)
+        assert np.all(np.abs(got[i].astype(np.float64) - ref) <= ulp), f"row {i} expert {e}"
+    with pytest.raises(ValueError):
+        orc.expert_hidden(_cfgd(c), w, x[:1], np.array([c.E], np.int32))
