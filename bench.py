@@ -202,6 +202,168 @@ def default_sample_tokens(cfg):
     return max(8, min(cfg.T, int(16 * 12 * 0.75e9 / per_tok)))
 
 
+# ------------------------------------------------------------------ roofline of one workload
+def routing_roofline(layer, cfg, xall, n_mb, stream, peaks):
+    """Touched experts per micro-batch (from one forward of each micro-batch's tokens) and
+    the layer roofline summed over micro-batches: each micro-batch is its own forward and
+    streams its own experts' weights."""
+    T = xall.shape[0]
+    ptc = tc_peak(peaks, cfg.dtype)
+    q, rem = divmod(T, n_mb)
+    sizes = [q + (1 if i < rem else 0) for i in range(n_mb)]
+    flops = lbytes = t_roof = 0.0
+    touched_list = []
+    bound = "hbm"
+    t0_ = 0
+    for sz in sizes:
+        sub = [xall[t0_:t0_ + sz]]
+        layer.forward(sub, [torch.empty_like(sub[0])], stream=stream)
+        r = layer.routing(sz)
+        tch = int((r["counts"].cpu() > 0).sum().item())
+        touched_list.append(tch)
+        f_i = roofline.layer_flops(cfg, sz)
+        b_i = roofline.layer_bytes(cfg, sz, tch)
+        tr_i, bound = roofline.t_roof(f_i, b_i, ptc, peaks["hbm_gbs"])
+        flops += f_i
+        lbytes += b_i
+        t_roof += tr_i
+        t0_ += sz
+    return dict(sizes=sizes, touched=touched_list, flops=flops, bytes=lbytes, t_roof=t_roof, bound=bound, ptc=ptc)
+
+
+def gemm_roofline(cfg, size0, touched0, k_avg, peaks):
+    """Roofline of the two GEMM launches of one (micro-)batch against their profiled times."""
+    ptc = tc_peak(peaks, cfg.dtype)
+    gu_bytes = roofline.gateup_bytes(cfg, size0, touched0)
+    dn_bytes = roofline.down_bytes(cfg, size0, touched0)
+    t_gemm = (k_avg["gemm_gateup"] + k_avg["gemm_down"]) / 1e3
+    t_r, _ = roofline.t_roof(roofline.layer_flops(cfg, size0), gu_bytes + dn_bytes, ptc, peaks["hbm_gbs"])
+    return dict(t_roof_ms=t_r * 1e3, t_ms=t_gemm * 1e3, frac=t_r / t_gemm if t_gemm > 0 else None), gu_bytes, dn_bytes
+
+
+def profile_kernels(layer, fwd, n):
+    """Average per-kernel milliseconds over n forwards run by fwd(i) with CUDA events around
+    each kernel (an untimed pass first creates the library's events)."""
+    layer.profile_begin()
+    for i in range(n):
+        fwd(i)
+    layer.profile_end()
+    torch.cuda.synchronize()
+    layer.profile_begin()
+    for i in range(n):
+        fwd(i)
+    kms, nf = layer.profile_end()
+    return {k: v / max(nf, 1) for k, v in kms.items()}
+
+
+# ------------------------------------------------------------------ per-batch sweep
+# Every decode batch of the workloads, one entry each: the Qwen3 bf16 layer at
+# B in {6, 48, 197, 395} x M in {1, 4, 8}, its fp8 variant at 4 x 395, the
+# DeepSeek-V3 fp8 layer at T in {512, 2048, 4096}, the Step3 layer as three
+# micro-batches of 8 x 256, and the tiny fp32 layer.
+def sweep_points():
+    pts = [("qwen3_bf16", b, m, 1) for (b, m) in synth.CONFIGS["qwen3_bf16"].batches]
+    pts.append(("qwen3_fp8", 395, 4, 1))
+    pts += [("dsv3_fp8", b, m, 1) for (b, m) in synth.CONFIGS["dsv3_fp8"].batches]
+    pts.append(("step3_bf16", 256, 8, 3))
+    pts.append(("tiny_fp32", 32, 2, 1))
+    return pts
+
+
+def measure_point(layer, cfg, n_micro, peaks, stream, local, min_s=0.3):
+    """One per-batch entry: tokens/s over a timed run of at least min_s seconds (CUDA
+    events on the launching stream, clocks sampled during it), the layer and GEMM
+    rooflines and the per-kernel split."""
+    T = cfg.T
+    inputs = [synth.make_sources(cfg, "cuda", seed=s) for s in range(4)]
+    outs = [[torch.empty_like(x) for x in srcs] for srcs in inputs]
+
+    def step(i):
+        layer.forward(inputs[i % 4], outs[i % 4], stream=stream, n_micro=n_micro)
+
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(5):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    est = max(e0.elapsed_time(e1) / 5e3, 1e-6)
+    steps = int(min(2000, max(20, min_s / est)))
+    sampler = ClockSampler(local)
+    time.sleep(0.2)
+    t_spin = time.perf_counter()
+    i = 0
+    while time.perf_counter() - t_spin < 0.15:
+        step(i)
+        i += 1
+        if i % 16 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    layer.check()
+    ms = e0.elapsed_time(e1) / steps
+    xall = torch.cat(inputs[0])
+    rl = routing_roofline(layer, cfg, xall, n_micro, stream, peaks)
+    size0 = rl["sizes"][0]
+    prof_in = [xall[:size0]]
+    prof_out = [torch.empty_like(prof_in[0])]
+    if n_micro == 1:
+        k_avg = profile_kernels(layer, step, min(steps, 30))
+    else:
+        k_avg = profile_kernels(layer, lambda i: layer.forward(prof_in, prof_out, stream=stream), min(steps, 30))
+    gr, _, _ = gemm_roofline(cfg, size0, rl["touched"][0], k_avg, peaks)
+    return {
+        "workload": f"{cfg.name} B={cfg.B} M={cfg.M} T={T}" + (f" n_micro={n_micro}" if n_micro > 1 else ""),
+        "T": T, "n_micro": n_micro, "steps": steps, "ms_per_step": ms, "value": T / (ms / 1e3),
+        "unit": "tokens/s", "tflops": rl["flops"] / (ms / 1e3) / 1e12,
+        "layer_roofline": {"t_roof_ms": rl["t_roof"] * 1e3, "bound": rl["bound"], "frac": rl["t_roof"] / (ms / 1e3),
+                           "touched_experts": rl["touched"][0] if n_micro == 1 else rl["touched"]},
+        "gemm_roofline": gr,
+        "kernel_ms": k_avg,
+        "gpu_launches_per_step": sum(layer.launches_per_forward(sz) for sz in rl["sizes"]),
+        "clocks": clocks,
+    }
+
+
+def per_batch_sweep(peaks, stream, local, reuse=None):
+    """All sweep points, grouped by layer so each layer's weights are made once.  `reuse`
+    = (cfg, layer) of a layer already built for the largest batch of its workload."""
+    from ffn_side_attention_gb300 import afd
+
+    entries = []
+    by_name = {}
+    for name, b, m, nm in sweep_points():
+        by_name.setdefault(name, []).append((b, m, nm))
+    for name, pts in by_name.items():
+        base = synth.CONFIGS[name]
+        max_t = max(b * m for b, m, _ in pts)
+        max_m = max(m for _, m, _ in pts)
+        if reuse is not None and reuse[0].name == name and reuse[0].T >= max_t and reuse[0].M >= max_m:
+            layer, own = reuse[1], False
+        else:
+            w = synth.make_weights(base, "cuda")
+            layer = afd.MoELayer(base.H, base.I, base.E, base.k, base.dtype, w, n_shared=base.S, max_tokens=max_t,
+                                 max_sources=max_m)
+            del w
+            torch.cuda.empty_cache()
+            own = True
+        for b, m, nm in pts:
+            entries.append(measure_point(layer, base.with_batch(b, m), nm, peaks, stream, local))
+        if own:
+            layer.close()
+            del layer
+            torch.cuda.empty_cache()
+    return entries
+
+
 # ------------------------------------------------------------------ main legs
 def run_reference(args, world, rank):
     if rank != 0:
@@ -320,40 +482,14 @@ def run_ours(args, world, rank, local):
     # first use, so an untimed pass creates them first.
     prof_timed = n_mb == 1
     if prof_timed:
-        layer.profile_begin()
-        for i in range(args.steps):
-            step(i)
-        layer.profile_end()
-        torch.cuda.synchronize()
-        layer.profile_begin()
-        for i in range(args.steps):
-            step(i)
-        kms, nf = layer.profile_end()
-
+        k_avg = profile_kernels(layer, step, args.steps)
 
     # routing statistics of input set 0 (touched experts), per micro-batch:
     # each micro-batch is its own forward and streams its own experts' weights
-    ptc = tc_peak(peaks, cfg.dtype)
-    q, rem = divmod(T, n_mb)
-    sizes = [q + (1 if i < rem else 0) for i in range(n_mb)]
     xall = torch.cat(inputs[0])
-    flops = lbytes = t_roof = 0.0
-    touched_list = []
-    bound = "hbm"
-    t0_ = 0
-    for sz in sizes:
-        sub = [xall[t0_:t0_ + sz]]
-        layer.forward(sub, [torch.empty_like(sub[0])], stream=stream)
-        r = layer.routing(sz)
-        tch = int((r["counts"].cpu() > 0).sum().item())
-        touched_list.append(tch)
-        f_i = roofline.layer_flops(cfg, sz)
-        b_i = roofline.layer_bytes(cfg, sz, tch)
-        tr_i, bound = roofline.t_roof(f_i, b_i, ptc, peaks["hbm_gbs"])
-        flops += f_i
-        lbytes += b_i
-        t_roof += tr_i
-        t0_ += sz
+    rl = routing_roofline(layer, cfg, xall, n_mb, stream, peaks)
+    sizes, touched_list = rl["sizes"], rl["touched"]
+    flops, lbytes, t_roof, bound, ptc = rl["flops"], rl["bytes"], rl["t_roof"], rl["bound"], rl["ptc"]
     touched = touched_list[0] if n_mb == 1 else touched_list
 
     # with micro-batches (three streams), per-kernel times come from a separate
@@ -361,18 +497,12 @@ def run_ours(args, world, rank, local):
     if not prof_timed:
         prof_in = [xall[:sizes[0]]]
         prof_out = [torch.empty_like(prof_in[0])]
-        layer.profile_begin()
-        for i in range(min(args.steps, 50)):
-            layer.forward(prof_in, prof_out, stream=stream)
-        kms, nf = layer.profile_end()
-    k_avg = {k: v / max(nf, 1) for k, v in kms.items()}
+        k_avg = profile_kernels(layer, lambda i: layer.forward(prof_in, prof_out, stream=stream),
+                                min(args.steps, 50))
     step_s = ms_step / 1e3
-    gu_bytes = roofline.gateup_bytes(cfg, sizes[0], touched_list[0])  # the profiled launch
+    gr, gu_bytes, dn_bytes = gemm_roofline(cfg, sizes[0], touched_list[0], k_avg, peaks)
     gu_s = k_avg["gemm_gateup"] / 1e3
-    dn_bytes = roofline.down_bytes(cfg, sizes[0], touched_list[0])
     dn_s = k_avg["gemm_down"] / 1e3
-    gemm_roof, _ = roofline.t_roof(roofline.layer_flops(cfg, sizes[0]), gu_bytes + dn_bytes, ptc,
-                                   peaks["hbm_gbs"])
     # the gate/up launch's own bound: tensor if its FLOPs at the dense tensor
     # peak take longer than its algorithmic bytes at the HBM peak
     gu_flops = roofline.gateup_flops(cfg, sizes[0])
@@ -438,8 +568,7 @@ def run_ours(args, world, rank, local):
         "layer_roofline": {"t_roof_ms": t_roof * 1e3, "bound": bound, "frac": t_roof / step_s,
                            "flops": flops, "bytes": lbytes, "touched_experts": touched,
                            "peak_tflops": ptc, "peak_gbs": peaks["hbm_gbs"], "peaks": peak_src},
-        "gemm_roofline": {"t_roof_ms": gemm_roof * 1e3, "t_ms": (gu_s + dn_s) * 1e3,
-                          "frac": gemm_roof / (gu_s + dn_s) if gu_s + dn_s > 0 else None},
+        "gemm_roofline": gr,
         "roofline": {"kernel": "gemm_gateup", "bound": "tensor" if gu_tensor else "hbm", "achieved": achieved,
                      "peak": rf_peak, "unit": rf_unit, "frac": achieved / rf_peak if achieved else None,
                      "traffic": traffic, "peak_src": peak_src},
@@ -453,8 +582,17 @@ def run_ours(args, world, rank, local):
         "gpu_launches": args.steps * sum(layer.launches_per_forward(sz) for sz in sizes),
         "clocks": clocks,
     }
+    if world == 1 and not args.no_per_batch:
+        # the per-batch roofline sweep (one GPU: the metric is per GB300); the headline's
+        # layer serves the workload it was built for
+        del w
+        torch.cuda.empty_cache()
+        line["per_batch"] = per_batch_sweep(peaks, stream, local, reuse=(cfg, layer) if n_mb == 1 else None)
+        w = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n = args.cpu_sample or default_sample_tokens(cfg)
+        if w is None:
+            w = synth.make_weights(cfg, "cuda")
         dt, n, cores, *_ = oracle_sample(cfg, inputs[0], w, n)
         line["cpu_baseline"] = {"value": n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": f"first {n} of {T} tokens, whole layer (routing + experts + combine)"}
@@ -484,6 +622,8 @@ def main():
     ap.add_argument("--I", type=int, default=None, help="override the expert intermediate size (profiling cases)")
     ap.add_argument("--cpu-sample", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-batch", action="store_true",
+                    help="skip the per-batch roofline sweep over every workload's decode batches")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per gate/up launch, when taken for the current kernel")
     args = ap.parse_args()
@@ -498,6 +638,10 @@ def main():
     args.M = args.M if args.M is not None else base.M
     args.n_micro = args.n_micro if args.n_micro is not None else base.n_micro
     args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus != world:
+        sys.exit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}; launch N > 1 ranks with "
+                 f"torchrun --nproc-per-node N")
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, world, rank)

@@ -25,7 +25,7 @@ KERNEL_NAMES = ["router", "routing", "pack", "gemm_gateup", "gemm_down", "combin
 
 EXPORTS = ["afd_ffn_create", "afd_ffn_create_error", "afd_ffn_forward", "afd_ffn_forward_pipelined",
            "afd_ffn_forward_host", "afd_ffn_forward_host_async", "afd_ffn_host_wait", "afd_ffn_debug_routing",
-           "afd_ffn_debug_inject", "afd_ffn_check", "afd_ffn_last_error",
+           "afd_ffn_debug_operands", "afd_ffn_debug_inject", "afd_ffn_check", "afd_ffn_last_error",
            "afd_ffn_profile_begin", "afd_ffn_profile_end", "afd_ffn_launches_per_forward",
            "afd_ffn_device_bytes", "afd_ffn_router_noalloc", "afd_ffn_destroy"]
 
@@ -75,6 +75,8 @@ def lib():
         L.afd_ffn_debug_inject.restype = ip
         L.afd_ffn_debug_routing.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.afd_ffn_debug_routing.restype = ip
+        L.afd_ffn_debug_operands.argtypes = [vp, vp, vp, vp, vp, vp]
+        L.afd_ffn_debug_operands.restype = ip
         L.afd_ffn_check.argtypes = [vp, vp]
         L.afd_ffn_check.restype = ip
         L.afd_ffn_last_error.argtypes = [vp]
@@ -150,6 +152,10 @@ def afd_ffn_debug_inject(h, stream, kind, arg):
 def afd_ffn_debug_routing(h, stream, topk_idx, topk_w, counts, offsets, perm_token, pos, logits):
     return _check(lib().afd_ffn_debug_routing(h, stream, topk_idx, topk_w, counts, offsets, perm_token, pos,
                                               logits), h)
+
+
+def afd_ffn_debug_operands(h, stream, P, P_scale, Hmid, H_scale):
+    return _check(lib().afd_ffn_debug_operands(h, stream, P, P_scale, Hmid, H_scale), h)
 
 
 def afd_ffn_check(h, stream):
@@ -288,6 +294,24 @@ class MoELayer:
         afd_ffn_debug_routing(self.handle, self._stream(stream), *[r[k].data_ptr() for k in
                                                                    ("idx", "w", "counts", "offsets", "perm", "pos",
                                                                     "logits")])
+        return r
+
+    def operands(self, T, stream=None):
+        """Expert-GEMM operands of the last forward (of its first micro-batch when it was
+        micro-batched): packed token rows P [R, H] and SwiGLU rows h [R, I], R = T*(k+S),
+        in the layer's operand format (uint8 e4m3 codes for fp8, with scales
+        [H/128, R] and [I/128, R])."""
+        torch = self.torch
+        dev = torch.device("cuda")
+        R = T * (self.k + self.S)
+        et = {"fp32": torch.float32, "bf16": torch.bfloat16, "fp8": torch.uint8}[self.dtype]
+        r = {"P": torch.empty(R, self.H, dtype=et, device=dev), "h": torch.empty(R, self.I, dtype=et, device=dev)}
+        if self.dtype == "fp8":
+            r["P_scale"] = torch.empty(self.H // 128, R, dtype=torch.float32, device=dev)
+            r["h_scale"] = torch.empty(self.I // 128, R, dtype=torch.float32, device=dev)
+        afd_ffn_debug_operands(self.handle, self._stream(stream), r["P"].data_ptr(),
+                               r["P_scale"].data_ptr() if "P_scale" in r else None, r["h"].data_ptr(),
+                               r["h_scale"].data_ptr() if "h_scale" in r else None)
         return r
 
     def debug_inject(self, kind, arg=0, stream=None):

@@ -17,7 +17,9 @@
 //
 // Set-up: the first call on a device (with that device current) looks up the
 // array's device address with cudaGetSymbolAddress and caches it for that
-// device; make that first call before any stream capture begins.  Every call
+// device for the life of the process; make that first call before any stream
+// capture begins.  A device reset invalidates the cached address, so a caller
+// that resets the device must restart the process before calling again.  Every call
 // shares the one array: calls whose kernels overlap on the GPU (two streams,
 // two host threads) race on it and must be serialised by the caller.  Each
 // call clears the tickets (they must start at zero) with cudaMemsetAsync on

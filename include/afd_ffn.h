@@ -196,6 +196,27 @@ int afd_ffn_host_wait(afd_ffn_t h);
 int afd_ffn_debug_routing(afd_ffn_t h, void* stream, int* topk_idx, float* topk_w, int* counts, int* offsets,
                           int* perm_token, int* pos, float* logits);
 
+/* Copy the expert-GEMM operands of the last forward (for a micro-batched
+ * forward, those of its first micro-batch) into caller device buffers, for
+ * tests that check the packing and the fp8 quantisation code for code.  Each
+ * pointer may be NULL to skip it.  R = T*(k + n_shared) packed rows: the
+ * routed rows in expert-contiguous order (offsets / perm_token of
+ * afd_ffn_debug_routing), then, with a shared expert, one row per token in
+ * token order.
+ *   P       [R, H] packed token rows: fp32 (AFD_FP32), bf16 (AFD_BF16) or
+ *           e4m3 codes (AFD_FP8_E4M3, one byte each)
+ *   P_scale [H/128, R] fp32 (AFD_FP8_E4M3 only): the scale of each row's
+ *           128-channel block; code * scale is the packed value
+ *   Hmid    [R, I] SwiGLU output, the down GEMM's operand: fp32, bf16 or
+ *           e4m3 codes as P
+ *   H_scale [I/128, R] fp32 (AFD_FP8_E4M3 only), as P_scale
+ * The quantisation follows "MoE系统与AFD架构概述", section 3.3 (FP8
+ * activations) with the per-token-per-128-channel rule of the fp8 layer:
+ * scale = amax/448, code = e4m3(x / scale), nearest even, saturating; an
+ * all-zero block has scale 1 and zero codes.  Scales are rejected (AFD_EINVAL)
+ * for layers other than AFD_FP8_E4M3.  Enqueued on `stream`. */
+int afd_ffn_debug_operands(afd_ffn_t h, void* stream, void* P, float* P_scale, void* Hmid, float* H_scale);
+
 /* Synchronise `stream`, then read and clear the device error word of every
  * workspace.  Returns 0, or AFD_EDEVICE with the word's bits in
  * afd_ffn_last_error(): 1 = a kernel's bounded wait ran out (the kernel
@@ -260,8 +281,10 @@ size_t afd_ffn_device_bytes(afd_ffn_t h);
  * Scratch: one file-scope device array of 4 MiB + 1 KiB (logits and
  * completion tickets), held by every GPU that loads the library until the
  * process exits.  The first call on a device (with it current) looks up the
- * array's address with cudaGetSymbolAddress; make that first call before any
- * stream capture begins.  All calls share the array: calls whose work
+ * array's address with cudaGetSymbolAddress and keeps it for the life of the
+ * process; make that first call before any stream capture begins.  After
+ * cudaDeviceReset (or anything else that destroys the device's primary
+ * context) that address is stale: restart the process before calling again.  All calls share the array: calls whose work
  * overlaps on the GPU race and must be serialised by the caller.  Each call
  * clears the tickets with cudaMemsetAsync on `stream`, then launches one
  * kernel; nothing is allocated or freed. */

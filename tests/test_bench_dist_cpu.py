@@ -86,3 +86,15 @@ def test_traffic_records_match_source_and_shapes(tmp_path, monkeypatch):
     assert bench.recorded_traffic("gemm_fp8.cu", synth.CONFIGS["qwen3_fp8"]) == []
     (src_dir / "gemm_tc.cu").write_bytes(b"kernel v2")  # the kernel changed since the capture
     assert bench.recorded_traffic("gemm_tc.cu", synth.CONFIGS["qwen3_bf16"]) == []
+
+
+def test_gpus_flag_must_match_the_launch():
+    """--gpus N without N ranks (WORLD_SIZE) is refused before any device work, instead of
+    silently running one replica."""
+    import subprocess
+
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--steps", "1"],
+                       capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode != 0
+    assert "--gpus 2 but WORLD_SIZE=1" in r.stderr
