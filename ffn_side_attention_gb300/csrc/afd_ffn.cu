@@ -143,7 +143,7 @@ int alloc_workspace(afd_ffn* h, Workspace& ws) {
       (rc = dmalloc_t(h, &ws.tile_counter, (T + afd::kRouterTokTile - 1) / afd::kRouterTokTile)) ||
       (rc = dmalloc_t(h, &ws.tok_ticket, T)) ||
       (rc = dmalloc_t(h, &ws.counts, G)) || (rc = dmalloc_t(h, &ws.offsets, G + 1)) ||
-      (rc = dmalloc_t(h, &ws.tile_base, G + 1)) || (rc = dmalloc_t(h, &ws.gu_done, G)) || (rc = dmalloc_t(h, &ws.block_hist, ((T + 255) / 256) * E)) ||
+      (rc = dmalloc_t(h, &ws.tile_base, G + 1)) || (rc = dmalloc_t(h, &ws.gu_done, G)) || (rc = dmalloc_t(h, &ws.block_hist, ((T + 255) / 256) * E)) || (rc = dmalloc_t(h, &ws.route_sync, 2)) ||
       (rc = dmalloc_t(h, &ws.perm, R)) ||
       (rc = dmalloc_t(h, &ws.pos, T * k)) || (rc = dmalloc(h, &ws.P, R * c.H * ab)) ||
       (rc = dmalloc(h, &ws.Hb, R * c.I * (c.dtype == AFD_FP8_E4M3 ? 1 : act_bytes(c)))) ||
@@ -162,6 +162,7 @@ int alloc_workspace(afd_ffn* h, Workspace& ws) {
   }
   CUDA_TRY(h, cudaMemset(ws.tile_counter, 0, sizeof(int32_t) * ((T + afd::kRouterTokTile - 1) / afd::kRouterTokTile)));
   CUDA_TRY(h, cudaMemset(ws.err, 0, sizeof(int)));
+  CUDA_TRY(h, cudaMemset(ws.route_sync, 0, 2 * sizeof(int32_t)));
   CUDA_TRY(h, cudaMemset(ws.tok_ticket, 0, sizeof(int32_t) * T));
   CUDA_TRY(h, cudaMemset(ws.P, 0, R * c.H * ab));
   CUDA_TRY(h, cudaMemset(ws.Hb, 0, R * c.I * (c.dtype == AFD_FP8_E4M3 ? 1 : act_bytes(c))));
@@ -177,7 +178,7 @@ int alloc_workspace(afd_ffn* h, Workspace& ws) {
 
 void free_workspace(Workspace& ws) {
   void* ptrs[] = {ws.topk_idx, ws.topk_w, ws.logits, ws.tile_counter, ws.tok_ticket, ws.counts, ws.offsets, ws.tile_base,
-                  ws.block_hist, ws.perm, ws.pos, ws.P, ws.P_scale, ws.Hb, ws.H_scale, ws.Y, ws.err,
+                  ws.block_hist, ws.route_sync, ws.perm, ws.pos, ws.P, ws.P_scale, ws.Hb, ws.H_scale, ws.Y, ws.err,
                   ws.stage, ws.Xc, ws.xnorm, ws.rpart};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -286,7 +287,7 @@ int run_layer(afd_ffn* h, const SrcTable& st, Workspace& ws, cudaStream_t s) {
   if ((rc = prof_mark(h, 1, s))) return rc;
   {
     NvtxRange r("afd.routing");
-    CUDA_TRY(h, afd::launch_routing(d, T, ws, s));
+    CUDA_TRY(h, afd::launch_routing(d, T, ws, h->num_sms, s));
   }
   if ((rc = prof_mark(h, 2, s))) return rc;
   {
@@ -593,6 +594,10 @@ int afd_ffn_forward_host_async(afd_ffn_t h, int n_micro, const void* const* src_
   }
   if (rc) {
     if (!h->async_rc) h->async_rc = rc;
+    // part of the layer may have been enqueued: mark the slot busy until it has run, so
+    // the next call on this slot does not overwrite sources those kernels still read
+    cudaEventRecord(h->ev_done[q], comp);
+    cudaEventRecord(h->ev_out[q], comp);
     return rc;
   }
   CUDA_TRY(h, cudaEventRecord(h->ev_done[q], comp));
@@ -643,6 +648,27 @@ int afd_ffn_debug_routing(afd_ffn_t h, void* stream, int* topk_idx, float* topk_
   return AFD_OK;
 }
 
+int afd_ffn_debug_operands(afd_ffn_t h, void* stream, void* P, float* P_scale, void* Hmid, float* H_scale) {
+  if (!h) return AFD_EINVAL;
+  const bool fp8 = h->cfg.dtype == AFD_FP8_E4M3;
+  if (!fp8 && (P_scale || H_scale)) return fail(h, AFD_EINVAL, "operand scales exist only for the fp8 layer");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Workspace& ws = h->ws[h->route_ws];
+  if (!ws.ready) return fail(h, AFD_EINVAL, "no forward has run on this handle");
+  const size_t R = (size_t)ws.last_T * (h->cfg.k + h->cfg.n_shared);
+  if (R == 0) return AFD_OK;
+  const size_t H = h->cfg.H, I = h->cfg.I, eb = fp8 ? 1 : act_bytes(h->cfg);
+  if (P) CUDA_TRY(h, cudaMemcpyAsync(P, ws.P, R * H * eb, cudaMemcpyDeviceToDevice, s));
+  if (Hmid) CUDA_TRY(h, cudaMemcpyAsync(Hmid, ws.Hb, R * I * eb, cudaMemcpyDeviceToDevice, s));
+  // scales are stored K-block major with row stride scale_ld: copy the first R of each block
+  const size_t ld = (size_t)ws.scale_ld * sizeof(float), w = R * sizeof(float);
+  if (P_scale)
+    CUDA_TRY(h, cudaMemcpy2DAsync(P_scale, w, ws.P_scale, ld, w, H / 128, cudaMemcpyDeviceToDevice, s));
+  if (H_scale)
+    CUDA_TRY(h, cudaMemcpy2DAsync(H_scale, w, ws.H_scale, ld, w, I / 128, cudaMemcpyDeviceToDevice, s));
+  return AFD_OK;
+}
+
 int afd_ffn_debug_inject(afd_ffn_t h, void* stream, int kind, long long arg) {
   if (!h) return AFD_EINVAL;
   if (kind != AFD_INJECT_TIMEOUT && kind != AFD_INJECT_RANGE)
@@ -662,7 +688,7 @@ int afd_ffn_debug_inject(afd_ffn_t h, void* stream, int kind, long long arg) {
   for (int j = 0; j < h->cfg.k; ++j) idx[j] = j == 0 ? h->cfg.E : j - 1;
   CUDA_TRY(h, cudaMemcpyAsync(ws.topk_idx, idx.data(), idx.size() * sizeof(int32_t), cudaMemcpyHostToDevice, s));
   CUDA_TRY(h, cudaStreamSynchronize(s));  // idx is a host temporary
-  CUDA_TRY(h, afd::launch_routing(h->dims, 1, ws, s));
+  CUDA_TRY(h, afd::launch_routing(h->dims, 1, ws, h->num_sms, s));
   return AFD_OK;
 }
 
@@ -712,13 +738,13 @@ int afd_ffn_profile_end(afd_ffn_t h, double* ms_per_kernel, int* n_forwards) {
 }
 
 // router (one kernel for fp32 and small bf16/fp8 batches; stage, tensor-core
-// logits and select otherwise), two routing-table kernels, pack, two GEMMs,
+// logits and select otherwise), the routing-table kernel, pack, two GEMMs,
 // combine
 int afd_ffn_launches_per_forward(afd_ffn_t h, int T) {
   if (!h || T < 1) return AFD_EINVAL;
   const afd::LayerDims& d = h->dims;
   const int router = d.dtype == AFD_FP32 ? 1 : afd::router_tc_launches(d, T, h->num_sms);
-  return router + 2 /* routing tables */ + 1 /* pack */ + 2 /* GEMMs */ + 1 /* combine */;
+  return router + 1 /* routing tables */ + 1 /* pack */ + 2 /* GEMMs */ + 1 /* combine */;
 }
 
 const char* afd_ffn_last_error(afd_ffn_t h) { return h ? h->err.c_str() : "handle is NULL"; }

@@ -379,6 +379,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  // The per-group down launch reads h through the progress counters and otherwise never
+  // waits for the gate/up grid; waiting here (free by now) keeps "this kernel complete
+  // implies every earlier kernel of the stream complete", which the next forward's
+  // routing relies on when it zeroes the counters.
+  pdl_wait();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

@@ -23,11 +23,16 @@
 // Bound: |Lt - exact| + |L - exact| <= (g_tc + g_c) * sum_h |x_h w_h|, and
 // sum |x w| <= ||x|| ||w_e|| (Cauchy-Schwarz, both norms rounded up).
 // g_c = n u / (1 - n u), n = H/32 + 6, u = 2^-24 (the fp32 fma chain and fold);
-// g_tc = (H + splits + 2) * 2^-21: the tensor core multiplies bf16 values
-// exactly and is taken to lose at most 2^-21 relative per accumulation step
-// (fp32 accumulation with truncation loses at most 2^-23; the factor 4 is
-// margin).  Each side's bias addition adds 2^-24 |Lt| rounding, covered by an
-// extra 2^-22 (|Lt_e| + |bias_e|) + 2^-100.
+// g_tc = (H/8 + splits + 2) * 2^-21: the tensor core multiplies bf16 values
+// exactly and adds them to its fp32 accumulator in groups (16 products per
+// K=16 instruction); it is taken to lose at most 2^-21 of sum |x w| per group
+// of 8 products (fp32 accumulation with truncation loses at most 2^-23 per
+// rounding: a factor 4 of margin, and a rounding counted every 8 products
+// rather than every 16), plus one step per split partial and two more.  The
+// GPU test of this band measures, on every shape the layer runs this path on,
+// the estimate's error against the canonical logits.  Each side's bias
+// addition adds 2^-24 |Lt| rounding, covered by an extra
+// 2^-22 (|Lt_e| + |bias_e|) + 2^-100.
 #include <cuda_bf16.h>
 
 #include "afd_internal.cuh"
@@ -774,7 +779,7 @@ cudaError_t launch_router_tc(const SrcTable& st, const void* wrT, const float* b
   const double u = 1.0 / 16777216.0;  // 2^-24
   const double n = d.H / 32.0 + 6.0;
   const double g_c = n * u / (1.0 - n * u);
-  const double g_tc = (d.H + nsplit + 2.0) * (1.0 / 2097152.0);  // 2^-21
+  const double g_tc = (d.H / 8.0 + nsplit + 2.0) * (1.0 / 2097152.0);  // 2^-21 per 8 products
   sa.g = (float)((g_c + g_tc) * 1.0001);
   sa.logits = ws.logits;
   sa.topk_idx = ws.topk_idx;

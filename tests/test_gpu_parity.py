@@ -7,7 +7,8 @@ import torch
 
 from ffn_side_attention_gb300 import afd, synth
 
-from gpu_helpers import (assert_close, assert_routing_exact, make_layer, out_to_f64, ref_to_f64, run_case)
+import oracle
+from gpu_helpers import (assert_close, assert_routing_exact, cfg_dict, make_layer, out_to_f64, ref_to_f64, run_case)
 
 pytestmark = pytest.mark.gpu
 
@@ -64,26 +65,34 @@ def test_bf16_zipf_bias_imbalance():
     assert_close(c, out_to_f64(outs), ref_to_f64(c, ref["out"]))
 
 
-@pytest.mark.parametrize("B,M", [(6, 1), (48, 4)])
-def test_qwen3_bf16_small_batches_full_output(B, M):
-    c = synth.CONFIGS["qwen3_bf16"].with_batch(B, M)
-    layer, srcs, outs, r, ref = run_case(c, [B] * M)
+@pytest.fixture(scope="module")
+def qwen3_bf16_layer():
+    """One qwen3_bf16 layer (H=4096, I=1536, E=128, k=8) sized for the largest aggregated
+    batch (8 x 395 tokens), shared by the twelve (B, M) decode-batch cases."""
+    c = synth.CONFIGS["qwen3_bf16"]
+    w = synth.make_weights(c, "cuda")
+    layer = make_layer(c, w, max_tokens=c.T, max_sources=c.M)
+    yield c, layer, synth.weights_numpy(w)
+    layer.close()
+
+
+@pytest.mark.parametrize("B,M", list(synth.CONFIGS["qwen3_bf16"].batches))
+def test_qwen3_bf16_every_decode_batch_full_output(qwen3_bf16_layer, B, M):
+    """Every (B, M) point of the Qwen3 bf16 workload: per-instance decode batches
+    B in {6, 48, 197, 395} (FastAFD blog section 1) aggregated from M in {1, 4, 8}
+    attention instances (section 2).  Routing bit-exact and the WHOLE output within the
+    bf16 tolerance of the oracle, up to T = 3160."""
+    base, layer, wn = qwen3_bf16_layer
+    c = base.with_batch(B, M)
+    srcs = synth.make_sources(c, "cuda", seed=B * 10 + M)
+    outs = layer.forward(srcs)
+    torch.cuda.synchronize()
+    layer.check()
+    r = layer.routing(c.T)
+    torch.cuda.synchronize()
+    ref = oracle.moe_forward(cfg_dict(c), [synth.to_numpy_bits(s) for s in srcs], wn)
     assert_routing_exact(c, r, ref, c.T)
     assert_close(c, out_to_f64(outs), ref_to_f64(c, ref["out"]))
-
-
-def test_qwen3_bf16_full_size_sampled():
-    """T = 8 x 395 = 3160 (the largest aggregated batch): routing bit-exact on
-    every token, outputs checked on sampled tokens (buffer edges + random)."""
-    c = synth.CONFIGS["qwen3_bf16"]
-    T = c.T
-    rng = np.random.default_rng(11)
-    edges = sorted({0, T - 1} | {m * c.B for m in range(c.M)} | {m * c.B - 1 for m in range(1, c.M)})
-    tokens = sorted(set(edges) | set(rng.choice(T, 16, replace=False).tolist()))
-    layer, srcs, outs, r, ref = run_case(c, [c.B] * c.M, tokens=tokens)
-    assert_routing_exact(c, r, ref, T)
-    got = out_to_f64(outs)[tokens]
-    assert_close(c, got, ref_to_f64(c, ref["out"]))
 
 
 def test_pipelined_equals_single_and_deterministic():
@@ -209,14 +218,36 @@ def test_device_checks_report_and_the_handle_recovers(kind, text):
 
 def test_launches_per_forward_by_batch():
     """One router launch for small batches, three (stage, logits, select) for
-    large ones; then 2 routing, pack, 2 GEMMs, combine."""
+    large ones; then one routing-table launch, pack, 2 GEMMs, combine."""
     c = synth.CONFIGS["qwen3_bf16"]
     w = synth.make_weights(c, "cuda")
     layer = make_layer(c, w, max_tokens=4096, max_sources=8)
-    assert layer.launches_per_forward(6) == 7
-    assert layer.launches_per_forward(3160) == 9
+    assert layer.launches_per_forward(6) == 6
+    assert layer.launches_per_forward(3160) == 8
     with pytest.raises(afd.AfdError):
         layer.launches_per_forward(0)
+
+
+@pytest.mark.parametrize("counts", [[1], [255, 1], [20000, 20001]])
+def test_routing_tables_one_launch_edges(counts):
+    """The routing tables come from one launch: chunks of 256 tokens, a grid of at most
+    one block per SM walking them, and a last-block hand-off.  One token; exactly one
+    full chunk; and more chunks (157) than SMs, so blocks walk several chunks.  Tables
+    bit-exact on each of several forwards in a row (the hand-off's epoch advances)."""
+    c = _small(E=16, k=4, H=256, I=128, S=1)
+    layer, srcs, outs, r, ref = run_case(c, counts)
+    T = sum(counts)
+    assert_routing_exact(c, r, ref, T)
+    assert_close(c, out_to_f64(outs), ref_to_f64(c, ref["out"]))
+    for _ in range(3):
+        again = layer.forward(srcs)
+        torch.cuda.synchronize()
+        layer.check()
+        r2 = layer.routing(T)
+        for key in ("counts", "offsets", "perm", "pos"):
+            assert torch.equal(r2[key], r[key]), key
+        for x, y in zip(outs, again):
+            assert torch.equal(x, y)
 
 
 def test_empty_batch_is_noop():
@@ -281,8 +312,9 @@ def test_fp8_shapes(shape, counts):
 @pytest.mark.parametrize("T", [1, 32, 33, 64, 65, 127, 160, 193])
 def test_fp8_tile_fill_at_the_short_tile_bounds(T):
     """k = E: every expert (and the shared one) gets all T tokens, so the last tile of each
-    group holds T mod 128 rows (128 when that is 0) and crosses the 32- and 64-row bounds
-    between the swapped short-tile MMA and the 128-token one."""
+    group holds T mod 128 rows (128 when that is 0): tiles filled to 1, 32, 33, 64, 65 and
+    127 rows exercise the TMA boxes of 32 token rows and the epilogue warps whose lanes
+    hold no token."""
     c = _small(dtype="fp8", E=8, k=8, H=512, I=256, S=1)
     layer, srcs, outs, r, ref = run_case(c, [T])
     assert_routing_exact(c, r, ref, T)
@@ -297,29 +329,32 @@ def _sampled(c, n_random=12, seed=13):
     return sorted(edges | set(rng.choice(T, n_random, replace=False).tolist()))
 
 
-def test_qwen3_fp8_full_size_sampled():
+def test_qwen3_fp8_full_output():
+    """qwen3_fp8 at its full size (T = 4 x 395): the whole output against the oracle."""
     c = synth.CONFIGS["qwen3_fp8"]
-    tokens = _sampled(c)
-    layer, srcs, outs, r, ref = run_case(c, [c.B] * c.M, tokens=tokens)
+    layer, srcs, outs, r, ref = run_case(c, [c.B] * c.M)
     assert_routing_exact(c, r, ref, c.T)
-    assert_close(c, out_to_f64(outs)[tokens], ref_to_f64(c, ref["out"]))
+    assert_close(c, out_to_f64(outs), ref_to_f64(c, ref["out"]))
 
 
 @pytest.mark.parametrize("B", [64, 256, 512])
-def test_dsv3_fp8_zipf_sampled(B):
-    """DeepSeek-V3 shapes, Zipf-biased routing, shared expert; T = 8 x B."""
+def test_dsv3_fp8_zipf(B):
+    """DeepSeek-V3 shapes, Zipf-biased routing, shared expert; T = 8 x B.  T = 512: the
+    whole output; T = 2048 and 4096 (oracle minutes per full pass): routing on every
+    token, outputs on 64 sampled tokens (buffer edges + random)."""
     c = synth.CONFIGS["dsv3_fp8"].with_batch(B, 8)
-    tokens = _sampled(c, n_random=8)
+    tokens = None if B == 64 else _sampled(c, n_random=48)
     layer, srcs, outs, r, ref = run_case(c, [c.B] * c.M, tokens=tokens)
     assert_routing_exact(c, r, ref, c.T)
-    assert_close(c, out_to_f64(outs)[tokens], ref_to_f64(c, ref["out"]))
+    got = out_to_f64(outs) if tokens is None else out_to_f64(outs)[tokens]
+    assert_close(c, got, ref_to_f64(c, ref["out"]))
 
 
 def test_step3_bf16_three_microbatches_sampled():
     """Step3 shapes: T = 8 x 256 as three pipelined micro-batches (683/683/682),
     bitwise equal to one pass, sampled tokens against the oracle."""
     c = synth.CONFIGS["step3_bf16"]
-    tokens = _sampled(c, n_random=8)
+    tokens = _sampled(c, n_random=48)
     layer, srcs, outs, r, ref = run_case(c, [c.B] * c.M, tokens=tokens)
     assert_routing_exact(c, r, ref, c.T)
     assert_close(c, out_to_f64(outs)[tokens], ref_to_f64(c, ref["out"]))
@@ -340,25 +375,77 @@ def test_small_batch_router_logits_all_canonical():
     assert_close(c, out_to_f64(outs), ref_to_f64(c, ref["out"]))
 
 
-def test_tensor_core_router_error_within_guard_band():
-    """The tensor-core logits that are not recomputed exactly must lie within
-    the bound the candidate rule assumes, with a wide margin (the model's
-    2^-21 per accumulation step is itself conservative)."""
-    c = synth.CONFIGS["qwen3_bf16"].with_batch(395, 2)  # T = 790: above the small-batch router
-    counts = [c.B] * c.M
-    layer, srcs, outs, r, ref = run_case(c, counts)
+def _router_splits(H, E, T, num_sms):
+    """K splits of the tensor-core router logits, as the launcher chooses them."""
+    tiles = -(-T // 128) * -(-E // 128)
+    num_kb = H // 64
+    splits = min(max(1, num_sms // tiles), max(num_kb // 4, 1), 8)
+    per = -(-num_kb // splits)
+    return -(-num_kb // per)
+
+
+GUARD_BAND_CASES = [
+    ("qwen3_bf16", 395, 2, 1),
+    ("qwen3_bf16", 395, 8, 1),
+    ("qwen3_fp8", 395, 4, 1),
+    ("dsv3_fp8", 64, 8, 1),
+    ("dsv3_fp8", 256, 8, 1),
+    ("dsv3_fp8", 512, 8, 1),
+    ("step3_bf16", 256, 8, 1),
+]
+
+
+@pytest.mark.parametrize("name,B,M,n_micro", GUARD_BAND_CASES)
+def test_tensor_core_router_error_within_guard_band(name, B, M, n_micro):
+    """The tensor-core logit estimates that are not recomputed exactly must lie within the
+    bound the candidate rule assumes, b_e = g * ||x|| * ||w_e|| + 2^-22 (|L~| + |bias|),
+    g = (g_canonical + (H/8 + splits + 2) * 2^-21) * 1.0001, with the norms rounded up as the
+    kernels round them.  Every shape the layer runs on the estimate path: qwen3 at T = 790
+    and 3160, qwen3 fp8, DeepSeek-V3 fp8 with the Zipf bias (H = 7168, E = 256) at its
+    three batches, and Step3 (H = 7168, E = 48, k = 3) in one pass (its 683-token micro-batches
+    take the small-batch router, whose logits are all canonical).  The
+    worst ratio must stay below 1/8 (the 2^-21 per 8 products in g is itself conservative);
+    selection and the selected logits are bit-exact against the oracle's canonical ones."""
+    c = synth.CONFIGS[name].with_batch(B, M)
     T, E = c.T, c.E
-    got = r["logits"].cpu().numpy().reshape(T, E).astype(np.float64)
-    exact = ref["logits"].astype(np.float64)
-    x = torch.cat([s.float() for s in srcs]).cpu().numpy().astype(np.float64)
-    w = synth.make_weights(c, "cuda")["w_router"].float().cpu().numpy().astype(np.float64)
-    xn = np.linalg.norm(x, axis=1) * (1 + 1 / 1024)
-    wn = np.linalg.norm(w, axis=0) * (1 + 1 / 1024)
+    srcs = synth.make_sources(c, "cuda")
+    w = synth.make_weights(c, "cuda")
+    layer = make_layer(c, w, max_tokens=T, max_sources=M)
+    x = torch.cat(srcs)
+    q, rem = divmod(T, n_micro)
+    T0 = q + (1 if rem else 0)  # the routing read-out is the first micro-batch's
+    layer.forward(srcs, n_micro=n_micro)
+    torch.cuda.synchronize()
+    layer.check()
+    r = layer.routing(T0)
+    torch.cuda.synchronize()
+    xb = synth.to_numpy_bits(x[:T0])
+    wr = synth.to_numpy_bits(w["w_router"])
+    bias = w["router_bias"].cpu().numpy() if "router_bias" in w else None
+    exact = oracle.router_logits(xb, wr, "bf16", bias)
+    idx_ref, w_ref = oracle.topk(exact, c.k)
+    idx = r["idx"].cpu().numpy().reshape(T0, c.k)
+    assert np.array_equal(idx, idx_ref), "top-k indices differ"
+    got32 = r["logits"].cpu().numpy().reshape(T0, E)
+    rows = np.arange(T0)[:, None]
+    assert np.array_equal(got32[rows, idx].view(np.uint32), exact[rows, idx].view(np.uint32))
+    assert np.abs(r["w"].cpu().numpy().reshape(T0, c.k) - w_ref).max() <= 2e-6
+    got = got32.astype(np.float64)
+    ex = exact.astype(np.float64)
+    xf = x[:T0].float().cpu().numpy().astype(np.float64)
+    wf = w["w_router"].float().cpu().numpy().astype(np.float64)
+    xn = np.linalg.norm(xf, axis=1) * (1 + 1 / 1024)
+    wn = np.linalg.norm(wf, axis=0) * (1 + 1 / 1024)
     u = 2.0 ** -24
     n = c.H / 32 + 6
-    g = (n * u / (1 - n * u) + (c.H + 8 + 2) * 2.0 ** -21) * 1.0001
-    bound = g * xn[:, None] * wn[None, :]
-    est = got != exact  # entries holding the tensor-core estimate
-    assert est.sum() > T * (E - 3 * c.k)  # most entries are estimates
-    ratio = np.abs(got - exact)[est] / bound[est]
-    assert ratio.max() < 1 / 16, f"tensor-core error reached {ratio.max():.3f} of the guard band"
+    ns = _router_splits(c.H, E, T0, torch.cuda.get_device_properties(0).multi_processor_count)
+    g = (n * u / (1 - n * u) + (c.H / 8 + ns + 2) * 2.0 ** -21) * 1.0001
+    babs = np.abs(bias.astype(np.float64))[None, :] if bias is not None else 0.0
+    bound = g * xn[:, None] * wn[None, :] + 2.0 ** -22 * (np.abs(got) + babs)
+    est = got32.view(np.uint32) != exact.view(np.uint32)  # entries holding the tensor-core estimate
+    assert est.sum() > T0 * E // 2  # most entries are estimates
+    ratio = np.abs(got - ex)[est] / bound[est]
+    print(f"guard band {name} T={T} n_micro={n_micro}: worst ratio {ratio.max():.3e}, "
+          f"candidates per token {(~est).sum() / T0:.2f}")
+    assert ratio.max() < 1 / 8, f"tensor-core error reached {ratio.max():.3f} of the guard band"
+    layer.close()
