@@ -202,7 +202,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_dec();
     if (warp == 0 && lane == 0) {
       // ---------------- TMA producer
-      const uint64_t pol_w = l2_policy_evict_first();
+      // weights: evict-first when only one token tile reads them, normal when the group's
+      // other tiles (items adjacent in the work list) read them again from L2
+      const uint64_t pol_w1 = l2_policy_evict_first();
+      const uint64_t pol_wn = l2_policy_evict_normal();
       const uint64_t pol_x = l2_policy_evict_last();
       int s = 0;
       uint32_t ph = 0, filled = 0, fill_ph = 0;
@@ -214,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rb1 = rb0 + args.w1_offset / 128;
         const int nbox = (it.nrows + kXBoxRows - 1) / kXBoxRows;
         const uint32_t bytes = 2 * kWTile + nbox * kXBoxRows * kRowBytes;
+        const uint64_t pol_w = (s_tb[it.g + 1] - s_tb[it.g]) > 1 ? pol_wn : pol_w1;
         for (int kb = 0; kb < args.num_kb; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u, abort, args.err)) {
             ok = false;

@@ -25,18 +25,22 @@
 //      warp sets bit `lane` of a per-expert word for every expert its token
 //      chose; the rank is the popcount of the lower lanes' bits plus the
 //      popcounts of the earlier warps' words.
-//   2. hand-off: each block, once its chunks' counts are out, takes a ticket;
-//      the last block turns the chunk counts into per-chunk bases (exclusive
-//      prefix over chunks, per expert), scans the totals into counts, offsets
-//      and GEMM tile bases, and publishes them by storing this launch's epoch
-//      to a flag (release).  The other blocks wait for the flag (acquire),
-//      with the same bounded wait as every other cross-block wait: on expiry
-//      they set the device error word and return.  Every waiting block has
-//      already taken its ticket, and the grid is no larger than the SM count,
-//      so the last block is never kept from running by a waiting one.
-//   3. place: pos = offsets[e] + chunk base + rank and perm[pos] = token.
+//   2. barrier: each block, once its chunks' counts are out, takes a ticket; the
+//      last block resets the ticket and stores this launch's epoch to a flag
+//      (release); the others wait for the flag (acquire), with the same bounded
+//      wait as every other cross-block wait: on expiry they set the device error
+//      word and return.  Every waiting block already holds its ticket and the
+//      grid is no larger than the SM count, so a waiting block never keeps the
+//      last one from running;
+//   3. every block then reads the chunk counts (independent loads, one running
+//      prefix per expert), keeps the bases of its own chunks, scans the totals
+//      into offsets (block 0 also writes counts, offsets, GEMM tile bases and
+//      zeroes the gate/up progress counters) and writes
+//      pos = offsets[e] + chunk base + rank and perm[pos] = token.
 // The earlier two-launch form (rank, then place with every block re-adding
 // the counts) cost one more kernel boundary per forward.
+#include <mutex>
+
 #include "afd_internal.cuh"
 
 namespace afd {
@@ -44,6 +48,7 @@ namespace {
 
 constexpr int kTok = 256;                  // tokens per chunk (one per thread)
 constexpr int kWarpsPerBlock = kTok / 32;  // 8
+constexpr size_t kRoutingMaxSmem = 200 * 1024;  // dynamic shared memory of the routing kernel (opt-in)
 
 // inclusive scan of one value per lane
 __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
@@ -77,7 +82,8 @@ __device__ __forceinline__ bool wait_equal(const int* p, int v, int* err) {
 struct RoutingArgs {
   const int32_t* idx;
   int T, k, E, S, BN, nchunks;
-  int32_t* chunk_hist;  // [nchunks][E]: counts, then (last block) per-chunk bases
+  int nmine;            // chunks per block at most: ceil(nchunks / grid)
+  int32_t* chunk_hist;  // [nchunks][E] per-chunk counts
   int32_t* counts;
   int32_t* offsets;
   int32_t* tile_base;
@@ -85,15 +91,17 @@ struct RoutingArgs {
   int32_t* pos;  // in-chunk ranks, then packed rows
   int32_t* gu_done;
   int32_t* ticket;  // zero between launches
-  int32_t* flag;    // the epoch of the launch whose tables are final
+  int32_t* flag;    // the epoch of the last launch whose blocks all took their tickets
   int epoch;
   int* err;
 };
 
 __global__ void __launch_bounds__(kTok) routing_kernel(const RoutingArgs a) {
   pdl_begin();
-  extern __shared__ uint32_t bits[];  // [kWarpsPerBlock][E]
-  __shared__ int s_last, s_ok;
+  extern __shared__ uint32_t dyn[];  // bits [kWarpsPerBlock][E], then bases [nmine][E]
+  uint32_t* bits = dyn;
+  int32_t* s_base = reinterpret_cast<int32_t*>(dyn + kWarpsPerBlock * a.E);
+  __shared__ int s_ok;
   __shared__ int s_cnt[kMaxExperts + 1], s_off[kMaxExperts + 1], s_tb[kMaxExperts + 1];
   const int E = a.E, k = a.k;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -130,49 +138,56 @@ __global__ void __launch_bounds__(kTok) routing_kernel(const RoutingArgs a) {
     }
     __syncthreads();  // bits are reused by the next chunk
   }
-  // 2. hand-off: the last block to finish step 1 builds the tables
+  // 2. grid barrier: the last block to take a ticket releases the others
   if (threadIdx.x == 0) {
     __threadfence();  // this block's chunk counts are visible before its ticket
-    s_last = atomicAdd(a.ticket, 1) == (int)gridDim.x - 1;
-    s_ok = 1;
+    if (atomicAdd(a.ticket, 1) == (int)gridDim.x - 1) {
+      *a.ticket = 0;  // every block has taken its ticket: reset for the next launch
+      __threadfence();
+      st_release_gpu(a.flag, a.epoch);
+      s_ok = 1;
+    } else {
+      s_ok = wait_equal(a.flag, a.epoch, a.err) ? 1 : 0;
+    }
   }
   __syncthreads();
+  if (!s_ok) return;
+  // 3. per expert: the running prefix over chunks (the loads are independent), the bases
+  // of this block's chunks and the total
   const int G = E + a.S;
-  if (s_last) {
-    __threadfence();
-    for (int e = threadIdx.x; e < E; e += kTok) {
-      int run = 0;
-      for (int c = 0; c < a.nchunks; ++c) {
-        int32_t* h = a.chunk_hist + (size_t)c * E + e;
-        const int v = __ldcg(h);
-        *h = run;  // per-chunk base of expert e
-        run += v;
-      }
-      s_cnt[e] = run;
+  for (int e = threadIdx.x; e < E; e += kTok) {
+    int run = 0;
+#pragma unroll 8
+    for (int c = 0; c < a.nchunks; ++c) {
+      if (c % (int)gridDim.x == (int)blockIdx.x) s_base[(c / (int)gridDim.x) * E + e] = run;
+      run += __ldcg(a.chunk_hist + (size_t)c * E + e);
     }
-    if (threadIdx.x == 0 && a.S) s_cnt[E] = a.T;
-    __syncthreads();
-    if (warp == 0) {  // exclusive scans over the groups: offsets and GEMM tile bases
-      int carry_o = 0, carry_t = 0;
-      for (int g0 = 0; g0 < G; g0 += 32) {
-        const int g = g0 + lane;
-        const int cg = (g < G) ? s_cnt[g] : 0;
-        const int nt = (cg + a.BN - 1) / a.BN;
-        const int io = warp_incl_scan(cg, lane);
-        const int it = warp_incl_scan(nt, lane);
-        if (g < G) {
-          s_off[g] = carry_o + io - cg;
-          s_tb[g] = carry_t + it - nt;
-        }
-        carry_o += __shfl_sync(0xffffffffu, io, 31);
-        carry_t += __shfl_sync(0xffffffffu, it, 31);
+    s_cnt[e] = run;
+  }
+  if (threadIdx.x == 0 && a.S) s_cnt[E] = a.T;
+  __syncthreads();
+  if (warp == 0) {  // exclusive scans over the groups: offsets and GEMM tile bases
+    int carry_o = 0, carry_t = 0;
+    for (int g0 = 0; g0 < G; g0 += 32) {
+      const int g = g0 + lane;
+      const int cg = (g < G) ? s_cnt[g] : 0;
+      const int nt = (cg + a.BN - 1) / a.BN;
+      const int io = warp_incl_scan(cg, lane);
+      const int it = warp_incl_scan(nt, lane);
+      if (g < G) {
+        s_off[g] = carry_o + io - cg;
+        s_tb[g] = carry_t + it - nt;
       }
-      if (lane == 0) {
-        s_off[G] = carry_o;
-        s_tb[G] = carry_t;
-      }
+      carry_o += __shfl_sync(0xffffffffu, io, 31);
+      carry_t += __shfl_sync(0xffffffffu, it, 31);
     }
-    __syncthreads();
+    if (lane == 0) {
+      s_off[G] = carry_o;
+      s_tb[G] = carry_t;
+    }
+  }
+  __syncthreads();
+  if (blockIdx.x == 0)
     for (int g = threadIdx.x; g <= G; g += kTok) {
       a.offsets[g] = s_off[g];
       a.tile_base[g] = s_tb[g];
@@ -181,29 +196,16 @@ __global__ void __launch_bounds__(kTok) routing_kernel(const RoutingArgs a) {
         a.gu_done[g] = 0;  // this forward's gate/up GEMM counts its finished items here
       }
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      *a.ticket = 0;  // every block has taken its ticket: reset for the next launch
-      __threadfence();
-      st_release_gpu(a.flag, a.epoch);
-    }
-  } else {
-    if (threadIdx.x == 0) s_ok = wait_equal(a.flag, a.epoch, a.err) ? 1 : 0;
-    __syncthreads();
-    if (!s_ok) return;
-    for (int g = threadIdx.x; g <= E; g += kTok) s_off[g] = __ldcg(a.offsets + g);
-    __syncthreads();
-  }
-  // 3. packed rows
-  for (int c = blockIdx.x; c < a.nchunks; c += gridDim.x) {
+  // packed rows
+  for (int c = blockIdx.x, i = 0; c < a.nchunks; c += gridDim.x, ++i) {
     const int t = c * kTok + threadIdx.x;
     if (t < a.T) {
       for (int j = 0; j < k; ++j) {
-        const size_t i = (size_t)t * k + j;
-        const int e = __ldg(a.idx + i);
+        const size_t q = (size_t)t * k + j;
+        const int e = __ldg(a.idx + q);
         if (e < 0 || e >= E) continue;
-        const int row = s_off[e] + __ldcg(a.chunk_hist + (size_t)c * E + e) + a.pos[i];
-        a.pos[i] = row;
+        const int row = s_off[e] + s_base[i * E + e] + a.pos[q];
+        a.pos[q] = row;
         a.perm[row] = t;
       }
       if (a.S) a.perm[(size_t)a.T * k + t] = t;
@@ -250,9 +252,19 @@ cudaError_t launch_routing(const LayerDims& d, int T, Workspace& ws, int num_sms
   a.epoch = ws.route_epoch;
   a.err = ws.err;
   const int grid = nchunks < num_sms ? nchunks : num_sms;
+  a.nmine = (nchunks + grid - 1) / grid;
+  const size_t smem = sizeof(uint32_t) * (size_t)(kWarpsPerBlock + a.nmine) * d.E;
+  if (smem > kRoutingMaxSmem) return cudaErrorInvalidValue;  // ~25M tokens: beyond any workspace here
+  if (smem > 48 * 1024) {
+    static std::once_flag once;
+    static cudaError_t set_e = cudaSuccess;
+    std::call_once(once, [] {
+      set_e = cudaFuncSetAttribute(routing_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRoutingMaxSmem);
+    });
+    if (set_e != cudaSuccess) return set_e;
+  }
   {
-    const cudaError_t e_ = launch_k(routing_kernel, dim3(grid), dim3(kTok), sizeof(uint32_t) * kWarpsPerBlock * d.E,
-                                    s, a);
+    const cudaError_t e_ = launch_k(routing_kernel, dim3(grid), dim3(kTok), smem, s, a);
     if (e_ != cudaSuccess) return e_;
   }
   return cudaGetLastError();
