@@ -49,6 +49,7 @@ namespace {
 constexpr int kTok = 256;                  // tokens per chunk (one per thread)
 constexpr int kWarpsPerBlock = kTok / 32;  // 8
 constexpr size_t kRoutingMaxSmem = 200 * 1024;  // dynamic shared memory of the routing kernel (opt-in)
+constexpr int kRouteMaxK = 16;                  // slots per token (the layer's limit on k)
 
 // inclusive scan of one value per lane
 __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
@@ -105,37 +106,47 @@ __global__ void __launch_bounds__(kTok) routing_kernel(const RoutingArgs a) {
   __shared__ int s_cnt[kMaxExperts + 1], s_off[kMaxExperts + 1], s_tb[kMaxExperts + 1];
   const int E = a.E, k = a.k;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // 1. ranks within each chunk, chunk counts
+  // 1. ranks within each chunk, chunk counts.  The thread's expert ids and ranks of the
+  // block's last chunk stay in registers for step 3 (earlier chunks go through pos).
+  int ex[kRouteMaxK], rk[kRouteMaxK];
+  int last_c = -1;
   for (int c = blockIdx.x; c < a.nchunks; c += gridDim.x) {
     const int t = c * kTok + threadIdx.x;
     for (int i = threadIdx.x; i < kWarpsPerBlock * E; i += kTok) bits[i] = 0;
     __syncthreads();
     uint32_t* my = bits + warp * E;
-    if (t < a.T)
-      for (int j = 0; j < k; ++j) {
+#pragma unroll
+    for (int j = 0; j < kRouteMaxK; ++j) {
+      ex[j] = -1;
+      if (j < k && t < a.T) {
         const int e = __ldg(a.idx + (size_t)t * k + j);
         if (e < 0 || e >= E) {
           atomicOr(a.err, kErrRange);
-          continue;
+        } else {
+          ex[j] = e;
+          atomicOr(my + e, 1u << lane);
         }
-        atomicOr(my + e, 1u << lane);
       }
+    }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += kTok) {
       int total = 0;
       for (int w = 0; w < kWarpsPerBlock; ++w) total += __popc(bits[w * E + e]);
       a.chunk_hist[(size_t)c * E + e] = total;
     }
-    if (t < a.T) {
-      const uint32_t lower = (1u << lane) - 1u;
-      for (int j = 0; j < k; ++j) {
-        const int e = __ldg(a.idx + (size_t)t * k + j);
-        if (e < 0 || e >= E) continue;
+    const uint32_t lower = (1u << lane) - 1u;
+#pragma unroll
+    for (int j = 0; j < kRouteMaxK; ++j) {
+      rk[j] = 0;
+      if (ex[j] >= 0) {
+        const int e = ex[j];
         int r = __popc(my[e] & lower);
         for (int w = 0; w < warp; ++w) r += __popc(bits[w * E + e]);
-        a.pos[(size_t)t * k + j] = r;
+        rk[j] = r;
+        if (c + (int)gridDim.x < a.nchunks) a.pos[(size_t)t * k + j] = r;  // not the last chunk
       }
     }
+    last_c = c;
     __syncthreads();  // bits are reused by the next chunk
   }
   // 2. grid barrier: the last block to take a ticket releases the others
@@ -199,7 +210,16 @@ __global__ void __launch_bounds__(kTok) routing_kernel(const RoutingArgs a) {
   // packed rows
   for (int c = blockIdx.x, i = 0; c < a.nchunks; c += gridDim.x, ++i) {
     const int t = c * kTok + threadIdx.x;
-    if (t < a.T) {
+    if (t >= a.T) continue;
+    if (c == last_c) {
+#pragma unroll
+      for (int j = 0; j < kRouteMaxK; ++j)
+        if (ex[j] >= 0) {
+          const int row = s_off[ex[j]] + s_base[i * E + ex[j]] + rk[j];
+          a.pos[(size_t)t * k + j] = row;
+          a.perm[row] = t;
+        }
+    } else {
       for (int j = 0; j < k; ++j) {
         const size_t q = (size_t)t * k + j;
         const int e = __ldg(a.idx + q);
@@ -208,8 +228,8 @@ __global__ void __launch_bounds__(kTok) routing_kernel(const RoutingArgs a) {
         a.pos[q] = row;
         a.perm[row] = t;
       }
-      if (a.S) a.perm[(size_t)a.T * k + t] = t;
     }
+    if (a.S) a.perm[(size_t)a.T * k + t] = t;
   }
 }
 
