@@ -57,8 +57,7 @@ struct Workspace {
   int32_t* tile_base = nullptr; // [E+S+1], prefix of ceil(counts / GEMM tile tokens)
   int32_t* gu_done = nullptr;   // [E+S] gate/up items finished per group (bf16 GEMMs; zeroed by the routing)
   int32_t* block_hist = nullptr; // [ceil(maxT/256)][E] per-chunk expert counts, then bases, of the routing kernel
-  int32_t* route_sync = nullptr; // [2]: the routing kernel's ticket (zero between launches) and epoch flag
-  int route_epoch = 0;           // epoch of the last routing launch on this workspace
+  int32_t* route_sync = nullptr; // [2]: the routing kernel's ticket (zero between launches) and barrier generation
   int32_t* perm = nullptr;      // [max_rows] token of each packed row
   int32_t* pos = nullptr;       // [maxT*k]  packed row of each (t, j)
   float* row_w = nullptr;       // [max_rows] routing weight of each packed row

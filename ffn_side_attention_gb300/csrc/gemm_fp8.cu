@@ -31,7 +31,8 @@
 //     FMAs (__ffma2_rn); warps whose lanes hold no token skip the math, and a
 //     TMEM buffer is handed back to the MMA as soon as it has been read;
 //   * after the last block: gate/up -> h = silu(G) * U, re-quantised per
-//     token per 128 channels of I (scale = amax/448, e4m3 RNE, saturating);
+//     token per 128 channels of I (scale = amax/448, codes e4m3(h * (1/scale))
+//     RNE, saturating);
 //     down -> Y in bf16.  Each thread stores its token's row in 32-byte
 //     pieces (full L2 sectors).
 // TMA ring of 4 stages x 48 KB.  Same device-side work list, persistent CTAs
@@ -392,6 +393,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (mine) {
           const float am = fmaxf(s_red[ipar][0][r], s_red[ipar][1][r]);
           const float sc = am == 0.0f ? 1.0f : __fdiv_rn(am, 448.0f);
+          // codes from h * (1/scale): one correctly rounded reciprocal per row instead of a
+          // division per value (gate/up 277 -> 262 us for qwen3 fp8); the code can differ
+          // from e4m3(h / scale) only where h / scale lies within two fp32 ulps of an e4m3
+          // rounding boundary
+          const float rs = __frcp_rn(sc);
           // 32-byte aligned: ld_out is a multiple of 128 and the offset of 64 codes
           uint8_t* dst = static_cast<uint8_t*>(args.out) + row * args.ld_out + it.mt * 128 + half * 64;
 #pragma unroll
@@ -400,8 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
               const int j = 32 * v + 4 * q;
-              const uint32_t lo = am == 0.0f ? 0u : cvt_e4m3x2(__fdiv_rn(h[j], sc), __fdiv_rn(h[j + 1], sc));
-              const uint32_t hi = am == 0.0f ? 0u : cvt_e4m3x2(__fdiv_rn(h[j + 2], sc), __fdiv_rn(h[j + 3], sc));
+              const uint32_t lo = am == 0.0f ? 0u : cvt_e4m3x2(h[j] * rs, h[j + 1] * rs);
+              const uint32_t hi = am == 0.0f ? 0u : cvt_e4m3x2(h[j + 2] * rs, h[j + 3] * rs);
               w[q] = lo | (hi << 16);
             }
             st_global_v8(dst + 32 * v, w);

@@ -25,13 +25,15 @@
 //      warp sets bit `lane` of a per-expert word for every expert its token
 //      chose; the rank is the popcount of the lower lanes' bits plus the
 //      popcounts of the earlier warps' words.
-//   2. barrier: each block, once its chunks' counts are out, takes a ticket; the
-//      last block resets the ticket and stores this launch's epoch to a flag
-//      (release); the others wait for the flag (acquire), with the same bounded
-//      wait as every other cross-block wait: on expiry they set the device error
-//      word and return.  Every waiting block already holds its ticket and the
-//      grid is no larger than the SM count, so a waiting block never keeps the
-//      last one from running;
+//   2. barrier: each block reads the barrier's generation, then, once its chunks'
+//      counts are out, takes a ticket; the last block resets the ticket and
+//      advances the generation (release); the others wait for it to change
+//      (acquire), with the same bounded wait as every other cross-block wait: on
+//      expiry they set the device error word and return.  The state lives on the
+//      device, so a forward captured in a CUDA graph and replayed synchronises
+//      the same way.  Every waiting block already holds its ticket and the grid
+//      is no larger than the SM count, so a waiting block never keeps the last
+//      one from running;
 //   3. every block then reads the chunk counts (independent loads, one running
 //      prefix per expert), keeps the bases of its own chunks, scans the totals
 //      into offsets (block 0 also writes counts, offsets, GEMM tile bases and
@@ -65,14 +67,14 @@ __device__ __forceinline__ void st_release_gpu(int* p, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Wait until *p == v (acquire), bounded like the other cross-block waits; on expiry the
+// Wait until *p != v (acquire), bounded like the other cross-block waits; on expiry the
 // kErrTimeout bit of the error word is set and false returned.
-__device__ __forceinline__ bool wait_equal(const int* p, int v, int* err) {
-  if (ld_acquire_gpu(p) == v) return true;
+__device__ __forceinline__ bool wait_change(const int* p, int v, int* err) {
+  if (ld_acquire_gpu(p) != v) return true;
   const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     __nanosleep(32);
-    if (ld_acquire_gpu(p) == v) return true;
+    if (ld_acquire_gpu(p) != v) return true;
     if ((it & 63u) == 0 && clock64() - t0 > 4000000000ll) {
       atomicOr(err, kErrTimeout);
       return false;
@@ -92,8 +94,7 @@ struct RoutingArgs {
   int32_t* pos;  // in-chunk ranks, then packed rows
   int32_t* gu_done;
   int32_t* ticket;  // zero between launches
-  int32_t* flag;    // the epoch of the last launch whose blocks all took their tickets
-  int epoch;
+  int32_t* flag;    // barrier generation, advanced once per launch by its last block
   int* err;
 };
 
@@ -149,16 +150,19 @@ __global__ void __launch_bounds__(kTok) routing_kernel(const RoutingArgs a) {
     last_c = c;
     __syncthreads();  // bits are reused by the next chunk
   }
-  // 2. grid barrier: the last block to take a ticket releases the others
+  // 2. grid barrier: the last block to take a ticket releases the others by advancing the
+  // generation every block read before taking its ticket (no host-side state, so a
+  // forward captured in a CUDA graph and replayed synchronises the same way)
   if (threadIdx.x == 0) {
+    const int gen = ld_acquire_gpu(a.flag);  // read before this block's ticket
     __threadfence();  // this block's chunk counts are visible before its ticket
     if (atomicAdd(a.ticket, 1) == (int)gridDim.x - 1) {
       *a.ticket = 0;  // every block has taken its ticket: reset for the next launch
       __threadfence();
-      st_release_gpu(a.flag, a.epoch);
+      st_release_gpu(a.flag, gen + 1);
       s_ok = 1;
     } else {
-      s_ok = wait_equal(a.flag, a.epoch, a.err) ? 1 : 0;
+      s_ok = wait_change(a.flag, gen, a.err) ? 1 : 0;
     }
   }
   __syncthreads();
@@ -267,9 +271,6 @@ cudaError_t launch_routing(const LayerDims& d, int T, Workspace& ws, int num_sms
   a.gu_done = ws.gu_done;
   a.ticket = ws.route_sync;
   a.flag = ws.route_sync + 1;
-  // positive and never 0 (the flag's initial value); wraps before overflowing
-  ws.route_epoch = ws.route_epoch >= 0x3fffffff ? 1 : ws.route_epoch + 1;
-  a.epoch = ws.route_epoch;
   a.err = ws.err;
   const int grid = nchunks < num_sms ? nchunks : num_sms;
   a.nmine = (nchunks + grid - 1) / grid;

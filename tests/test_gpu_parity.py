@@ -250,6 +250,42 @@ def test_routing_tables_one_launch_edges(counts):
             assert torch.equal(x, y)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_forward_captured_in_a_cuda_graph_replays_like_eager(dtype):
+    """afd_ffn_forward enqueues no host synchronisation and keeps no per-launch host state
+    on the device path, so a serving loop can capture it in a CUDA graph: replaying the
+    graph over new contents of the captured source buffers gives, each time, the eager
+    forward's outputs bit for bit (the routing kernel's grid barrier included: 550 tokens
+    are three chunks of 256)."""
+    c = _small(dtype=dtype, E=16, k=4, H=256, I=256, S=1)
+    counts = [300, 0, 250]
+    w = synth.make_weights(c, "cuda")
+    layer = make_layer(c, w, max_tokens=600, max_sources=4)
+    static_in = synth.make_sources(c, "cuda", seed=1, counts=counts)
+    static_out = [torch.empty_like(x) for x in static_in]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        layer.forward(static_in, static_out)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.forward(static_in, static_out)
+    for seed in (2, 3, 4):
+        fresh = synth.make_sources(c, "cuda", seed=seed, counts=counts)
+        for dst, src in zip(static_in, fresh):
+            dst.copy_(src)
+        graph.replay()
+        torch.cuda.synchronize()
+        eager = layer.forward(fresh)
+        torch.cuda.synchronize()
+        for x, y in zip(static_out, eager):
+            assert torch.equal(x, y), f"replay with inputs {seed} differs from the eager forward"
+    layer.check()
+    layer.close()
+
+
 def test_empty_batch_is_noop():
     c = _small()
     w = synth.make_weights(c, "cuda")
