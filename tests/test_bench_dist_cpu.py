@@ -98,3 +98,18 @@ def test_gpus_flag_must_match_the_launch():
                        capture_output=True, text=True, env=env, timeout=300)
     assert r.returncode != 0
     assert "--gpus 2 but WORLD_SIZE=1" in r.stderr
+
+
+def test_per_batch_sweep_covers_every_decode_batch():
+    """The default bench line's per_batch list: every (B, M) point of the Qwen3 bf16 layer,
+    its fp8 variant, the three DeepSeek-V3 batches, Step3 as three micro-batches and the
+    tiny fp32 layer -- 18 entries, no duplicates."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    pts = bench.sweep_points()
+    assert len(pts) == len(set(pts)) == 18
+    q = {(b, m) for name, b, m, n in pts if name == "qwen3_bf16"}
+    assert q == {(b, m) for b in (6, 48, 197, 395) for m in (1, 4, 8)}
+    assert ("qwen3_fp8", 395, 4, 1) in pts and ("step3_bf16", 256, 8, 3) in pts and ("tiny_fp32", 32, 2, 1) in pts
+    assert {(b, m) for name, b, m, n in pts if name == "dsv3_fp8"} == {(64, 8), (256, 8), (512, 8)}
