@@ -432,6 +432,28 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     layer.check()
 
+    # --graph: the timed steps replay CUDA graphs that captured one forward per input set
+    # (the library enqueues no host synchronisation and keeps no per-launch host state on
+    # the device path, so a capture replays the forward exactly); the per-kernel profile
+    # and the end-to-end legs stay eager.
+    timed_step = step
+    if args.graph:
+        graphs = []
+        for j in range(n_sets):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                layer.forward(inputs[j], outs[j], stream=torch.cuda.current_stream(), n_micro=args.n_micro)
+            graphs.append(g)
+        torch.cuda.synchronize()
+
+        def timed_step(i):
+            graphs[i % n_sets].replay()
+
+        for i in range(args.warmup):
+            timed_step(i)
+        torch.cuda.synchronize()
+        layer.check()
+
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler is not None:
         time.sleep(0.3)
@@ -439,7 +461,7 @@ def run_ours(args, world, rank, local):
     t_spin = time.perf_counter()
     i = 0
     while time.perf_counter() - t_spin < 0.5:
-        step(i)
+        timed_step(i)
         i += 1
         if i % 16 == 0:
             torch.cuda.synchronize()
@@ -453,7 +475,7 @@ def run_ours(args, world, rank, local):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for i in range(args.steps):
-        step(i)
+        timed_step(i)
     ev1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -468,7 +490,7 @@ def run_ours(args, world, rank, local):
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     evs[0].record(stream)
     for i in range(args.steps):
-        step(i)
+        timed_step(i)
         evs[i + 1].record(stream)
     torch.cuda.synchronize()
     per_step = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps))
@@ -559,7 +581,7 @@ def run_ours(args, world, rank, local):
         "scaling": "weak", "vs_baseline": None,
         "dtype": {"fp32": "f32", "bf16": "bf16", "fp8": "e4m3"}[cfg.dtype], "data": "synthetic",
         "config": {"workload": f"{cfg.name} B={cfg.B} M={cfg.M} T={T}", "H": cfg.H, "I": cfg.I, "E": cfg.E,
-                   "k": cfg.k, "S": cfg.S, "n_micro": args.n_micro,
+                   "k": cfg.k, "S": cfg.S, "n_micro": args.n_micro, "cuda_graph": bool(args.graph),
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs > L2: expert weights streamed every step; 4 rotating input sets"},
         "tflops": flops / step_s / 1e12,
@@ -618,6 +640,8 @@ def main():
     ap.add_argument("--B", type=int, default=None)
     ap.add_argument("--M", type=int, default=None)
     ap.add_argument("--n-micro", type=int, default=None)
+    ap.add_argument("--graph", action="store_true",
+                    help="time CUDA-graph replays of captured forwards instead of eager launches")
     ap.add_argument("--E", type=int, default=None, help="override the expert count (small profiling cases)")
     ap.add_argument("--I", type=int, default=None, help="override the expert intermediate size (profiling cases)")
     ap.add_argument("--cpu-sample", type=int, default=0)

@@ -250,13 +250,14 @@ def test_routing_tables_one_launch_edges(counts):
             assert torch.equal(x, y)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
-def test_forward_captured_in_a_cuda_graph_replays_like_eager(dtype):
+@pytest.mark.parametrize("dtype,n_micro", [("bf16", 1), ("fp8", 1), ("bf16", 3)])
+def test_forward_captured_in_a_cuda_graph_replays_like_eager(dtype, n_micro):
     """afd_ffn_forward enqueues no host synchronisation and keeps no per-launch host state
     on the device path, so a serving loop can capture it in a CUDA graph: replaying the
     graph over new contents of the captured source buffers gives, each time, the eager
     forward's outputs bit for bit (the routing kernel's grid barrier included: 550 tokens
-    are three chunks of 256)."""
+    are three chunks of 256).  With micro-batches the capture spans the library's own
+    streams, forked from and joined back to the capturing stream with events."""
     c = _small(dtype=dtype, E=16, k=4, H=256, I=256, S=1)
     counts = [300, 0, 250]
     w = synth.make_weights(c, "cuda")
@@ -266,12 +267,12 @@ def test_forward_captured_in_a_cuda_graph_replays_like_eager(dtype):
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
-        layer.forward(static_in, static_out)
+        layer.forward(static_in, static_out, n_micro=n_micro)
     torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        layer.forward(static_in, static_out)
+        layer.forward(static_in, static_out, n_micro=n_micro)
     for seed in (2, 3, 4):
         fresh = synth.make_sources(c, "cuda", seed=seed, counts=counts)
         for dst, src in zip(static_in, fresh):
