@@ -143,7 +143,7 @@ int alloc_workspace(afd_ffn* h, Workspace& ws) {
       (rc = dmalloc_t(h, &ws.tile_counter, (T + afd::kRouterTokTile - 1) / afd::kRouterTokTile)) ||
       (rc = dmalloc_t(h, &ws.tok_ticket, T)) ||
       (rc = dmalloc_t(h, &ws.counts, G)) || (rc = dmalloc_t(h, &ws.offsets, G + 1)) ||
-      (rc = dmalloc_t(h, &ws.tile_base, G + 1)) || (rc = dmalloc_t(h, &ws.gu_done, G)) || (rc = dmalloc_t(h, &ws.block_hist, ((T + 255) / 256) * E)) || (rc = dmalloc_t(h, &ws.route_sync, 2)) ||
+      (rc = dmalloc_t(h, &ws.tile_base, G + 1)) || (rc = dmalloc_t(h, &ws.gu_done, G)) || (rc = dmalloc_t(h, &ws.block_hist, ((T + 255) / 256) * E)) ||
       (rc = dmalloc_t(h, &ws.perm, R)) ||
       (rc = dmalloc_t(h, &ws.pos, T * k)) || (rc = dmalloc(h, &ws.P, R * c.H * ab)) ||
       (rc = dmalloc(h, &ws.Hb, R * c.I * (c.dtype == AFD_FP8_E4M3 ? 1 : act_bytes(c)))) ||
@@ -162,7 +162,6 @@ int alloc_workspace(afd_ffn* h, Workspace& ws) {
   }
   CUDA_TRY(h, cudaMemset(ws.tile_counter, 0, sizeof(int32_t) * ((T + afd::kRouterTokTile - 1) / afd::kRouterTokTile)));
   CUDA_TRY(h, cudaMemset(ws.err, 0, sizeof(int)));
-  CUDA_TRY(h, cudaMemset(ws.route_sync, 0, 2 * sizeof(int32_t)));
   CUDA_TRY(h, cudaMemset(ws.tok_ticket, 0, sizeof(int32_t) * T));
   CUDA_TRY(h, cudaMemset(ws.P, 0, R * c.H * ab));
   CUDA_TRY(h, cudaMemset(ws.Hb, 0, R * c.I * (c.dtype == AFD_FP8_E4M3 ? 1 : act_bytes(c))));
@@ -178,7 +177,7 @@ int alloc_workspace(afd_ffn* h, Workspace& ws) {
 
 void free_workspace(Workspace& ws) {
   void* ptrs[] = {ws.topk_idx, ws.topk_w, ws.logits, ws.tile_counter, ws.tok_ticket, ws.counts, ws.offsets, ws.tile_base,
-                  ws.block_hist, ws.route_sync, ws.perm, ws.pos, ws.P, ws.P_scale, ws.Hb, ws.H_scale, ws.Y, ws.err,
+                  ws.block_hist, ws.perm, ws.pos, ws.P, ws.P_scale, ws.Hb, ws.H_scale, ws.Y, ws.err,
                   ws.stage, ws.Xc, ws.xnorm, ws.rpart};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -287,7 +286,7 @@ int run_layer(afd_ffn* h, const SrcTable& st, Workspace& ws, cudaStream_t s) {
   if ((rc = prof_mark(h, 1, s))) return rc;
   {
     NvtxRange r("afd.routing");
-    CUDA_TRY(h, afd::launch_routing(d, T, ws, h->num_sms, s));
+    CUDA_TRY(h, afd::launch_routing(d, T, ws, s));
   }
   if ((rc = prof_mark(h, 2, s))) return rc;
   {
@@ -688,7 +687,7 @@ int afd_ffn_debug_inject(afd_ffn_t h, void* stream, int kind, long long arg) {
   for (int j = 0; j < h->cfg.k; ++j) idx[j] = j == 0 ? h->cfg.E : j - 1;
   CUDA_TRY(h, cudaMemcpyAsync(ws.topk_idx, idx.data(), idx.size() * sizeof(int32_t), cudaMemcpyHostToDevice, s));
   CUDA_TRY(h, cudaStreamSynchronize(s));  // idx is a host temporary
-  CUDA_TRY(h, afd::launch_routing(h->dims, 1, ws, h->num_sms, s));
+  CUDA_TRY(h, afd::launch_routing(h->dims, 1, ws, s));
   return AFD_OK;
 }
 
@@ -738,13 +737,13 @@ int afd_ffn_profile_end(afd_ffn_t h, double* ms_per_kernel, int* n_forwards) {
 }
 
 // router (one kernel for fp32 and small bf16/fp8 batches; stage, tensor-core
-// logits and select otherwise), the routing-table kernel, pack, two GEMMs,
-// combine
+// logits and select otherwise), the routing tables (one launch up to 256 tokens,
+// two above), pack, two GEMMs, combine
 int afd_ffn_launches_per_forward(afd_ffn_t h, int T) {
   if (!h || T < 1) return AFD_EINVAL;
   const afd::LayerDims& d = h->dims;
   const int router = d.dtype == AFD_FP32 ? 1 : afd::router_tc_launches(d, T, h->num_sms);
-  return router + 1 /* routing tables */ + 1 /* pack */ + 2 /* GEMMs */ + 1 /* combine */;
+  return router + afd::routing_launches(T) + 1 /* pack */ + 2 /* GEMMs */ + 1 /* combine */;
 }
 
 const char* afd_ffn_last_error(afd_ffn_t h) { return h ? h->err.c_str() : "handle is NULL"; }

@@ -56,8 +56,7 @@ struct Workspace {
   int32_t* offsets = nullptr;   // [E+S+1]
   int32_t* tile_base = nullptr; // [E+S+1], prefix of ceil(counts / GEMM tile tokens)
   int32_t* gu_done = nullptr;   // [E+S] gate/up items finished per group (bf16 GEMMs; zeroed by the routing)
-  int32_t* block_hist = nullptr; // [ceil(maxT/256)][E] per-chunk expert counts, then bases, of the routing kernel
-  int32_t* route_sync = nullptr; // [2]: the routing kernel's ticket (zero between launches) and barrier generation
+  int32_t* block_hist = nullptr; // [ceil(maxT/256)][E] per-block expert counts of the routing kernels
   int32_t* perm = nullptr;      // [max_rows] token of each packed row
   int32_t* pos = nullptr;       // [maxT*k]  packed row of each (t, j)
   float* row_w = nullptr;       // [max_rows] routing weight of each packed row
@@ -133,7 +132,8 @@ cudaError_t launch_router_wnorm(const void* wrT, int H, int E, float* wnorm, cud
 cudaError_t launch_router_tc(const SrcTable& st, const void* wrT, const float* bias, const float* wnorm,
                              const CUtensorMap* tm_wr, const LayerDims& d, Workspace& ws, int num_sms,
                              cudaStream_t s);
-cudaError_t launch_routing(const LayerDims& d, int T, Workspace& ws, int num_sms, cudaStream_t s);
+cudaError_t launch_routing(const LayerDims& d, int T, Workspace& ws, cudaStream_t s);
+int routing_launches(int T);  // 1 for at most 256 tokens (one block), else 2
 cudaError_t launch_pack(const SrcTable& st, const LayerDims& d, int T, Workspace& ws, int num_sms,
                         cudaStream_t s);
 cudaError_t launch_combine(const SrcTable& st, const LayerDims& d, int T, Workspace& ws, int num_sms,

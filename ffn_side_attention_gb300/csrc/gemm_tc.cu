@@ -379,11 +379,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  // The per-group down launch reads h through the progress counters and otherwise never
-  // waits for the gate/up grid; waiting here (free by now) keeps "this kernel complete
-  // implies every earlier kernel of the stream complete", which the next forward's
-  // routing relies on when it zeroes the counters.
-  pdl_wait();
+  // The per-group down launch reads h through the progress counters and never waits for
+  // the gate/up grid as a whole.  When it completes normally every gate/up increment has
+  // been made (each group's count reached its total), so nothing of that grid can touch
+  // the counters after the next forward's routing zeroes them.  A CTA that gave up (a
+  // bounded wait ran out) waits for the previous grid before it exits, so "this kernel
+  // complete implies every earlier kernel complete" holds on that path too.  (An exit
+  // wait in every thread on every path cost 2.7% of the step at T=3160.)
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort) pdl_wait();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

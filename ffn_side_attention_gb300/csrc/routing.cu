@@ -16,42 +16,71 @@
 // T*k .. T*k+T-1.  tile_base[g] = sum over g' < g of ceil(counts[g'] / BN), the
 // GEMM work list (BN = tokens per GEMM tile).
 //
-// One launch, in chunks of 256 tokens (one thread per token), a persistent grid of
-// at most one block per SM walking the chunks:
-//   1. rank: per chunk, the per-expert counts (to a [chunks][E] array) and each
-//      entry's rank among the chunk's entries of the same expert, in token
-//      order (kept in pos).  A token's k experts are distinct, so that rank is
-//      the number of earlier tokens of the chunk that chose the expert: each
-//      warp sets bit `lane` of a per-expert word for every expert its token
-//      chose; the rank is the popcount of the lower lanes' bits plus the
-//      popcounts of the earlier warps' words.
-//   2. barrier: each block reads the barrier's generation, then, once its chunks'
-//      counts are out, takes a ticket; the last block resets the ticket and
-//      advances the generation (release); the others wait for it to change
-//      (acquire), with the same bounded wait as every other cross-block wait: on
-//      expiry they set the device error word and return.  The state lives on the
-//      device, so a forward captured in a CUDA graph and replayed synchronises
-//      the same way.  Every waiting block already holds its ticket and the grid
-//      is no larger than the SM count, so a waiting block never keeps the last
-//      one from running;
-//   3. every block then reads the chunk counts (independent loads, one running
-//      prefix per expert), keeps the bases of its own chunks, scans the totals
-//      into offsets (block 0 also writes counts, offsets, GEMM tile bases and
-//      zeroes the gate/up progress counters) and writes
-//      pos = offsets[e] + chunk base + rank and perm[pos] = token.
-// The earlier two-launch form (rank, then place with every block re-adding
-// the counts) cost one more kernel boundary per forward.
-#include <mutex>
-
+// Batches of at most 256 tokens (one block): one launch, routing_one_block_kernel.
+// The block ranks its tokens' entries (below), keeps the per-expert counts in shared
+// memory, scans them and writes pos / perm, with no global synchronisation.
+//
+// Larger batches: two launches, both one thread per token in blocks of 256 tokens:
+//   block_rank: per block, the per-expert counts (to a [blocks][E] array) and
+//     each entry's rank among the block's entries of the same expert, in
+//     token order.  A token's k experts are distinct, so that rank is the
+//     number of earlier tokens of the block that chose the expert: each warp
+//     sets bit `lane` of a per-expert word for every expert its token chose;
+//     the rank is the popcount of the lower lanes' bits plus the popcounts of
+//     the earlier warps' words.
+//   place: every block re-adds the block counts (totals, its own base per
+//     expert), scans them into offsets and tile bases, and writes
+//     pos = offsets[e] + base + rank and perm[pos] = token.
+// A single launch with a device-wide barrier between the two steps (a ticket,
+// then a generation flag, bounded waits) was built and measured slower than the
+// two launches with programmatic dependent launch: the second launch's blocks are
+// resident and released by the hardware as soon as the first grid completes,
+// while the barrier's atomics and polling cost more.
 #include "afd_internal.cuh"
 
 namespace afd {
 namespace {
 
-constexpr int kTok = 256;                  // tokens per chunk (one per thread)
+constexpr int kTok = 256;                  // tokens per block (one per thread)
 constexpr int kWarpsPerBlock = kTok / 32;  // 8
-constexpr size_t kRoutingMaxSmem = 200 * 1024;  // dynamic shared memory of the routing kernel (opt-in)
-constexpr int kRouteMaxK = 16;                  // slots per token (the layer's limit on k)
+constexpr int kRouteMaxK = 16;             // slots per token (the layer's limit on k)
+
+__global__ void __launch_bounds__(kTok) block_rank_kernel(const int32_t* __restrict__ idx, int T, int k, int E,
+                                                          int32_t* __restrict__ block_hist,
+                                                          int32_t* __restrict__ rank, int* err) {
+  pdl_begin();
+  extern __shared__ uint32_t bits[];  // [kWarpsPerBlock][E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kTok + threadIdx.x;
+  for (int i = threadIdx.x; i < kWarpsPerBlock * E; i += kTok) bits[i] = 0;
+  __syncthreads();
+  uint32_t* my = bits + warp * E;
+  if (t < T)
+    for (int j = 0; j < k; ++j) {
+      const int e = __ldg(idx + (size_t)t * k + j);
+      if (e < 0 || e >= E) {
+        atomicOr(err, kErrRange);
+        continue;
+      }
+      atomicOr(my + e, 1u << lane);
+    }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kTok) {
+    int total = 0;
+    for (int w = 0; w < kWarpsPerBlock; ++w) total += __popc(bits[w * E + e]);
+    block_hist[(size_t)blockIdx.x * E + e] = total;
+  }
+  if (t < T) {
+    const uint32_t lower = (1u << lane) - 1u;
+    for (int j = 0; j < k; ++j) {
+      const int e = __ldg(idx + (size_t)t * k + j);
+      if (e < 0 || e >= E) continue;
+      int r = __popc(my[e] & lower);
+      for (int w = 0; w < warp; ++w) r += __popc(bits[w * E + e]);
+      rank[(size_t)t * k + j] = r;
+    }
+  }
+}
 
 // inclusive scan of one value per lane
 __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
@@ -63,134 +92,38 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
   return v;
 }
 
-__device__ __forceinline__ void st_release_gpu(int* p, int v) {
-  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Wait until *p != v (acquire), bounded like the other cross-block waits; on expiry the
-// kErrTimeout bit of the error word is set and false returned.
-__device__ __forceinline__ bool wait_change(const int* p, int v, int* err) {
-  if (ld_acquire_gpu(p) != v) return true;
-  const long long t0 = clock64();
-  for (uint32_t it = 1;; ++it) {
-    __nanosleep(32);
-    if (ld_acquire_gpu(p) != v) return true;
-    if ((it & 63u) == 0 && clock64() - t0 > 4000000000ll) {
-      atomicOr(err, kErrTimeout);
-      return false;
-    }
-  }
-}
-
-struct RoutingArgs {
-  const int32_t* idx;
-  int T, k, E, S, BN, nchunks;
-  int nmine;            // chunks per block at most: ceil(nchunks / grid)
-  int32_t* chunk_hist;  // [nchunks][E] per-chunk counts
-  int32_t* counts;
-  int32_t* offsets;
-  int32_t* tile_base;
-  int32_t* perm;
-  int32_t* pos;  // in-chunk ranks, then packed rows
-  int32_t* gu_done;
-  int32_t* ticket;  // zero between launches
-  int32_t* flag;    // barrier generation, advanced once per launch by its last block
-  int* err;
-};
-
-__global__ void __launch_bounds__(kTok) routing_kernel(const RoutingArgs a) {
+__global__ void __launch_bounds__(kTok)
+    place_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ block_hist, int nblocks, int T, int k,
+                 int E, int S, int BN, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                 int32_t* __restrict__ tile_base, int32_t* __restrict__ perm, int32_t* __restrict__ pos,
+                 int32_t* __restrict__ gu_done) {
   pdl_begin();
-  extern __shared__ uint32_t dyn[];  // bits [kWarpsPerBlock][E], then bases [nmine][E]
-  uint32_t* bits = dyn;
-  int32_t* s_base = reinterpret_cast<int32_t*>(dyn + kWarpsPerBlock * a.E);
-  __shared__ int s_ok;
-  __shared__ int s_cnt[kMaxExperts + 1], s_off[kMaxExperts + 1], s_tb[kMaxExperts + 1];
-  const int E = a.E, k = a.k;
+  __shared__ int s_cnt[kMaxExperts + 1], s_base[kMaxExperts], s_off[kMaxExperts + 1], s_tb[kMaxExperts + 1];
+  const int G = E + S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // 1. ranks within each chunk, chunk counts.  The thread's expert ids and ranks of the
-  // block's last chunk stay in registers for step 3 (earlier chunks go through pos).
-  int ex[kRouteMaxK], rk[kRouteMaxK];
-  int last_c = -1;
-  for (int c = blockIdx.x; c < a.nchunks; c += gridDim.x) {
-    const int t = c * kTok + threadIdx.x;
-    for (int i = threadIdx.x; i < kWarpsPerBlock * E; i += kTok) bits[i] = 0;
-    __syncthreads();
-    uint32_t* my = bits + warp * E;
-#pragma unroll
-    for (int j = 0; j < kRouteMaxK; ++j) {
-      ex[j] = -1;
-      if (j < k && t < a.T) {
-        const int e = __ldg(a.idx + (size_t)t * k + j);
-        if (e < 0 || e >= E) {
-          atomicOr(a.err, kErrRange);
-        } else {
-          ex[j] = e;
-          atomicOr(my + e, 1u << lane);
-        }
-      }
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += kTok) {
-      int total = 0;
-      for (int w = 0; w < kWarpsPerBlock; ++w) total += __popc(bits[w * E + e]);
-      a.chunk_hist[(size_t)c * E + e] = total;
-    }
-    const uint32_t lower = (1u << lane) - 1u;
-#pragma unroll
-    for (int j = 0; j < kRouteMaxK; ++j) {
-      rk[j] = 0;
-      if (ex[j] >= 0) {
-        const int e = ex[j];
-        int r = __popc(my[e] & lower);
-        for (int w = 0; w < warp; ++w) r += __popc(bits[w * E + e]);
-        rk[j] = r;
-        if (c + (int)gridDim.x < a.nchunks) a.pos[(size_t)t * k + j] = r;  // not the last chunk
-      }
-    }
-    last_c = c;
-    __syncthreads();  // bits are reused by the next chunk
-  }
-  // 2. grid barrier: the last block to take a ticket releases the others by advancing the
-  // generation every block read before taking its ticket (no host-side state, so a
-  // forward captured in a CUDA graph and replayed synchronises the same way)
-  if (threadIdx.x == 0) {
-    const int gen = ld_acquire_gpu(a.flag);  // read before this block's ticket
-    __threadfence();  // this block's chunk counts are visible before its ticket
-    if (atomicAdd(a.ticket, 1) == (int)gridDim.x - 1) {
-      *a.ticket = 0;  // every block has taken its ticket: reset for the next launch
-      __threadfence();
-      st_release_gpu(a.flag, gen + 1);
-      s_ok = 1;
-    } else {
-      s_ok = wait_change(a.flag, gen, a.err) ? 1 : 0;
-    }
-  }
-  __syncthreads();
-  if (!s_ok) return;
-  // 3. per expert: the running prefix over chunks (the loads are independent), the bases
-  // of this block's chunks and the total
-  const int G = E + a.S;
   for (int e = threadIdx.x; e < E; e += kTok) {
-    int run = 0;
-#pragma unroll 8
-    for (int c = 0; c < a.nchunks; ++c) {
-      if (c % (int)gridDim.x == (int)blockIdx.x) s_base[(c / (int)gridDim.x) * E + e] = run;
-      run += __ldcg(a.chunk_hist + (size_t)c * E + e);
+    int before = 0, total = 0;
+    for (int b = 0; b < nblocks; ++b) {
+      const int c = __ldg(block_hist + (size_t)b * E + e);
+      if (b < (int)blockIdx.x) before += c;
+      total += c;
     }
-    s_cnt[e] = run;
+    s_cnt[e] = total;
+    s_base[e] = before;
   }
-  if (threadIdx.x == 0 && a.S) s_cnt[E] = a.T;
+  if (threadIdx.x == 0 && S) s_cnt[E] = T;
   __syncthreads();
-  if (warp == 0) {  // exclusive scans over the groups: offsets and GEMM tile bases
+  // exclusive scans over the groups (warp 0): offsets and GEMM tile bases
+  if (warp == 0) {
     int carry_o = 0, carry_t = 0;
     for (int g0 = 0; g0 < G; g0 += 32) {
       const int g = g0 + lane;
-      const int cg = (g < G) ? s_cnt[g] : 0;
-      const int nt = (cg + a.BN - 1) / a.BN;
-      const int io = warp_incl_scan(cg, lane);
+      const int c = (g < G) ? s_cnt[g] : 0;
+      const int nt = (c + BN - 1) / BN;
+      const int io = warp_incl_scan(c, lane);
       const int it = warp_incl_scan(nt, lane);
       if (g < G) {
-        s_off[g] = carry_o + io - cg;
+        s_off[g] = carry_o + io - c;
         s_tb[g] = carry_t + it - nt;
       }
       carry_o += __shfl_sync(0xffffffffu, io, 31);
@@ -204,36 +137,107 @@ __global__ void __launch_bounds__(kTok) routing_kernel(const RoutingArgs a) {
   __syncthreads();
   if (blockIdx.x == 0)
     for (int g = threadIdx.x; g <= G; g += kTok) {
-      a.offsets[g] = s_off[g];
-      a.tile_base[g] = s_tb[g];
+      offsets[g] = s_off[g];
+      tile_base[g] = s_tb[g];
       if (g < G) {
-        a.counts[g] = s_cnt[g];
-        a.gu_done[g] = 0;  // this forward's gate/up GEMM counts its finished items here
+        counts[g] = s_cnt[g];
+        gu_done[g] = 0;  // this forward's gate/up GEMM counts its finished items here
       }
     }
-  // packed rows
-  for (int c = blockIdx.x, i = 0; c < a.nchunks; c += gridDim.x, ++i) {
-    const int t = c * kTok + threadIdx.x;
-    if (t >= a.T) continue;
-    if (c == last_c) {
+  const int t = blockIdx.x * kTok + threadIdx.x;
+  if (t < T) {
+    for (int j = 0; j < k; ++j) {
+      const size_t i = (size_t)t * k + j;
+      const int e = __ldg(idx + i);
+      if (e < 0 || e >= E) continue;
+      const int row = s_off[e] + s_base[e] + pos[i];  // pos holds the in-block rank
+      pos[i] = row;
+      perm[row] = t;
+    }
+    if (S) perm[(size_t)T * k + t] = t;
+  }
+}
+
+// Whole routing of a batch of at most kTok tokens in one block: ranks (as in
+// block_rank_kernel), counts kept in shared memory, exclusive scans, placement.
+__global__ void __launch_bounds__(kTok)
+    routing_one_block_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int S, int BN,
+                             int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                             int32_t* __restrict__ tile_base, int32_t* __restrict__ perm, int32_t* __restrict__ pos,
+                             int32_t* __restrict__ gu_done, int* err) {
+  pdl_begin();
+  extern __shared__ uint32_t bits[];  // [kWarpsPerBlock][E]
+  __shared__ int s_cnt[kMaxExperts + 1], s_off[kMaxExperts + 1], s_tb[kMaxExperts + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = threadIdx.x;
+  const int G = E + S;
+  for (int i = threadIdx.x; i < kWarpsPerBlock * E; i += kTok) bits[i] = 0;
+  __syncthreads();
+  uint32_t* my = bits + warp * E;
+  int ex[kRouteMaxK];
 #pragma unroll
-      for (int j = 0; j < kRouteMaxK; ++j)
-        if (ex[j] >= 0) {
-          const int row = s_off[ex[j]] + s_base[i * E + ex[j]] + rk[j];
-          a.pos[(size_t)t * k + j] = row;
-          a.perm[row] = t;
-        }
-    } else {
-      for (int j = 0; j < k; ++j) {
-        const size_t q = (size_t)t * k + j;
-        const int e = __ldg(a.idx + q);
-        if (e < 0 || e >= E) continue;
-        const int row = s_off[e] + s_base[i * E + e] + a.pos[q];
-        a.pos[q] = row;
-        a.perm[row] = t;
+  for (int j = 0; j < kRouteMaxK; ++j) {
+    ex[j] = -1;
+    if (j < k && t < T) {
+      const int e = __ldg(idx + (size_t)t * k + j);
+      if (e < 0 || e >= E) {
+        atomicOr(err, kErrRange);
+      } else {
+        ex[j] = e;
+        atomicOr(my + e, 1u << lane);
       }
     }
-    if (a.S) a.perm[(size_t)a.T * k + t] = t;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kTok) {
+    int total = 0;
+    for (int w = 0; w < kWarpsPerBlock; ++w) total += __popc(bits[w * E + e]);
+    s_cnt[e] = total;
+  }
+  if (threadIdx.x == 0 && S) s_cnt[E] = T;
+  __syncthreads();
+  if (warp == 0) {  // exclusive scans over the groups: offsets and GEMM tile bases
+    int carry_o = 0, carry_t = 0;
+    for (int g0 = 0; g0 < G; g0 += 32) {
+      const int g = g0 + lane;
+      const int c = (g < G) ? s_cnt[g] : 0;
+      const int nt = (c + BN - 1) / BN;
+      const int io = warp_incl_scan(c, lane);
+      const int it = warp_incl_scan(nt, lane);
+      if (g < G) {
+        s_off[g] = carry_o + io - c;
+        s_tb[g] = carry_t + it - nt;
+      }
+      carry_o += __shfl_sync(0xffffffffu, io, 31);
+      carry_t += __shfl_sync(0xffffffffu, it, 31);
+    }
+    if (lane == 0) {
+      s_off[G] = carry_o;
+      s_tb[G] = carry_t;
+    }
+  }
+  __syncthreads();
+  for (int g = threadIdx.x; g <= G; g += kTok) {
+    offsets[g] = s_off[g];
+    tile_base[g] = s_tb[g];
+    if (g < G) {
+      counts[g] = s_cnt[g];
+      gu_done[g] = 0;  // this forward's gate/up GEMM counts its finished items here
+    }
+  }
+  if (t < T) {
+    const uint32_t lower = (1u << lane) - 1u;
+#pragma unroll
+    for (int j = 0; j < kRouteMaxK; ++j)
+      if (ex[j] >= 0) {
+        const int e = ex[j];
+        int r = __popc(my[e] & lower);
+        for (int w = 0; w < warp; ++w) r += __popc(bits[w * E + e]);
+        const int row = s_off[e] + r;
+        pos[(size_t)t * k + j] = row;
+        perm[row] = t;
+      }
+    if (S) perm[(size_t)T * k + t] = t;
   }
 }
 
@@ -251,41 +255,31 @@ __global__ void wait_probe_kernel(int* err, long long limit) {
   mbar_wait(&bar, 0, &abort, err, limit);  // phase 0 never completes
 }
 
-cudaError_t launch_routing(const LayerDims& d, int T, Workspace& ws, int num_sms, cudaStream_t s) {
+int routing_launches(int T) { return T <= kTok ? 1 : 2; }
+
+cudaError_t launch_routing(const LayerDims& d, int T, Workspace& ws, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const int nchunks = (T + kTok - 1) / kTok;
-  RoutingArgs a{};
-  a.idx = ws.topk_idx;
-  a.T = T;
-  a.k = d.k;
-  a.E = d.E;
-  a.S = d.S;
-  a.BN = d.dtype == AFD_FP8_E4M3 ? kGemmBNFp8 : bf16_tile_tokens(d, T);  // tokens per GEMM tile
-  a.nchunks = nchunks;
-  a.chunk_hist = ws.block_hist;
-  a.counts = ws.counts;
-  a.offsets = ws.offsets;
-  a.tile_base = ws.tile_base;
-  a.perm = ws.perm;
-  a.pos = ws.pos;
-  a.gu_done = ws.gu_done;
-  a.ticket = ws.route_sync;
-  a.flag = ws.route_sync + 1;
-  a.err = ws.err;
-  const int grid = nchunks < num_sms ? nchunks : num_sms;
-  a.nmine = (nchunks + grid - 1) / grid;
-  const size_t smem = sizeof(uint32_t) * (size_t)(kWarpsPerBlock + a.nmine) * d.E;
-  if (smem > kRoutingMaxSmem) return cudaErrorInvalidValue;  // ~25M tokens: beyond any workspace here
-  if (smem > 48 * 1024) {
-    static std::once_flag once;
-    static cudaError_t set_e = cudaSuccess;
-    std::call_once(once, [] {
-      set_e = cudaFuncSetAttribute(routing_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRoutingMaxSmem);
-    });
-    if (set_e != cudaSuccess) return set_e;
+  const int nblocks = (T + kTok - 1) / kTok;
+  const int bn = d.dtype == AFD_FP8_E4M3 ? kGemmBNFp8 : bf16_tile_tokens(d, T);  // tokens per GEMM tile
+  if (nblocks == 1) {
+    const cudaError_t e_ = launch_k(routing_one_block_kernel, dim3(1), dim3(kTok),
+                                    sizeof(uint32_t) * kWarpsPerBlock * d.E, s, ws.topk_idx, T, d.k, d.E, d.S, bn,
+                                    ws.counts, ws.offsets, ws.tile_base, ws.perm, ws.pos, ws.gu_done, ws.err);
+    if (e_ != cudaSuccess) return e_;
+    return cudaGetLastError();
   }
   {
-    const cudaError_t e_ = launch_k(routing_kernel, dim3(grid), dim3(kTok), smem, s, a);
+    const cudaError_t e_ = launch_k(block_rank_kernel, dim3(nblocks), dim3(kTok),
+                                    sizeof(uint32_t) * kWarpsPerBlock * d.E, s, ws.topk_idx, T, d.k, d.E,
+                                    ws.block_hist, ws.pos, ws.err);
+    if (e_ != cudaSuccess) return e_;
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  {
+    const cudaError_t e_ = launch_k(place_kernel, dim3(nblocks), dim3(kTok), 0, s, ws.topk_idx, ws.block_hist,
+                                    nblocks, T, d.k, d.E, d.S, bn, ws.counts, ws.offsets, ws.tile_base, ws.perm,
+                                    ws.pos, ws.gu_done);
     if (e_ != cudaSuccess) return e_;
   }
   return cudaGetLastError();

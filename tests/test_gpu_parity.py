@@ -218,22 +218,23 @@ def test_device_checks_report_and_the_handle_recovers(kind, text):
 
 def test_launches_per_forward_by_batch():
     """One router launch for small batches, three (stage, logits, select) for
-    large ones; then one routing-table launch, pack, 2 GEMMs, combine."""
+    large ones; routing tables in one launch up to 256 tokens (a single block) and two
+    above; then pack, 2 GEMMs, combine."""
     c = synth.CONFIGS["qwen3_bf16"]
     w = synth.make_weights(c, "cuda")
     layer = make_layer(c, w, max_tokens=4096, max_sources=8)
     assert layer.launches_per_forward(6) == 6
-    assert layer.launches_per_forward(3160) == 8
+    assert layer.launches_per_forward(256) == 6
+    assert layer.launches_per_forward(3160) == 9
     with pytest.raises(afd.AfdError):
         layer.launches_per_forward(0)
 
 
-@pytest.mark.parametrize("counts", [[1], [255, 1], [20000, 20001]])
-def test_routing_tables_one_launch_edges(counts):
-    """The routing tables come from one launch: chunks of 256 tokens, a grid of at most
-    one block per SM walking them, and a last-block hand-off.  One token; exactly one
-    full chunk; and more chunks (157) than SMs, so blocks walk several chunks.  Tables
-    bit-exact on each of several forwards in a row (the hand-off's epoch advances)."""
+@pytest.mark.parametrize("counts", [[1], [255, 1], [256, 1], [20000, 20001]])
+def test_routing_tables_edges(counts):
+    """Routing tables at the boundary between the single-block launch (up to 256 tokens)
+    and the two-launch form: one token, exactly 256, 257, and 40001 tokens (157 blocks).
+    Tables bit-exact against the oracle, and identical on several forwards in a row."""
     c = _small(E=16, k=4, H=256, I=128, S=1)
     layer, srcs, outs, r, ref = run_case(c, counts)
     T = sum(counts)
@@ -255,9 +256,9 @@ def test_forward_captured_in_a_cuda_graph_replays_like_eager(dtype, n_micro):
     """afd_ffn_forward enqueues no host synchronisation and keeps no per-launch host state
     on the device path, so a serving loop can capture it in a CUDA graph: replaying the
     graph over new contents of the captured source buffers gives, each time, the eager
-    forward's outputs bit for bit (the routing kernel's grid barrier included: 550 tokens
-    are three chunks of 256).  With micro-batches the capture spans the library's own
-    streams, forked from and joined back to the capturing stream with events."""
+    forward's outputs bit for bit (550 tokens: the two-launch routing tables).  With
+    micro-batches the capture spans the library's own streams, forked from and joined
+    back to the capturing stream with events."""
     c = _small(dtype=dtype, E=16, k=4, H=256, I=256, S=1)
     counts = [300, 0, 250]
     w = synth.make_weights(c, "cuda")
