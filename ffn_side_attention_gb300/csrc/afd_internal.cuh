@@ -84,7 +84,11 @@ struct Workspace {
 // launch), so nothing upstream is read early; launch_dependents then lets the
 // next kernel's CTAs be scheduled while this one runs, which hides the next
 // launch's latency behind this kernel's tail.  Completion order is unchanged:
-// each kernel waits for its predecessor, hence for every earlier one.
+// each kernel waits for its predecessor, hence for every earlier one -- with one
+// exception: the bf16 down GEMM reads h through per-expert progress counters and
+// does not wait for the gate/up grid as a whole, except on its abort path.  It
+// completes only after every gate/up increment, so the gate/up grid writes
+// nothing the next forward depends on after the down grid has completed.
 __device__ __forceinline__ void pdl_begin() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
