@@ -43,7 +43,7 @@ namespace {
 constexpr int kMaxK = 16;
 constexpr int kMaxCand = 64;
 constexpr int kPer = 8;  // router entries per lane: E <= 256 routed experts
-constexpr int kSmallRouterWaves = 8;  // small-batch path while its grid is at most this many waves
+constexpr int kSmallRouterWaves = 3;  // small-batch path while its grid is at most this many waves
 
 // ---------------------------------------------------------------- 1. stage
 __global__ void __launch_bounds__(256) stage_x_kernel(SrcTable st, int H, uint16_t* __restrict__ Xc,

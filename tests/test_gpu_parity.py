@@ -217,14 +217,16 @@ def test_device_checks_report_and_the_handle_recovers(kind, text):
 
 
 def test_launches_per_forward_by_batch():
-    """One router launch for small batches, three (stage, logits, select) for
-    large ones; routing tables in one launch up to 256 tokens (a single block) and two
-    above; then pack, 2 GEMMs, combine."""
+    """One router launch for small batches (up to 224 tokens with 128 experts), three
+    (stage, logits, select) for larger ones; routing tables in one launch up to 256 tokens
+    (a single block) and two above; then pack, 2 GEMMs, combine."""
     c = synth.CONFIGS["qwen3_bf16"]
     w = synth.make_weights(c, "cuda")
     layer = make_layer(c, w, max_tokens=4096, max_sources=8)
     assert layer.launches_per_forward(6) == 6
-    assert layer.launches_per_forward(256) == 6
+    assert layer.launches_per_forward(224) == 6   # last batch of the single-launch router
+    assert layer.launches_per_forward(232) == 8   # three router launches, one routing launch
+    assert layer.launches_per_forward(257) == 9   # and two routing launches above 256 tokens
     assert layer.launches_per_forward(3160) == 9
     with pytest.raises(afd.AfdError):
         layer.launches_per_forward(0)
@@ -403,9 +405,10 @@ def test_step3_bf16_three_microbatches_sampled():
 
 
 def test_small_batch_router_logits_all_canonical():
-    """Up to 512 tokens the router computes every logit in the canonical order
-    (no tensor-core estimate): all T*E logits equal the oracle's bit for bit."""
-    c = synth.CONFIGS["qwen3_bf16"].with_batch(197, 2)
+    """Small batches (a router grid of at most three waves: up to 224 tokens with 128
+    experts) compute every logit in the canonical order with no tensor-core estimate: all
+    T*E logits equal the oracle's bit for bit.  T = 224 is the last batch on that path."""
+    c = synth.CONFIGS["qwen3_bf16"].with_batch(112, 2)
     layer, srcs, outs, r, ref = run_case(c, [c.B] * c.M)
     got = r["logits"].cpu().numpy().reshape(c.T, c.E)
     assert np.array_equal(got.view(np.uint32), ref["logits"].view(np.uint32))
