@@ -55,31 +55,33 @@ __device__ __forceinline__ int packed_rows(const int32_t* __restrict__ pos, int 
 // DeepSeek-V3 fp8 pack slower).
 constexpr int kPackGCopy = 8;
 constexpr int kPackGFp8 = 4;
+constexpr int kPackSmallChunks = 1024;  // up to this many 512-byte chunks: one chunk per unit
 
-// bf16 / fp32 layers: row copy.
+// bf16 / fp32 layers: row copy.  G chunks per unit; warps per block from the launch.
+template <int G>
 __global__ void __launch_bounds__(256) pack_copy_kernel(SrcTable st, const int32_t* __restrict__ pos, int T, int k,
                                                         int S, int row_bytes, uint8_t* __restrict__ P) {
   pdl_begin();
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, wpb = blockDim.x >> 5;
   const int nchunk = (row_bytes + 511) >> 9;  // 512 bytes per warp step
-  const int ngroup = (nchunk + kPackGCopy - 1) / kPackGCopy;
+  const int ngroup = (nchunk + G - 1) / G;
   const int nvec = row_bytes >> 4;
   const long units = (long)T * ngroup;
-  for (long u = (long)blockIdx.x * 8 + (threadIdx.x >> 5); u < units; u += (long)gridDim.x * 8) {
-    const int t = (int)(u / ngroup), c0 = (int)(u - (long)t * ngroup) * kPackGCopy;
+  for (long u = (long)blockIdx.x * wpb + (threadIdx.x >> 5); u < units; u += (long)gridDim.x * wpb) {
+    const int t = (int)(u / ngroup), c0 = (int)(u - (long)t * ngroup) * G;
     int rows[kMaxCopies];
     const int n = packed_rows(pos, t, T, k, S, rows);
     const uint4* src = reinterpret_cast<const uint4*>(src_row(st, t, row_bytes));
-    uint4 x[kPackGCopy];
+    uint4 x[G];
 #pragma unroll
-    for (int g = 0; g < kPackGCopy; ++g) {
+    for (int g = 0; g < G; ++g) {
       const int v = (c0 + g) * 32 + lane;
       if (v < nvec) x[g] = __ldg(src + v);
     }
     for (int q = 0; q < n; ++q) {
       uint4* dst = reinterpret_cast<uint4*>(P + (size_t)rows[q] * row_bytes);
 #pragma unroll
-      for (int g = 0; g < kPackGCopy; ++g) {
+      for (int g = 0; g < G; ++g) {
         const int v = (c0 + g) * 32 + lane;
         if (v < nvec) dst[v] = x[g];
       }
@@ -235,10 +237,21 @@ cudaError_t launch_pack(const SrcTable& st, const LayerDims& d, int T, Workspace
                                       static_cast<uint8_t*>(ws.P), ws.P_scale, ws.scale_ld);
       if (e_ != cudaSuccess) return e_;
     }
+  else if (T * ((row_bytes + 511) / 512) <= kPackSmallChunks)
+    {
+      // few tokens: one 512-byte chunk per unit and two warps per block, so the stores
+      // of the copies spread over many SMs instead of draining from a few (qwen3 shapes,
+      // 6 and 48 tokens: pack 10.2 -> 6.1 us; at 395 tokens and above this form was
+      // slower than 8-chunk units)
+      const int units = T * ((row_bytes + 511) / 512);
+      const cudaError_t e_ = launch_k(pack_copy_kernel<1>, dim3((units + 1) / 2), dim3(64), 0, s, st, ws.pos, T, d.k,
+                                      d.S, row_bytes, static_cast<uint8_t*>(ws.P));
+      if (e_ != cudaSuccess) return e_;
+    }
   else
     {
-      const cudaError_t e_ = launch_k(pack_copy_kernel, dim3(grid), dim3(256), 0, s, st, ws.pos, T, d.k, d.S,
-                                      row_bytes, static_cast<uint8_t*>(ws.P));
+      const cudaError_t e_ = launch_k(pack_copy_kernel<kPackGCopy>, dim3(grid), dim3(256), 0, s, st, ws.pos, T, d.k,
+                                      d.S, row_bytes, static_cast<uint8_t*>(ws.P));
       if (e_ != cudaSuccess) return e_;
     }
   return cudaGetLastError();

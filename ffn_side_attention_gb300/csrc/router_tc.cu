@@ -336,68 +336,73 @@ __device__ __forceinline__ float canonical_dot_xs(const uint4* xs, const uint16_
   return p;
 }
 
-__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
+// Order-preserving key of a float: larger value, larger key; +0 and -0 share one
+// key, as they compare equal.  Key 0 is below every value's key (that of -inf is
+// 0x007fffff) and marks an entry that is taken or absent.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t b = __float_as_uint(__fadd_rn(v, 0.0f));  // -0 + 0 = +0
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// warp-wide best (value desc, id asc) among this lane's untaken entries
+// Warp-wide best entry (value desc, id asc; entry q of lane l is id l + 32 q) among
+// the keys not yet 0: one max-reduction over the warp, then the lowest id holding
+// that key.  The entry's key is set to 0 (taken); returns its id.
 template <int PER>
-__device__ __forceinline__ void warp_best(const float (&v)[PER], const bool (&taken)[PER], int lane, float& bv,
-                                         int& bi) {
-  bv = 0.0f;
-  bi = 0x7fffffff;
+__device__ __forceinline__ int warp_take_best(uint32_t (&key)[PER], int lane) {
+  uint32_t best = 0;
 #pragma unroll
-  for (int q = 0; q < PER; ++q) {
-    const int e = lane + 32 * q;
-    if (!taken[q] && (bi == 0x7fffffff || ranks_before(v[q], e, bv, bi))) {
-      bv = v[q];
-      bi = e;
-    }
+  for (int q = 0; q < PER; ++q) best = max(best, key[q]);
+  const uint32_t w = __reduce_max_sync(0xffffffffu, best);
+  int bi = 0;
+#pragma unroll
+  for (int q = PER - 1; q >= 0; --q) {
+    const unsigned m = __ballot_sync(0xffffffffu, key[q] == w);
+    if (m) bi = 32 * q + __ffs(m) - 1;
   }
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-    if (oi != 0x7fffffff && (bi == 0x7fffffff || ranks_before(ov, oi, bv, bi))) {
-      bv = ov;
-      bi = oi;
-    }
-  }
+  for (int q = 0; q < PER; ++q)
+    if (lane + 32 * q == bi) key[q] = 0u;
+  return bi;
+}
+
+// value of entry e (warp-uniform) to every lane
+template <int PER>
+__device__ __forceinline__ float warp_value(const float (&v)[PER], int e) {
+  float x = v[0];
+#pragma unroll
+  for (int q = 1; q < PER; ++q)
+    if (q == (e >> 5)) x = v[q];
+  return __shfl_sync(0xffffffffu, x, e & 31);
 }
 
 // Top-k (value desc, id asc) among the entries not marked in tk, then the
-// softmax over the selected: lane 0 writes slots and weights of one token.
+// softmax over the selected: lane j writes slot j.  The exponentials are those
+// of one thread's loop over the slots and their sum runs in slot order.
 template <int PER>
-__device__ __forceinline__ void write_topk(const float (&lc)[PER], bool (&tk)[PER], int k, int lane,
+__device__ __forceinline__ void write_topk(const float (&lc)[PER], const bool (&tk)[PER], int k, int lane,
                                            int32_t* __restrict__ idx, float* __restrict__ wout) {
-  float sel_v[kMaxK];
-  int sel_i[kMaxK];
+  uint32_t key[PER];
 #pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
-    if (j >= k) break;
-    float bv;
-    int bi;
-    warp_best<PER>(lc, tk, lane, bv, bi);
-    sel_v[j] = bv;
-    sel_i[j] = bi;
-#pragma unroll
-    for (int q = 0; q < PER; ++q)
-      if (lane + 32 * q == bi) tk[q] = true;
+  for (int q = 0; q < PER; ++q) key[q] = tk[q] ? 0u : order_key(lc[q]);
+  float my_v = 0.0f;  // lane j: the j-th selected value and expert
+  int my_i = 0;
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) {
+    const int bi = warp_take_best<PER>(key, lane);
+    const float bv = warp_value<PER>(lc, bi);
+    if (lane == j) {
+      my_v = bv;
+      my_i = bi;
+    }
   }
-  if (lane == 0) {
-    float den = 0.0f, ex[kMaxK];
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      if (j >= k) break;
-      ex[j] = expf(sel_v[j] - sel_v[0]);
-      den += ex[j];
-    }
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      if (j >= k) break;
-      idx[j] = sel_i[j];
-      wout[j] = ex[j] / den;
-    }
+  const float v0 = __shfl_sync(0xffffffffu, my_v, 0);
+  const float ex = expf(my_v - v0);
+  float den = 0.0f;
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) den += __shfl_sync(0xffffffffu, ex, j);
+  if (lane < k) {
+    idx[lane] = my_i;
+    wout[lane] = ex / den;
   }
 }
 
@@ -466,18 +471,13 @@ __global__ void __launch_bounds__(256, MINB) router_select_warp_kernel(const Sel
   // m = k-th largest lower end
   float m = 0.0f;
   {
-    bool tk[PER];
+    uint32_t key[PER];
 #pragma unroll
-    for (int q = 0; q < PER; ++q) tk[q] = taken[q];
-    for (int j = 0; j < k; ++j) {
-      float bv;
-      int bi;
-      warp_best<PER>(lo, tk, lane, bv, bi);
-      m = bv;
-#pragma unroll
-      for (int q = 0; q < PER; ++q)
-        if (lane + 32 * q == bi) tk[q] = true;
-    }
+    for (int q = 0; q < PER; ++q) key[q] = taken[q] ? 0u : order_key(lo[q]);
+    int bi = 0;
+#pragma unroll 1
+    for (int j = 0; j < k; ++j) bi = warp_take_best<PER>(key, lane);
+    m = warp_value<PER>(lo, bi);
   }
   // candidates: upper end >= m
   unsigned cmask[PER];
@@ -585,25 +585,29 @@ __global__ void __launch_bounds__(256, MINB) router_select_warp_kernel(const Sel
 // ---------------------------------------------------------------- small batches
 // Few tokens: every logit in the canonical order, straight from the source
 // buffers, in one launch (no staging, no estimate).  Block = 8 warps = 8
-// tokens x one octet of experts: thread 0 copies the octet's 8 router rows
-// (contiguous in W_r) into shared memory with one bulk copy while every warp
-// loads its token's row into registers; lane l then runs the canonical chain
-// over chunks l, l+32, ... for the 8 experts at once (8 independent chains).
+// tokens x kOct experts (2, 4 or 8): thread 0 copies the block's kOct router
+// rows (contiguous in W_r) and its token rows into shared memory, bulk copies
+// on one barrier; lane l then runs the canonical chain over chunks l, l+32, ...
+// for the kOct experts at once (kOct independent chains).  The chunk loop
+// stays rolled: fully unrolled over a token row held in registers, the kernel
+// was slower (qwen3 shapes, 6 tokens: 20.5 -> 17.3 us per router launch with
+// this form).
 // The last warp to finish a token (atomic ticket per token) selects its top-k
 // from the stored logits and resets the ticket.
 constexpr int kSelWarps = 8;
-constexpr int kOct = 8;               // experts per block
+constexpr int kOctMax = 8;            // experts per block: 2, 4 or 8
 constexpr int kSmallMaxChunks = 28;   // H <= 7168: chunks of 8 channels per lane
 constexpr int kSmallMaxH = 32 * 8 * kSmallMaxChunks;
-constexpr int kSmallDynSmem = kOct * kSmallMaxH * 2;  // 112 KB
+constexpr int kSmallDynSmem = (kOctMax + kSelWarps) * kSmallMaxH * 2;  // 224 KB
 
+template <int kOct>
 __global__ void __launch_bounds__(32 * kSelWarps, 1)
     router_small_kernel(const SrcTable st, const uint16_t* __restrict__ wrT, const float* __restrict__ bias, int H,
                         int E, int k, float* __restrict__ logits, int32_t* __restrict__ topk_idx,
                         float* __restrict__ topk_w, int32_t* __restrict__ ticket, int* err) {
   pdl_begin();
   constexpr int PER = kPer;
-  extern __shared__ __align__(16) uint4 s_w[];  // [kOct][H/8]
+  extern __shared__ __align__(16) uint4 s_w[];  // [kOct][H/8] router rows, then [8][H/8] token rows
   __shared__ __align__(8) uint64_t bar;
   __shared__ int s_abort;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -615,40 +619,37 @@ __global__ void __launch_bounds__(32 * kSelWarps, 1)
     s_abort = 0;
     mbar_init(&bar, 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(&bar, (uint32_t)(ne * nc * 16));
+    const int tok0 = (blockIdx.x / noct) * kSelWarps, ntok = min(kSelWarps, st.T - tok0);
+    mbar_arrive_expect_tx(&bar, (uint32_t)((ne + ntok) * nc * 16));
     bulk_load(s_w, reinterpret_cast<const uint4*>(wrT) + (size_t)e0 * nc, (uint32_t)(ne * nc * 16), &bar);
+    for (int w = 0; w < ntok; ++w) {
+      const int tw = tok0 + w, m = src_of_token(st, tw);
+      bulk_load(s_w + (size_t)(kOct + w) * nc, reinterpret_cast<const uint4*>(st.src[m]) + (size_t)(tw - st.row0[m]) * nc,
+                (uint32_t)(nc * 16), &bar);
+    }
   }
-  const int t = (blockIdx.x / noct) * kSelWarps + warp;
+  const int tok0 = (blockIdx.x / noct) * kSelWarps;
+  const int t = tok0 + warp;
   const bool valid = t < st.T;
-  uint4 xr[kSmallMaxChunks];
-  if (valid) {
-    const int m = src_of_token(st, t);
-    const uint4* x = reinterpret_cast<const uint4*>(st.src[m]) + (size_t)(t - st.row0[m]) * nc;
-#pragma unroll
-    for (int j = 0; j < kSmallMaxChunks; ++j)
-      if (lane + 32 * j < nc) xr[j] = __ldg(x + lane + 32 * j);
-  }
-  __syncthreads();  // barrier initialised before anyone waits on it
-  const bool ok = mbar_wait(&bar, 0, &s_abort, err);  // every thread: the copy lands before the block exits
-  if (!valid || !ok) return;
   float p[kOct];
 #pragma unroll
   for (int i = 0; i < kOct; ++i) p[i] = 0.0f;
+  __syncthreads();  // barrier initialised before anyone waits on it
+  const bool ok = mbar_wait(&bar, 0, &s_abort, err);  // every thread: the copies land before the block exits
+  if (!valid || !ok) return;
+  const uint4* xs = s_w + (size_t)(kOct + warp) * nc;
+#pragma unroll 2
+  for (int c = lane; c < nc; c += 32) {
+    const uint4 a = xs[c];
 #pragma unroll
-  for (int j = 0; j < kSmallMaxChunks; ++j) {
-    const int c = lane + 32 * j;
-    if (c < nc) {
-      const uint4 a = xr[j];
-#pragma unroll
-      for (int i = 0; i < kOct; ++i)
-        if (i < ne) {
-          const uint4 b = s_w[i * nc + c];
-          p[i] = fma_bf16_lo(a.x, b.x, p[i]); p[i] = fma_bf16_hi(a.x, b.x, p[i]);
-          p[i] = fma_bf16_lo(a.y, b.y, p[i]); p[i] = fma_bf16_hi(a.y, b.y, p[i]);
-          p[i] = fma_bf16_lo(a.z, b.z, p[i]); p[i] = fma_bf16_hi(a.z, b.z, p[i]);
-          p[i] = fma_bf16_lo(a.w, b.w, p[i]); p[i] = fma_bf16_hi(a.w, b.w, p[i]);
-        }
-    }
+    for (int i = 0; i < kOct; ++i)
+      if (i < ne) {
+        const uint4 b = s_w[i * nc + c];
+        p[i] = fma_bf16_lo(a.x, b.x, p[i]); p[i] = fma_bf16_hi(a.x, b.x, p[i]);
+        p[i] = fma_bf16_lo(a.y, b.y, p[i]); p[i] = fma_bf16_hi(a.y, b.y, p[i]);
+        p[i] = fma_bf16_lo(a.z, b.z, p[i]); p[i] = fma_bf16_hi(a.z, b.z, p[i]);
+        p[i] = fma_bf16_lo(a.w, b.w, p[i]); p[i] = fma_bf16_hi(a.w, b.w, p[i]);
+      }
   }
   float v = 0.0f;
 #pragma unroll
@@ -703,7 +704,11 @@ cudaError_t router_tc_setup() {
   e = cudaFuncSetAttribute(router_select_warp_kernel<3, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSelXsMaxBytes);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmallDynSmem);
+  for (auto f : {router_small_kernel<2>, router_small_kernel<4>, router_small_kernel<8>}) {
+    e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmallDynSmem);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_router_wnorm(const void* wrT, int H, int E, float* wnorm, cudaStream_t s) {
@@ -722,8 +727,18 @@ int router_tc_splits(const LayerDims& d, int T, int num_sms) {
   return splits;
 }
 
+// Experts per small-router block: the fewest that keep the grid within one wave.  Each
+// warp's chains get shorter with fewer experts, and more SMs share the router rows
+// (qwen3 shapes, 6 tokens: 2 experts per block, router 17.4 -> 13.9 us).
+static int small_oct(const LayerDims& d, int T, int num_sms) {
+  const int tg = (T + kSelWarps - 1) / kSelWarps;
+  for (int o = 2; o < kOctMax; o *= 2)
+    if ((long)((d.E + o - 1) / o) * tg <= num_sms) return o;
+  return kOctMax;
+}
+
 static bool router_small_path(const LayerDims& d, int T, int num_sms) {
-  const int noct = (d.E + kOct - 1) / kOct;
+  const int noct = (d.E + kOctMax - 1) / kOctMax;
   return (long)noct * ((T + kSelWarps - 1) / kSelWarps) <= (long)kSmallRouterWaves * num_sms && d.H <= kSmallMaxH;
 }
 
@@ -735,10 +750,12 @@ cudaError_t launch_router_tc(const SrcTable& st, const void* wrT, const float* b
   const int T = st.T;
   if (T == 0) return cudaSuccess;
   if (router_small_path(d, T, num_sms)) {
-    const int noct = (d.E + kOct - 1) / kOct;
+    const int oct = small_oct(d, T, num_sms);
+    const int noct = (d.E + oct - 1) / oct;
+    auto kern = oct == 2 ? router_small_kernel<2> : (oct == 4 ? router_small_kernel<4> : router_small_kernel<8>);
     {
-      const cudaError_t e_ = launch_k(router_small_kernel, dim3(noct * ((T + kSelWarps - 1) / kSelWarps)),
-                                      dim3(32 * kSelWarps), (size_t)kOct * d.H * 2, s, st,
+      const cudaError_t e_ = launch_k(kern, dim3(noct * ((T + kSelWarps - 1) / kSelWarps)),
+                                      dim3(32 * kSelWarps), (size_t)(oct + kSelWarps) * d.H * 2, s, st,
                                       static_cast<const uint16_t*>(wrT), bias, d.H, d.E, d.k, ws.logits,
                                       ws.topk_idx, ws.topk_w, ws.tok_ticket, ws.err);
       if (e_ != cudaSuccess) return e_;
