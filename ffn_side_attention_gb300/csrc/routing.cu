@@ -92,6 +92,46 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
   return v;
 }
 
+// Exclusive scans of the group counts into row offsets and GEMM tile bases (BN tokens
+// per tile), by a whole block of kTok threads: one group per thread, warp scans, then
+// the warp totals (integer sums, so the order does not matter).  A group past the
+// block's threads (G = 257) is added last by the last thread.  Ends with a barrier.
+__device__ __forceinline__ void scan_groups(const int* s_cnt, int G, int BN, int* s_off, int* s_tb) {
+  __shared__ int s_wo[kWarpsPerBlock], s_wt[kWarpsPerBlock];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = threadIdx.x;
+  const int c = (g < G) ? s_cnt[g] : 0;
+  const int nt = (c + BN - 1) / BN;
+  const int io = warp_incl_scan(c, lane);
+  const int it = warp_incl_scan(nt, lane);
+  if (lane == 31) {
+    s_wo[warp] = io;
+    s_wt[warp] = it;
+  }
+  __syncthreads();
+  int po = 0, pt = 0;
+  for (int w = 0; w < warp; ++w) {
+    po += s_wo[w];
+    pt += s_wt[w];
+  }
+  if (g < G) {
+    s_off[g] = po + io - c;
+    s_tb[g] = pt + it - nt;
+  }
+  if (threadIdx.x == kTok - 1) {
+    int to = po + io, tt = pt + it;
+    for (int x = kTok; x < G; ++x) {
+      s_off[x] = to;
+      s_tb[x] = tt;
+      to += s_cnt[x];
+      tt += (s_cnt[x] + BN - 1) / BN;
+    }
+    s_off[G] = to;
+    s_tb[G] = tt;
+  }
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(kTok)
     place_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ block_hist, int nblocks, int T, int k,
                  int E, int S, int BN, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
@@ -100,7 +140,6 @@ __global__ void __launch_bounds__(kTok)
   pdl_begin();
   __shared__ int s_cnt[kMaxExperts + 1], s_base[kMaxExperts], s_off[kMaxExperts + 1], s_tb[kMaxExperts + 1];
   const int G = E + S;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int e = threadIdx.x; e < E; e += kTok) {
     int before = 0, total = 0;
     for (int b = 0; b < nblocks; ++b) {
@@ -113,28 +152,7 @@ __global__ void __launch_bounds__(kTok)
   }
   if (threadIdx.x == 0 && S) s_cnt[E] = T;
   __syncthreads();
-  // exclusive scans over the groups (warp 0): offsets and GEMM tile bases
-  if (warp == 0) {
-    int carry_o = 0, carry_t = 0;
-    for (int g0 = 0; g0 < G; g0 += 32) {
-      const int g = g0 + lane;
-      const int c = (g < G) ? s_cnt[g] : 0;
-      const int nt = (c + BN - 1) / BN;
-      const int io = warp_incl_scan(c, lane);
-      const int it = warp_incl_scan(nt, lane);
-      if (g < G) {
-        s_off[g] = carry_o + io - c;
-        s_tb[g] = carry_t + it - nt;
-      }
-      carry_o += __shfl_sync(0xffffffffu, io, 31);
-      carry_t += __shfl_sync(0xffffffffu, it, 31);
-    }
-    if (lane == 0) {
-      s_off[G] = carry_o;
-      s_tb[G] = carry_t;
-    }
-  }
-  __syncthreads();
+  scan_groups(s_cnt, G, BN, s_off, s_tb);
   if (blockIdx.x == 0)
     for (int g = threadIdx.x; g <= G; g += kTok) {
       offsets[g] = s_off[g];
@@ -196,27 +214,7 @@ __global__ void __launch_bounds__(kTok)
   }
   if (threadIdx.x == 0 && S) s_cnt[E] = T;
   __syncthreads();
-  if (warp == 0) {  // exclusive scans over the groups: offsets and GEMM tile bases
-    int carry_o = 0, carry_t = 0;
-    for (int g0 = 0; g0 < G; g0 += 32) {
-      const int g = g0 + lane;
-      const int c = (g < G) ? s_cnt[g] : 0;
-      const int nt = (c + BN - 1) / BN;
-      const int io = warp_incl_scan(c, lane);
-      const int it = warp_incl_scan(nt, lane);
-      if (g < G) {
-        s_off[g] = carry_o + io - c;
-        s_tb[g] = carry_t + it - nt;
-      }
-      carry_o += __shfl_sync(0xffffffffu, io, 31);
-      carry_t += __shfl_sync(0xffffffffu, it, 31);
-    }
-    if (lane == 0) {
-      s_off[G] = carry_o;
-      s_tb[G] = carry_t;
-    }
-  }
-  __syncthreads();
+  scan_groups(s_cnt, G, BN, s_off, s_tb);
   for (int g = threadIdx.x; g <= G; g += kTok) {
     offsets[g] = s_off[g];
     tile_base[g] = s_tb[g];
