@@ -42,7 +42,6 @@ namespace {
 
 constexpr int kMaxK = 16;
 constexpr int kMaxCand = 64;
-constexpr int kPer = 8;  // router entries per lane: E <= 256 routed experts
 constexpr int kSmallRouterWaves = 3;  // small-batch path while its grid is at most this many waves
 
 // ---------------------------------------------------------------- 1. stage
@@ -432,10 +431,13 @@ struct SelectArgs {
 // launcher takes 3 only when that turns a second wave into none).  XS: each
 // warp first copies its token row into shared memory, so the candidate dots
 // read only the expert rows from L2 (the row is reused by every candidate).
-template <int MINB, bool XS>
+// PER = entries per lane (E <= 32 PER): the selection rounds and the candidate
+// bookkeeping cost instructions per entry, and with a whole wave of warps on the
+// SMs the kernel is bound by instruction issue (T=3160: 58 -> 50 us with PER = 4
+// instead of 8 for 128 experts, and the split partials loaded four splits at a time).
+template <int MINB, bool XS, int PER>
 __global__ void __launch_bounds__(256, MINB) router_select_warp_kernel(const SelectArgs a) {
   pdl_begin();
-  constexpr int PER = kPer;
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= a.T) return;
@@ -452,17 +454,39 @@ __global__ void __launch_bounds__(256, MINB) router_select_warp_kernel(const Sel
   float* lrow = a.logits + (size_t)t * E;
   float lo[PER], hi[PER];  // bounds of the estimate (the estimate itself goes to the logits row now)
   bool taken[PER];
+  float est[PER], wn[PER], bs[PER];
 #pragma unroll
   for (int q = 0; q < PER; ++q) {
     const int e = lane + 32 * q;
     taken[q] = e >= E;
+    est[q] = 0.0f;
+    wn[q] = taken[q] ? 0.0f : __ldg(a.wnorm + e);
+    bs[q] = (taken[q] || !a.bias) ? 0.0f : __ldg(a.bias + e);
+  }
+  // the split partials, four splits of every group in flight at once; each sum in split order
+  for (int sp0 = 0; sp0 < a.splits; sp0 += 4) {
+    float pv[4][PER];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int q = 0; q < PER; ++q)
+        pv[u][q] = (sp0 + u < a.splits && !taken[q])
+                       ? __ldcg(a.part + ((size_t)(sp0 + u) * a.T + t) * E + lane + 32 * q)
+                       : 0.0f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int q = 0; q < PER; ++q)
+        if (sp0 + u < a.splits) est[q] += pv[u][q];
+  }
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int e = lane + 32 * q;
     lo[q] = hi[q] = 0.0f;
     if (e < E) {
-      float s = 0.0f;
-      for (int sp = 0; sp < a.splits; ++sp) s += __ldcg(a.part + ((size_t)sp * a.T + t) * E + e);
-      const float bs = a.bias ? __ldg(a.bias + e) : 0.0f;
-      if (a.bias) s = __fadd_rn(s, bs);
-      const float b = a.g * xn * __ldg(a.wnorm + e) + 0x1p-22f * (fabsf(s) + fabsf(bs)) + 0x1p-100f;
+      float s = est[q];
+      if (a.bias) s = __fadd_rn(s, bs[q]);
+      const float b = a.g * xn * wn[q] + 0x1p-22f * (fabsf(s) + fabsf(bs[q])) + 0x1p-100f;
       lrow[e] = s;  // replaced by the canonical value below if e is a candidate
       lo[q] = s - b;
       hi[q] = s + b;
@@ -600,13 +624,12 @@ constexpr int kSmallMaxChunks = 28;   // H <= 7168: chunks of 8 channels per lan
 constexpr int kSmallMaxH = 32 * 8 * kSmallMaxChunks;
 constexpr int kSmallDynSmem = (kOctMax + kSelWarps) * kSmallMaxH * 2;  // 224 KB
 
-template <int kOct>
+template <int kOct, int PER>
 __global__ void __launch_bounds__(32 * kSelWarps, 1)
     router_small_kernel(const SrcTable st, const uint16_t* __restrict__ wrT, const float* __restrict__ bias, int H,
                         int E, int k, float* __restrict__ logits, int32_t* __restrict__ topk_idx,
                         float* __restrict__ topk_w, int32_t* __restrict__ ticket, int* err) {
   pdl_begin();
-  constexpr int PER = kPer;
   extern __shared__ __align__(16) uint4 s_w[];  // [kOct][H/8] router rows, then [8][H/8] token rows
   __shared__ __align__(8) uint64_t bar;
   __shared__ int s_abort;
@@ -698,17 +721,33 @@ __global__ void wnorm_kernel(const uint16_t* __restrict__ wrT, int H, int E, flo
 cudaError_t router_tc_setup() {
   cudaError_t e = cudaFuncSetAttribute(router_logits_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRDynSmem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(router_select_warp_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSelXsMaxBytes);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(router_select_warp_kernel<3, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSelXsMaxBytes);
-  if (e != cudaSuccess) return e;
-  for (auto f : {router_small_kernel<2>, router_small_kernel<4>, router_small_kernel<8>}) {
+  for (auto f : {router_select_warp_kernel<2, true, 2>, router_select_warp_kernel<3, true, 2>,
+                 router_select_warp_kernel<2, true, 4>, router_select_warp_kernel<3, true, 4>,
+                 router_select_warp_kernel<2, true, 8>, router_select_warp_kernel<3, true, 8>}) {
+    e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelXsMaxBytes);
+    if (e != cudaSuccess) return e;
+  }
+  for (auto f : {router_small_kernel<2, 2>, router_small_kernel<4, 2>, router_small_kernel<8, 2>,
+                 router_small_kernel<2, 4>, router_small_kernel<4, 4>, router_small_kernel<8, 4>,
+                 router_small_kernel<2, 8>, router_small_kernel<4, 8>, router_small_kernel<8, 8>}) {
     e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmallDynSmem);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+// entries per lane of the selection: E <= 32 * PER
+static int router_per(int E) { return E <= 64 ? 2 : (E <= 128 ? 4 : 8); }
+
+template <int PER>
+static void (*select_kernel(bool three, bool xs))(const SelectArgs) {
+  return three ? (xs ? router_select_warp_kernel<3, true, PER> : router_select_warp_kernel<3, false, PER>)
+               : (xs ? router_select_warp_kernel<2, true, PER> : router_select_warp_kernel<2, false, PER>);
+}
+
+template <int kOct>
+static auto small_kernel(int per) {
+  return per == 2 ? router_small_kernel<kOct, 2> : (per == 4 ? router_small_kernel<kOct, 4> : router_small_kernel<kOct, 8>);
 }
 
 cudaError_t launch_router_wnorm(const void* wrT, int H, int E, float* wnorm, cudaStream_t s) {
@@ -752,7 +791,8 @@ cudaError_t launch_router_tc(const SrcTable& st, const void* wrT, const float* b
   if (router_small_path(d, T, num_sms)) {
     const int oct = small_oct(d, T, num_sms);
     const int noct = (d.E + oct - 1) / oct;
-    auto kern = oct == 2 ? router_small_kernel<2> : (oct == 4 ? router_small_kernel<4> : router_small_kernel<8>);
+    const int per = router_per(d.E);
+    auto kern = oct == 2 ? small_kernel<2>(per) : (oct == 4 ? small_kernel<4>(per) : small_kernel<8>(per));
     {
       const cudaError_t e_ = launch_k(kern, dim3(noct * ((T + kSelWarps - 1) / kSelWarps)),
                                       dim3(32 * kSelWarps), (size_t)(oct + kSelWarps) * d.H * 2, s, st,
@@ -807,8 +847,9 @@ cudaError_t launch_router_tc(const SrcTable& st, const void* wrT, const float* b
   const size_t xs_bytes = (size_t)kSelWarps * d.H * 2;
   const bool xs = xs_bytes <= (size_t)kSelXsMaxBytes;
   const bool three = blocks > 2 * num_sms && blocks <= 3 * num_sms && (!xs || 3 * xs_bytes <= kSelXsThreeBytes);
-  void (*kern)(const SelectArgs) = three ? (xs ? router_select_warp_kernel<3, true> : router_select_warp_kernel<3, false>)
-                                         : (xs ? router_select_warp_kernel<2, true> : router_select_warp_kernel<2, false>);
+  const int per = router_per(d.E);
+  void (*kern)(const SelectArgs) =
+      per == 2 ? select_kernel<2>(three, xs) : (per == 4 ? select_kernel<4>(three, xs) : select_kernel<8>(three, xs));
   {
     const cudaError_t e_ = launch_k(kern, dim3(blocks), dim3(32 * kSelWarps), xs ? xs_bytes : 0, s, sa);
     if (e_ != cudaSuccess) return e_;
