@@ -164,7 +164,8 @@ __global__ void __launch_bounds__(256) combine_bf16_kernel(SrcTable st, const in
   // Y rows are read once: loaded evict-first, so the rows the down GEMM left in L2 stay
   // there until their own reader comes (measured: T=3160 combine 44 -> 37.6 us)
   const uint64_t pol = l2_policy_evict_first();
-  for (long u = (long)blockIdx.x * 8 + (threadIdx.x >> 5); u < units; u += (long)gridDim.x * 8) {
+  const int wpb = blockDim.x >> 5;
+  for (long u = (long)blockIdx.x * wpb + (threadIdx.x >> 5); u < units; u += (long)gridDim.x * wpb) {
     const int t = (int)(u / nchunk), c = (int)(u - (long)t * nchunk);
     const int v = c * 32 + lane;
     float acc[8];
@@ -260,27 +261,32 @@ cudaError_t launch_pack(const SrcTable& st, const LayerDims& d, int T, Workspace
 cudaError_t launch_combine(const SrcTable& st, const LayerDims& d, int T, Workspace& ws, int num_sms,
                            cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const int grid = grid_for(8, d.dtype == AFD_FP32 ? T : T * (d.H / 256), num_sms);
+  const int units = d.dtype == AFD_FP32 ? T : T * (d.H / 256);
+  // few tokens: two warps per block, so the k row reads of the units spread over more SMs
+  // (qwen3 shapes: T = 6 step 0.2361 -> 0.2352 ms, T = 24 0.5495 -> 0.5465 ms)
+  const bool small = d.dtype != AFD_FP32 && units <= kPackSmallChunks;
+  const int grid = small ? (units + 1) / 2 : grid_for(8, units, num_sms);
+  const dim3 blk(small ? 64 : 256);
   const uint16_t* Y = static_cast<const uint16_t*>(ws.Y);
-  const int early = grid <= num_sms * 8;  // one wave of 8 resident blocks per SM
+  const int early = small || grid <= num_sms * 8;  // one wave of 8 resident blocks per SM
   if (d.dtype == AFD_FP32)
     return launch_k(combine_f32_kernel, dim3(grid), dim3(256), 0, s, st, ws.pos, ws.topk_w,
                     static_cast<const float*>(ws.Y), T, d.k, d.S, d.H);
   switch (d.k) {  // k known at compile time keeps a unit's k row loads in flight together
     case 1:
-      return launch_k(combine_bf16_kernel<1>, dim3(grid), dim3(256), 0, s, st, ws.pos, ws.topk_w, Y, T, d.k, d.S, d.H, early);
+      return launch_k(combine_bf16_kernel<1>, dim3(grid), blk, 0, s, st, ws.pos, ws.topk_w, Y, T, d.k, d.S, d.H, early);
     case 2:
-      return launch_k(combine_bf16_kernel<2>, dim3(grid), dim3(256), 0, s, st, ws.pos, ws.topk_w, Y, T, d.k, d.S, d.H, early);
+      return launch_k(combine_bf16_kernel<2>, dim3(grid), blk, 0, s, st, ws.pos, ws.topk_w, Y, T, d.k, d.S, d.H, early);
     case 3:
-      return launch_k(combine_bf16_kernel<3>, dim3(grid), dim3(256), 0, s, st, ws.pos, ws.topk_w, Y, T, d.k, d.S, d.H, early);
+      return launch_k(combine_bf16_kernel<3>, dim3(grid), blk, 0, s, st, ws.pos, ws.topk_w, Y, T, d.k, d.S, d.H, early);
     case 4:
-      return launch_k(combine_bf16_kernel<4>, dim3(grid), dim3(256), 0, s, st, ws.pos, ws.topk_w, Y, T, d.k, d.S, d.H, early);
+      return launch_k(combine_bf16_kernel<4>, dim3(grid), blk, 0, s, st, ws.pos, ws.topk_w, Y, T, d.k, d.S, d.H, early);
     case 6:
-      return launch_k(combine_bf16_kernel<6>, dim3(grid), dim3(256), 0, s, st, ws.pos, ws.topk_w, Y, T, d.k, d.S, d.H, early);
+      return launch_k(combine_bf16_kernel<6>, dim3(grid), blk, 0, s, st, ws.pos, ws.topk_w, Y, T, d.k, d.S, d.H, early);
     case 8:
-      return launch_k(combine_bf16_kernel<8>, dim3(grid), dim3(256), 0, s, st, ws.pos, ws.topk_w, Y, T, d.k, d.S, d.H, early);
+      return launch_k(combine_bf16_kernel<8>, dim3(grid), blk, 0, s, st, ws.pos, ws.topk_w, Y, T, d.k, d.S, d.H, early);
     default:
-      return launch_k(combine_bf16_kernel<0>, dim3(grid), dim3(256), 0, s, st, ws.pos, ws.topk_w, Y, T, d.k, d.S, d.H, early);
+      return launch_k(combine_bf16_kernel<0>, dim3(grid), blk, 0, s, st, ws.pos, ws.topk_w, Y, T, d.k, d.S, d.H, early);
   }
 }
 

@@ -58,15 +58,22 @@ __global__ void __launch_bounds__(kTok) block_rank_kernel(const int32_t* __restr
   for (int i = threadIdx.x; i < kWarpsPerBlock * E; i += kTok) bits[i] = 0;
   __syncthreads();
   uint32_t* my = bits + warp * E;
-  if (t < T)
-    for (int j = 0; j < k; ++j) {
-      const int e = __ldg(idx + (size_t)t * k + j);
-      if (e < 0 || e >= E) {
-        atomicOr(err, kErrRange);
-        continue;
-      }
-      atomicOr(my + e, 1u << lane);
+  // this token's experts, all loaded before any use (a load per slot in a loop over k
+  // serialised the round trips: T = 3160 routing 16.7 -> 15.4 us with this and the batched
+  // loads of place_kernel)
+  int ex[kRouteMaxK];
+#pragma unroll
+  for (int j = 0; j < kRouteMaxK; ++j) ex[j] = (j < k && t < T) ? __ldg(idx + (size_t)t * k + j) : -1;
+#pragma unroll
+  for (int j = 0; j < kRouteMaxK; ++j) {
+    if (j >= k || t >= T) break;
+    if (ex[j] < 0 || ex[j] >= E) {
+      atomicOr(err, kErrRange);
+      ex[j] = -1;
+    } else {
+      atomicOr(my + ex[j], 1u << lane);
     }
+  }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += kTok) {
     int total = 0;
@@ -75,13 +82,13 @@ __global__ void __launch_bounds__(kTok) block_rank_kernel(const int32_t* __restr
   }
   if (t < T) {
     const uint32_t lower = (1u << lane) - 1u;
-    for (int j = 0; j < k; ++j) {
-      const int e = __ldg(idx + (size_t)t * k + j);
-      if (e < 0 || e >= E) continue;
-      int r = __popc(my[e] & lower);
-      for (int w = 0; w < warp; ++w) r += __popc(bits[w * E + e]);
-      rank[(size_t)t * k + j] = r;
-    }
+#pragma unroll
+    for (int j = 0; j < kRouteMaxK; ++j)
+      if (ex[j] >= 0) {
+        int r = __popc(my[ex[j]] & lower);
+        for (int w = 0; w < warp; ++w) r += __popc(bits[w * E + ex[j]]);
+        rank[(size_t)t * k + j] = r;
+      }
   }
 }
 
@@ -145,10 +152,15 @@ __global__ void __launch_bounds__(kTok)
   const int G = E + S;
   for (int e = threadIdx.x; e < E; e += kTok) {
     int before = 0, total = 0;
-    for (int b = 0; b < nblocks; ++b) {
-      const int c = __ldg(block_hist + (size_t)b * E + e);
-      if (b < (int)blockIdx.x) before += c;
-      total += c;
+    for (int b0 = 0; b0 < nblocks; b0 += 16) {  // sixteen blocks' counts in flight at once
+      int c[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) c[u] = b0 + u < nblocks ? __ldg(block_hist + (size_t)(b0 + u) * E + e) : 0;
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        if (b0 + u < (int)blockIdx.x) before += c[u];
+        total += c[u];
+      }
     }
     s_cnt[e] = total;
     s_base[e] = before;
@@ -167,12 +179,18 @@ __global__ void __launch_bounds__(kTok)
     }
   const int t = blockIdx.x * kTok + threadIdx.x;
   if (t < T) {
-    for (int j = 0; j < k; ++j) {
-      const size_t i = (size_t)t * k + j;
-      const int e = __ldg(idx + i);
-      if (e < 0 || e >= E) continue;
-      const int row = s_off[e] + s_base[e] + pos[i];  // pos holds the in-block rank
-      pos[i] = row;
+    int ex[kRouteMaxK], rk[kRouteMaxK];  // experts and in-block ranks, all loaded before any use
+#pragma unroll
+    for (int j = 0; j < kRouteMaxK; ++j) {
+      ex[j] = j < k ? __ldg(idx + (size_t)t * k + j) : -1;
+      rk[j] = j < k ? pos[(size_t)t * k + j] : 0;  // pos holds the in-block rank
+    }
+#pragma unroll
+    for (int j = 0; j < kRouteMaxK; ++j) {
+      const int e = ex[j];
+      if (j >= k || e < 0 || e >= E) continue;
+      const int row = s_off[e] + s_base[e] + rk[j];
+      pos[(size_t)t * k + j] = row;
       perm[row] = t;
     }
     if (S) perm[(size_t)T * k + t] = t;
