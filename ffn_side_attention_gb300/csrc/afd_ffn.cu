@@ -46,6 +46,11 @@ struct afd_ffn {
   float* wd32 = nullptr;    // fp32 layer: [(E+S), I, H]
   CUtensorMap tm_wg{}, tm_wu{}, tm_wd{};
   Workspace ws[AFD_MAX_MICRO];
+  // tensor maps of each workspace's last sources (the tensor-core router reads its token
+  // tiles through them); re-encoded when a source pointer or row count changes
+  afd::SrcMaps src_maps[AFD_MAX_MICRO];
+  const void* map_src[AFD_MAX_MICRO][AFD_MAX_SOURCES] = {};
+  int map_rows[AFD_MAX_MICRO][AFD_MAX_SOURCES] = {};
   cudaStream_t mstream[AFD_MAX_MICRO] = {};
   cudaEvent_t ev_fork = nullptr;
   cudaEvent_t ev_join[AFD_MAX_MICRO] = {};
@@ -154,12 +159,8 @@ int alloc_workspace(afd_ffn* h, Workspace& ws) {
       return rc;
     ws.scale_ld = (int)R;
   }
-  if (c.dtype != AFD_FP32) {
-    if ((rc = dmalloc(h, &ws.Xc, T * c.H * 2)) || (rc = dmalloc_t(h, &ws.xnorm, T)) ||
-        (rc = dmalloc_t(h, &ws.rpart, (size_t)afd::kRouterMaxSplits * T * E)))
-      return rc;
-    CUDA_TRY(h, cudaMemset(ws.Xc, 0, T * c.H * 2));
-  }
+  if (c.dtype != AFD_FP32)
+    if ((rc = dmalloc_t(h, &ws.rpart, (size_t)afd::kRouterMaxSplits * T * E))) return rc;
   CUDA_TRY(h, cudaMemset(ws.tile_counter, 0, sizeof(int32_t) * ((T + afd::kRouterTokTile - 1) / afd::kRouterTokTile)));
   CUDA_TRY(h, cudaMemset(ws.err, 0, sizeof(int)));
   CUDA_TRY(h, cudaMemset(ws.tok_ticket, 0, sizeof(int32_t) * T));
@@ -167,8 +168,7 @@ int alloc_workspace(afd_ffn* h, Workspace& ws) {
   CUDA_TRY(h, cudaMemset(ws.Hb, 0, R * c.I * (c.dtype == AFD_FP8_E4M3 ? 1 : act_bytes(c))));
   if (c.dtype != AFD_FP32) {
     const bool fp8 = c.dtype == AFD_FP8_E4M3;
-    if (!make_map(&ws.tm_P, ws.P, fp8, c.H, R, 32) || !make_map(&ws.tm_H, ws.Hb, fp8, c.I, R, 32) ||
-        !make_map(&ws.tm_X, ws.Xc, false, c.H, T, 128))
+    if (!make_map(&ws.tm_P, ws.P, fp8, c.H, R, 32) || !make_map(&ws.tm_H, ws.Hb, fp8, c.I, R, 32))
       return fail(h, AFD_ECUDA, "cuTensorMapEncodeTiled failed for a workspace operand");
   }
   ws.ready = true;
@@ -178,7 +178,7 @@ int alloc_workspace(afd_ffn* h, Workspace& ws) {
 void free_workspace(Workspace& ws) {
   void* ptrs[] = {ws.topk_idx, ws.topk_w, ws.logits, ws.tile_counter, ws.tok_ticket, ws.counts, ws.offsets, ws.tile_base,
                   ws.block_hist, ws.perm, ws.pos, ws.P, ws.P_scale, ws.Hb, ws.H_scale, ws.Y, ws.err,
-                  ws.stage, ws.Xc, ws.xnorm, ws.rpart};
+                  ws.stage, ws.rpart};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   ws = Workspace{};
@@ -267,6 +267,20 @@ struct NvtxRange {
   NvtxRange& operator=(const NvtxRange&) = delete;
 };
 
+// Tensor maps of the sources of st for workspace wi (bf16 [rows, H], 128-row boxes),
+// encoded again only where a pointer or row count changed since the last forward.
+int update_src_maps(afd_ffn* h, int wi, const SrcTable& st) {
+  for (int m = 0; m < st.M; ++m) {
+    const int rows = st.row0[m + 1] - st.row0[m];
+    if (rows == 0 || (h->map_src[wi][m] == st.src[m] && h->map_rows[wi][m] == rows)) continue;
+    if (!make_map(&h->src_maps[wi].m[m], const_cast<void*>(st.src[m]), false, h->cfg.H, rows, 128))
+      return fail(h, AFD_ECUDA, "cuTensorMapEncodeTiled failed for source %d", m);
+    h->map_src[wi][m] = st.src[m];
+    h->map_rows[wi][m] = rows;
+  }
+  return AFD_OK;
+}
+
 int run_layer(afd_ffn* h, const SrcTable& st, Workspace& ws, cudaStream_t s) {
   const LayerDims& d = h->dims;
   const int T = st.T;
@@ -281,7 +295,12 @@ int run_layer(afd_ffn* h, const SrcTable& st, Workspace& ws, cudaStream_t s) {
     if (d.dtype == AFD_FP32)
       CUDA_TRY(h, afd::launch_router(st, h->wrT, h->bias, d, ws, s));
     else
-      CUDA_TRY(h, afd::launch_router_tc(st, h->wrT, h->bias, h->wnorm, &h->tm_wr, d, ws, h->num_sms, s));
+    {
+      const int wi = (int)(&ws - h->ws);
+      if (afd::router_tc_launches(d, T, h->num_sms) > 1 && (rc = update_src_maps(h, wi, st))) return rc;
+      CUDA_TRY(h, afd::launch_router_tc(st, h->src_maps[wi], h->wrT, h->bias, h->wnorm, &h->tm_wr, d, ws,
+                                        h->num_sms, s));
+    }
   }
   if ((rc = prof_mark(h, 1, s))) return rc;
   {

@@ -45,6 +45,12 @@ __device__ __forceinline__ int src_of_token(const SrcTable& s, int t) {
   return lo;
 }
 
+// token t's row in its source buffer
+__device__ __forceinline__ const uint8_t* src_row(const SrcTable& st, int t, size_t row_bytes) {
+  const int m = src_of_token(st, t);
+  return reinterpret_cast<const uint8_t*>(st.src[m]) + (size_t)(t - st.row0[m]) * row_bytes;
+}
+
 // ---------------------------------------------------------------- workspace
 struct Workspace {
   int32_t* topk_idx = nullptr;  // [maxT*k]
@@ -68,10 +74,7 @@ struct Workspace {
   void* Y = nullptr;            // [max_rows, H] weighted expert outputs
   int* err = nullptr;           // device error word
   void* stage = nullptr;        // forward_host staging: [maxT, H] in + [maxT, H] out
-  void* Xc = nullptr;           // [maxT, H] bf16 token rows, contiguous (tensor-core router)
-  float* xnorm = nullptr;       // [maxT] ||x_t||_2 rounded up
   float* rpart = nullptr;       // [kRouterMaxSplits][maxT][E] router logit partials
-  CUtensorMap tm_X;
   int last_T = 0;
   CUtensorMap tm_P, tm_H;       // B operands of the two GEMMs
   bool ready = false;
@@ -122,6 +125,13 @@ inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Tensor maps of the M source buffers (bf16 [rows, H], 128-row boxes, 128-byte swizzle):
+// the tensor-core router reads its token tiles straight from the sources.  Passed by
+// value as a kernel parameter (8 KB at the source limit).
+struct SrcMaps {
+  CUtensorMap m[AFD_MAX_SOURCES];
+};
+
 // ---------------------------------------------------------------- launchers
 struct LayerDims {
   int H, I, E, k, S, dtype;  // dtype: afd_dtype
@@ -133,9 +143,10 @@ cudaError_t router_setup();  // opt-in shared memory sizes (once per process)
 cudaError_t router_tc_setup();
 int router_tc_launches(const LayerDims& d, int T, int num_sms);  // kernels launch_router_tc enqueues
 cudaError_t launch_router_wnorm(const void* wrT, int H, int E, float* wnorm, cudaStream_t s);
-cudaError_t launch_router_tc(const SrcTable& st, const void* wrT, const float* bias, const float* wnorm,
-                             const CUtensorMap* tm_wr, const LayerDims& d, Workspace& ws, int num_sms,
-                             cudaStream_t s);
+// maps: the sources' tensor maps, read when router_tc_launches(d, T, num_sms) > 1
+cudaError_t launch_router_tc(const SrcTable& st, const SrcMaps& maps, const void* wrT, const float* bias,
+                             const float* wnorm, const CUtensorMap* tm_wr, const LayerDims& d, Workspace& ws,
+                             int num_sms, cudaStream_t s);
 cudaError_t launch_routing(const LayerDims& d, int T, Workspace& ws, cudaStream_t s);
 int routing_launches(int T);  // 1 for at most 256 tokens (one block), else 2
 cudaError_t launch_pack(const SrcTable& st, const LayerDims& d, int T, Workspace& ws, int num_sms,

@@ -20,11 +20,6 @@
 namespace afd {
 namespace {
 
-__device__ __forceinline__ const uint8_t* src_row(const SrcTable& st, int t, size_t row_bytes) {
-  int m = src_of_token(st, t);
-  return reinterpret_cast<const uint8_t*>(st.src[m]) + (size_t)(t - st.row0[m]) * row_bytes;
-}
-
 __device__ __forceinline__ uint8_t* out_row(const SrcTable& st, int t, size_t row_bytes) {
   int m = src_of_token(st, t);
   return reinterpret_cast<uint8_t*>(st.out[m]) + (size_t)(t - st.row0[m]) * row_bytes;

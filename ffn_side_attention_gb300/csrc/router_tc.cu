@@ -7,11 +7,11 @@
 // The selection is defined by the canonical fp32 logits L (router.cu's order).
 // Computing all T*E of them on CUDA cores is most of the router's cost, but
 // only the experts near a token's k-th largest logit can change the answer:
-//   1. stage: the token rows are copied into one contiguous bf16 matrix X and
-//      ||x_t||_2 is computed per token (rounded up);
-//   2. logits: Lt = X . Wr on tcgen05 (bf16 in, fp32 accumulate), K split
-//      over CTAs into fp32 partials that are added in a fixed order;
-//   3. select (one warp per token): with b_e a bound on |Lt_e - L_e|, the
+//   1. logits: Lt = X . Wr on tcgen05 (bf16 in, fp32 accumulate), the token
+//      tiles read by TMA straight from the source buffers (a tile never spans two
+//      sources), K split over CTAs into fp32 partials added in a fixed order;
+//   2. select (one warp per token): ||x_t||_2 from the token row (rounded up), then
+//      with b_e a bound on |Lt_e - L_e|, the
 //      canonical top-k is contained in C = {e : Lt_e + b_e >= m}, m = k-th
 //      largest of Lt - b (k experts have L >= m, and any e outside C has
 //      L_e <= Lt_e + b_e < m).  The canonical L is then computed for the
@@ -40,35 +40,10 @@
 namespace afd {
 namespace {
 
-constexpr int kMaxK = 16;
 constexpr int kMaxCand = 64;
 constexpr int kSmallRouterWaves = 3;  // small-batch path while its grid is at most this many waves
 
-// ---------------------------------------------------------------- 1. stage
-__global__ void __launch_bounds__(256) stage_x_kernel(SrcTable st, int H, uint16_t* __restrict__ Xc,
-                                                      float* __restrict__ xnorm) {
-  pdl_begin();
-  const int lane = threadIdx.x & 31;
-  for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < st.T; t += gridDim.x * 8) {
-    const int m = src_of_token(st, t);
-    const uint4* s = reinterpret_cast<const uint4*>(st.src[m]) + (size_t)(t - st.row0[m]) * (H >> 3);
-    uint4* d = reinterpret_cast<uint4*>(Xc) + (size_t)t * (H >> 3);
-    float ss = 0.0f;
-    for (int v = lane; v < (H >> 3); v += 32) {
-      const uint4 u = __ldg(s + v);
-      d[v] = u;
-      const float f[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
-                          bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
-#pragma unroll
-      for (int q = 0; q < 8; ++q) ss = fmaf(f[q], f[q], ss);
-    }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) xnorm[t] = sqrtf(ss) * (1.0f + 1.0f / 1024.0f);  // rounded up
-  }
-}
-
-// ---------------------------------------------------------------- 2. logits
+// ---------------------------------------------------------------- 1. logits
 constexpr int kRBM = 128;                     // experts per MMA tile
 constexpr int kRBN = 128;                     // tokens per tile
 constexpr int kRStages = 4;
@@ -81,11 +56,16 @@ struct LogitArgs {
   int T, E, num_kb, kb_per_split;
   float* part;  // [splits][T][E]
   int* err;
+  int nsrc;                          // sources
+  int tile0[AFD_MAX_SOURCES + 1];    // first token tile of each source (prefix of ceil(rows / 128))
+  int row0[AFD_MAX_SOURCES + 1];     // first token of each source
 };
 
-// CTA (n, m, s): tokens [128 n, +128), experts [128 m, +128), K blocks of split s.
+// CTA (n, m, s): token tile n (tile j of source src: its tokens [128 j, +128)),
+// experts [128 m, +128), K blocks of split s.  Rows past the source's end are read
+// as zeros and not stored.
 __global__ void __launch_bounds__(192, 1)
-    router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+    router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ SrcMaps maps,
                             const LogitArgs args) {
   pdl_begin();
   extern __shared__ uint8_t dyn_smem[];
@@ -98,7 +78,16 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* tfull = bars + 2 * kRStages;
   uint64_t* drain = tfull + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kRBN, m0 = blockIdx.y * kRBM;
+  int lo = 0, hi = args.nsrc - 1;  // last source whose first tile is at most this one
+  while (lo < hi) {                // (an empty source shares its first tile with the next)
+    const int mid = (lo + hi + 1) >> 1;
+    if (args.tile0[mid] <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
+  }
+  const int src = lo;
+  const int jt = (int)blockIdx.x - args.tile0[src];
+  const int n0 = args.row0[src] + jt * kRBN, m0 = blockIdx.y * kRBM;
+  const int nrows = min(kRBN, args.row0[src + 1] - n0);
+  const CUtensorMap* tmX = &maps.m[src];
   const int kb0 = blockIdx.z * args.kb_per_split;
   const int nkb = min(args.kb_per_split, args.num_kb - kb0);
   if (threadIdx.x == 0) {
@@ -111,7 +100,7 @@ __global__ void __launch_bounds__(192, 1)
     s_abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmW);
-    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(tmX);
   }
   if (warp == 1) {
     tmem_alloc(&s_tmem, 128);
@@ -134,7 +123,7 @@ __global__ void __launch_bounds__(192, 1)
       uint8_t* st = smem + s * kRStageBytes;
       mbar_arrive_expect_tx(&full[s], 2 * kRTile);
       tma_load_2d(st, &tmW, &full[s], (kb0 + kb) * 64, m0);
-      tma_load_2d(st + kRTile, &tmX, &full[s], (kb0 + kb) * 64, n0);
+      tma_load_2d(st + kRTile, tmX, &full[s], (kb0 + kb) * 64, jt * kRBN);
       filled |= 1u << s;
       fill_ph = (fill_ph & ~(1u << s)) | (ph << s);
       if (++s == kRStages) {
@@ -176,14 +165,14 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
       float* out = args.part + (size_t)blockIdx.z * args.T * args.E;
-      for (int c = 0; c < kRBN && n0 + c < args.T; c += 32) {
+      for (int c = 0; c < nrows; c += 32) {
         float d[32];
         tmem_ld_32x32b_x32(t_lane + (uint32_t)c, d);
         tmem_ld_wait();
         if (e < args.E) {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (n0 + c + j < args.T) out[(size_t)(n0 + c + j) * args.E + e] = d[j];
+            if (c + j < nrows) out[(size_t)(n0 + c + j) * args.E + e] = d[j];
         }
       }
     }
@@ -196,7 +185,7 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-// ---------------------------------------------------------------- 3. select
+// ---------------------------------------------------------------- 2. select
 __device__ __forceinline__ float fma_bf16_lo(uint32_t a, uint32_t b, float c) {
   float d;
   asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
@@ -411,10 +400,9 @@ constexpr int kSelXsMaxBytes = 8 * 4096 * 2;
 constexpr int kSelXsThreeBytes = 220 * 1024;  // three such blocks per SM
 
 struct SelectArgs {
-  const uint16_t* Xc;
+  SrcTable st;          // token rows, read in place from the source buffers
   const uint16_t* wrT;  // [E][H]
   const float* wnorm;   // [E], rounded up
-  const float* xnorm;   // [T], rounded up
   const float* bias;
   const float* part;    // [splits][T][E]
   int splits, T, H, E, k;
@@ -443,14 +431,25 @@ __global__ void __launch_bounds__(256, MINB) router_select_warp_kernel(const Sel
   if (t >= a.T) return;
   extern __shared__ uint4 sel_xs[];  // XS: [8 warps][H / 8]
   uint4* xs = sel_xs + (size_t)(threadIdx.x >> 5) * (a.H >> 3);
-  if (XS) {
-    const uint4* xg = reinterpret_cast<const uint4*>(a.Xc + (size_t)t * a.H);
-    for (int c = lane; c < (a.H >> 3); c += 32) xs[c] = __ldg(xg + c);
-    __syncwarp();
+  const uint16_t* x = reinterpret_cast<const uint16_t*>(src_row(a.st, t, (size_t)a.H * 2));
+  float xn;  // ||x_t||_2 rounded up (lane chains over its chunks, then a butterfly), and with
+  {          // XS the row into shared memory on the same pass
+    const uint4* xg = reinterpret_cast<const uint4*>(x);
+    float ss = 0.0f;
+    for (int c = lane; c < (a.H >> 3); c += 32) {
+      const uint4 u = __ldg(xg + c);
+      if (XS) xs[c] = u;
+      const float f[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
+                          bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
+#pragma unroll
+      for (int q = 0; q < 8; ++q) ss = fmaf(f[q], f[q], ss);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    xn = sqrtf(ss) * (1.0f + 1.0f / 1024.0f);
+    if (XS) __syncwarp();
   }
   const int E = a.E, k = a.k;
-  const uint16_t* x = a.Xc + (size_t)t * a.H;
-  const float xn = __ldg(a.xnorm + t);
   float* lrow = a.logits + (size_t)t * E;
   float lo[PER], hi[PER];  // bounds of the estimate (the estimate itself goes to the logits row now)
   bool taken[PER];
@@ -755,8 +754,8 @@ cudaError_t launch_router_wnorm(const void* wrT, int H, int E, float* wnorm, cud
   return cudaGetLastError();
 }
 
-int router_tc_splits(const LayerDims& d, int T, int num_sms) {
-  const int tiles = ((T + kRBN - 1) / kRBN) * ((d.E + kRBM - 1) / kRBM);
+int router_tc_splits(const LayerDims& d, int token_tiles, int num_sms) {
+  const int tiles = token_tiles * ((d.E + kRBM - 1) / kRBM);
   const int num_kb = d.H / 64;
   int splits = num_sms / tiles;  // whole waves: tiles * splits <= SM count
   splits = splits < 1 ? 1 : splits;
@@ -781,11 +780,11 @@ static bool router_small_path(const LayerDims& d, int T, int num_sms) {
   return (long)noct * ((T + kSelWarps - 1) / kSelWarps) <= (long)kSmallRouterWaves * num_sms && d.H <= kSmallMaxH;
 }
 
-int router_tc_launches(const LayerDims& d, int T, int num_sms) { return router_small_path(d, T, num_sms) ? 1 : 3; }
+int router_tc_launches(const LayerDims& d, int T, int num_sms) { return router_small_path(d, T, num_sms) ? 1 : 2; }
 
-cudaError_t launch_router_tc(const SrcTable& st, const void* wrT, const float* bias, const float* wnorm,
-                             const CUtensorMap* tm_wr, const LayerDims& d, Workspace& ws, int num_sms,
-                             cudaStream_t s) {
+cudaError_t launch_router_tc(const SrcTable& st, const SrcMaps& maps, const void* wrT, const float* bias,
+                             const float* wnorm, const CUtensorMap* tm_wr, const LayerDims& d, Workspace& ws,
+                             int num_sms, cudaStream_t s) {
   const int T = st.T;
   if (T == 0) return cudaSuccess;
   if (router_small_path(d, T, num_sms)) {
@@ -802,30 +801,35 @@ cudaError_t launch_router_tc(const SrcTable& st, const void* wrT, const float* b
     }
     return cudaGetLastError();
   }
+  const int num_kb = d.H / 64;
+  LogitArgs la{};
+  la.T = T;
+  la.E = d.E;
+  la.num_kb = num_kb;
+  la.part = ws.rpart;
+  la.err = ws.err;
+  la.nsrc = st.M;
+  la.tile0[0] = 0;
+  for (int m = 0; m < st.M; ++m) {
+    la.row0[m] = st.row0[m];
+    la.tile0[m + 1] = la.tile0[m] + (st.row0[m + 1] - st.row0[m] + kRBN - 1) / kRBN;
+  }
+  la.row0[st.M] = st.row0[st.M];
+  const int ntiles = la.tile0[st.M];
+  const int splits = router_tc_splits(d, ntiles, num_sms);
+  la.kb_per_split = (num_kb + splits - 1) / splits;
+  const int nsplit = (num_kb + la.kb_per_split - 1) / la.kb_per_split;
+  dim3 grid(ntiles, (d.E + kRBM - 1) / kRBM, nsplit);
   {
-    const cudaError_t e_ = launch_k(stage_x_kernel, dim3((T + 7) / 8), dim3(256), 0, s, st, d.H,
-                                    static_cast<uint16_t*>(ws.Xc), ws.xnorm);
+    const cudaError_t e_ = launch_k(router_logits_tc_kernel, dim3(grid), dim3(192), kRDynSmem, s, *tm_wr, maps, la);
     if (e_ != cudaSuccess) return e_;
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int splits = router_tc_splits(d, T, num_sms);
-  const int num_kb = d.H / 64;
-  LogitArgs la{T, d.E, num_kb, (num_kb + splits - 1) / splits, ws.rpart, ws.err};
-  const int nsplit = (num_kb + la.kb_per_split - 1) / la.kb_per_split;
-  dim3 grid((T + kRBN - 1) / kRBN, (d.E + kRBM - 1) / kRBM, nsplit);
-  {
-    const cudaError_t e_ = launch_k(router_logits_tc_kernel, dim3(grid), dim3(192), kRDynSmem, s, *tm_wr, ws.tm_X,
-                                    la);
-    if (e_ != cudaSuccess) return e_;
-  }
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   SelectArgs sa{};
-  sa.Xc = static_cast<const uint16_t*>(ws.Xc);
+  sa.st = st;
   sa.wrT = static_cast<const uint16_t*>(wrT);
   sa.wnorm = wnorm;
-  sa.xnorm = ws.xnorm;
   sa.bias = bias;
   sa.part = ws.rpart;
   sa.splits = nsplit;

@@ -55,6 +55,20 @@ def test_largest_router_and_source_table(dtype):
         layer.close()
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_tensor_core_router_tiles_per_source(dtype):
+    """The tensor-core router reads its 128-token tiles from each source buffer in place:
+    sources of 300, 0, 129, 1 and 77 rows give tiles that end mid-source, a source of one
+    row, and an empty source between two others (507 tokens, 128 experts: the estimate
+    path)."""
+    c = _small(dtype=dtype, E=128, k=8, H=256, I=128)
+    counts = [300, 0, 129, 1, 77]
+    layer, srcs, outs, r, ref = run_case(c, counts)
+    assert layer.launches_per_forward(sum(counts)) == 8  # two router launches: not the small path
+    assert_routing_exact(c, r, ref, sum(counts))
+    assert_close(c, out_to_f64(outs), ref_to_f64(c, ref["out"]))
+
+
 def test_bf16_zipf_bias_imbalance():
     """Zipf(1.2) log-bias on the logits: a few experts take most tokens."""
     c = _small(E=64, k=8, H=512, I=256, zipf=1.2)
@@ -217,17 +231,17 @@ def test_device_checks_report_and_the_handle_recovers(kind, text):
 
 
 def test_launches_per_forward_by_batch():
-    """One router launch for small batches (up to 224 tokens with 128 experts), three
-    (stage, logits, select) for larger ones; routing tables in one launch up to 256 tokens
-    (a single block) and two above; then pack, 2 GEMMs, combine."""
+    """One router launch for small batches (up to 224 tokens with 128 experts), two
+    (tensor-core logits, select) for larger ones; routing tables in one launch up to 256
+    tokens (a warp or a single block) and two above; then pack, 2 GEMMs, combine."""
     c = synth.CONFIGS["qwen3_bf16"]
     w = synth.make_weights(c, "cuda")
     layer = make_layer(c, w, max_tokens=4096, max_sources=8)
     assert layer.launches_per_forward(6) == 6
     assert layer.launches_per_forward(224) == 6   # last batch of the single-launch router
-    assert layer.launches_per_forward(232) == 8   # three router launches, one routing launch
-    assert layer.launches_per_forward(257) == 9   # and two routing launches above 256 tokens
-    assert layer.launches_per_forward(3160) == 9
+    assert layer.launches_per_forward(232) == 7   # two router launches, one routing launch
+    assert layer.launches_per_forward(257) == 8   # and two routing launches above 256 tokens
+    assert layer.launches_per_forward(3160) == 8
     with pytest.raises(afd.AfdError):
         layer.launches_per_forward(0)
 
@@ -416,9 +430,10 @@ def test_small_batch_router_logits_all_canonical():
     assert_close(c, out_to_f64(outs), ref_to_f64(c, ref["out"]))
 
 
-def _router_splits(H, E, T, num_sms):
-    """K splits of the tensor-core router logits, as the launcher chooses them."""
-    tiles = -(-T // 128) * -(-E // 128)
+def _router_splits(H, E, counts, num_sms):
+    """K splits of the tensor-core router logits, as the launcher chooses them: token tiles
+    of 128 rows within each source (a tile never spans two sources)."""
+    tiles = sum(-(-c // 128) for c in counts) * -(-E // 128)
     num_kb = H // 64
     splits = min(max(1, num_sms // tiles), max(num_kb // 4, 1), 8)
     per = -(-num_kb // splits)
@@ -479,7 +494,8 @@ def test_tensor_core_router_error_within_guard_band(name, B, M, n_micro):
     wn = np.linalg.norm(wf, axis=0) * (1 + 1 / 1024)
     u = 2.0 ** -24
     n = c.H / 32 + 6
-    ns = _router_splits(c.H, E, T0, torch.cuda.get_device_properties(0).multi_processor_count)
+    assert n_micro == 1  # the split count below is for the whole batch's sources
+    ns = _router_splits(c.H, E, [c.B] * c.M, torch.cuda.get_device_properties(0).multi_processor_count)
     g = (n * u / (1 - n * u) + (c.H / 8 + ns + 2) * 2.0 ** -21) * 1.0001
     babs = np.abs(bias.astype(np.float64))[None, :] if bias is not None else 0.0
     bound = g * xn[:, None] * wn[None, :] + 2.0 ** -22 * (np.abs(got) + babs)
