@@ -267,18 +267,24 @@ def test_routing_tables_edges(counts):
             assert torch.equal(x, y)
 
 
-@pytest.mark.parametrize("dtype,n_micro", [("bf16", 1), ("fp8", 1), ("bf16", 3)])
-def test_forward_captured_in_a_cuda_graph_replays_like_eager(dtype, n_micro):
+@pytest.mark.parametrize("dtype,n_micro,E", [("bf16", 1, 16), ("fp8", 1, 16), ("bf16", 3, 16), ("bf16", 1, 128),
+                                             ("fp8", 1, 128)])
+def test_forward_captured_in_a_cuda_graph_replays_like_eager(dtype, n_micro, E):
     """afd_ffn_forward enqueues no host synchronisation and keeps no per-launch host state
     on the device path, so a serving loop can capture it in a CUDA graph: replaying the
     graph over new contents of the captured source buffers gives, each time, the eager
     forward's outputs bit for bit (550 tokens: the two-launch routing tables).  With
     micro-batches the capture spans the library's own streams, forked from and joined
-    back to the capturing stream with events."""
-    c = _small(dtype=dtype, E=16, k=4, H=256, I=256, S=1)
+    back to the capturing stream with events.  With 128 experts the router takes the
+    tensor-core path, whose source tensor maps are kernel parameters: the eager forwards
+    in between run on other buffers (the library encodes their maps), and each replay
+    still reads the captured buffers."""
+    c = _small(dtype=dtype, E=E, k=4, H=256, I=256, S=1)
     counts = [300, 0, 250]
     w = synth.make_weights(c, "cuda")
     layer = make_layer(c, w, max_tokens=600, max_sources=4)
+    router = 2 if E == 128 else 1  # tensor-core logits + select, or the small-batch kernel
+    assert layer.launches_per_forward(550) == router + 2 + 1 + 2 + 1  # routing, pack, GEMMs, combine
     static_in = synth.make_sources(c, "cuda", seed=1, counts=counts)
     static_out = [torch.empty_like(x) for x in static_in]
     side = torch.cuda.Stream()
