@@ -246,11 +246,13 @@ def test_launches_per_forward_by_batch():
         layer.launches_per_forward(0)
 
 
-@pytest.mark.parametrize("counts", [[1], [255, 1], [256, 1], [20000, 20001]])
+@pytest.mark.parametrize("counts", [[1], [31, 1], [32, 1], [255, 1], [256, 1], [1000, 24], [1024, 1],
+                                    [20000, 20001]])
 def test_routing_tables_edges(counts):
-    """Routing tables at the boundary between the single-block launch (up to 256 tokens)
-    and the two-launch form: one token, exactly 256, 257, and 40001 tokens (157 blocks).
-    Tables bit-exact against the oracle, and identical on several forwards in a row."""
+    """Routing tables at the boundaries of their forms: one warp up to 32 tokens, one block
+    of 256 threads up to 256, one block of 1024 threads up to 1024, two launches above
+    (32/33, 256/257, 1024/1025 tokens, and 40001 tokens in 157 blocks).  Tables bit-exact
+    against the oracle, and identical on several forwards in a row."""
     c = _small(E=16, k=4, H=256, I=128, S=1)
     layer, srcs, outs, r, ref = run_case(c, counts)
     T = sum(counts)
