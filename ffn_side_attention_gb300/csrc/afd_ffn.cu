@@ -756,7 +756,7 @@ int afd_ffn_profile_end(afd_ffn_t h, double* ms_per_kernel, int* n_forwards) {
 }
 
 // router (one kernel for fp32 and small bf16/fp8 batches; tensor-core logits and
-// select otherwise), the routing tables (one launch up to 256 tokens, two above),
+// select otherwise), the routing tables (one launch up to 2048 tokens, two above),
 // pack, two GEMMs, combine
 int afd_ffn_launches_per_forward(afd_ffn_t h, int T) {
   if (!h || T < 1) return AFD_EINVAL;

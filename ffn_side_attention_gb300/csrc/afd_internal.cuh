@@ -148,7 +148,7 @@ cudaError_t launch_router_tc(const SrcTable& st, const SrcMaps& maps, const void
                              const float* wnorm, const CUtensorMap* tm_wr, const LayerDims& d, Workspace& ws,
                              int num_sms, cudaStream_t s);
 cudaError_t launch_routing(const LayerDims& d, int T, Workspace& ws, cudaStream_t s);
-int routing_launches(int T);  // 1 for at most 256 tokens (one block), else 2
+int routing_launches(int T);  // 1 for at most 2048 tokens, else 2
 cudaError_t launch_pack(const SrcTable& st, const LayerDims& d, int T, Workspace& ws, int num_sms,
                         cudaStream_t s);
 cudaError_t launch_combine(const SrcTable& st, const LayerDims& d, int T, Workspace& ws, int num_sms,

@@ -23,6 +23,7 @@
 // The block ranks its tokens' entries (below), keeps the per-expert counts in shared
 // memory, scans them and writes pos / perm, with no global synchronisation.
 //
+// 257..2048 tokens: one launch, routing_fused_kernel (below).
 // Larger batches: two launches, both one thread per token in blocks of 256 tokens:
 //   block_rank: per block, the per-expert counts (to a [blocks][E] array) and
 //     each entry's rank among the block's entries of the same expert, in
@@ -332,6 +333,92 @@ __global__ void __launch_bounds__(32)
   }
 }
 
+
+// Batches of 257..kFusedMaxTok tokens in one launch, no global synchronisation: block b
+// ranks its own 256 tokens' entries (as block_rank_kernel) and counts every token's
+// entries itself (per-warp histograms in shared memory), which gives both the totals
+// and its base (entries of the tokens before its own) without a second launch.
+__global__ void __launch_bounds__(kTok)
+    routing_fused_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int S, int BN,
+                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ tile_base,
+                         int32_t* __restrict__ perm, int32_t* __restrict__ pos, int32_t* __restrict__ gu_done,
+                         int* err) {
+  pdl_begin();
+  extern __shared__ uint32_t bits[];  // [kWarpsPerBlock][E] rank words, then [kWarpsPerBlock][2][E] counts
+  int* whist = reinterpret_cast<int*>(bits + kWarpsPerBlock * E);  // per warp: [0][E] before, [1][E] total
+  __shared__ int s_cnt[kMaxExperts + 1], s_base[kMaxExperts], s_off[kMaxExperts + 1], s_tb[kMaxExperts + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = E + S;
+  const int t = blockIdx.x * kTok + threadIdx.x;
+  for (int i = threadIdx.x; i < kWarpsPerBlock * E * 3; i += kTok) bits[i] = 0;
+  __syncthreads();
+  uint32_t* my = bits + warp * E;
+  int ex[kRouteMaxK];
+#pragma unroll
+  for (int j = 0; j < kRouteMaxK; ++j) ex[j] = (j < k && t < T) ? __ldg(idx + (size_t)t * k + j) : -1;
+#pragma unroll
+  for (int j = 0; j < kRouteMaxK; ++j) {
+    if (j >= k || t >= T) break;
+    if (ex[j] < 0 || ex[j] >= E) {
+      atomicOr(err, kErrRange);
+      ex[j] = -1;
+    } else {
+      atomicOr(my + ex[j], 1u << lane);
+    }
+  }
+  // every entry of the batch: per-warp counts (total, and before this block's tokens)
+  int* hb = whist + warp * 2 * E;
+  const int n = T * k, n_before = (int)blockIdx.x * kTok * k;
+  for (int i0 = threadIdx.x; i0 < n; i0 += kTok * 8) {
+    int e8[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) e8[u] = i0 + u * kTok < n ? __ldg(idx + i0 + u * kTok) : -1;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = e8[u];
+      if (e < 0 || e >= E) continue;
+      atomicAdd(hb + E + e, 1);
+      if (i0 + u * kTok < n_before) atomicAdd(hb + e, 1);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kTok) {
+    int before = 0, total = 0;
+    for (int w = 0; w < kWarpsPerBlock; ++w) {
+      before += whist[w * 2 * E + e];
+      total += whist[w * 2 * E + E + e];
+    }
+    s_cnt[e] = total;
+    s_base[e] = before;
+  }
+  if (threadIdx.x == 0 && S) s_cnt[E] = T;
+  __syncthreads();
+  scan_groups(s_cnt, G, BN, s_off, s_tb);
+  if (blockIdx.x == 0)
+    for (int g = threadIdx.x; g <= G; g += kTok) {
+      offsets[g] = s_off[g];
+      tile_base[g] = s_tb[g];
+      if (g < G) {
+        counts[g] = s_cnt[g];
+        gu_done[g] = 0;  // this forward's gate/up GEMM counts its finished items here
+      }
+    }
+  if (t < T) {
+    const uint32_t lower = (1u << lane) - 1u;
+#pragma unroll
+    for (int j = 0; j < kRouteMaxK; ++j)
+      if (ex[j] >= 0) {
+        const int e = ex[j];
+        int r = __popc(my[e] & lower);
+        for (int w = 0; w < warp; ++w) r += __popc(bits[w * E + e]);
+        const int row = s_off[e] + s_base[e] + r;
+        pos[(size_t)t * k + j] = row;
+        perm[row] = t;
+      }
+    if (S) perm[(size_t)T * k + t] = t;
+  }
+}
+
 }  // namespace
 
 __global__ void wait_probe_kernel(int* err, long long limit) {
@@ -346,7 +433,13 @@ __global__ void wait_probe_kernel(int* err, long long limit) {
   mbar_wait(&bar, 0, &abort, err, limit);  // phase 0 never completes
 }
 
-int routing_launches(int T) { return T <= kTok ? 1 : 2; }
+// One launch up to this many tokens.  Every block of the single launch reads all T*k
+// entries, so its cost grows with T times the blocks: up to 2048 tokens it beat the two
+// launches (qwen3 shapes: T = 395 step -2.9 us, T = 1580 -1.2 us; DeepSeek-V3 T = 512
+// -3.8 us, T = 2048 -4 us); at T = 3160 and 4096 it was slower (+6 us at 4096).
+constexpr int kFusedMaxTok = 2048;
+
+int routing_launches(int T) { return T <= kFusedMaxTok ? 1 : 2; }
 
 cudaError_t launch_routing(const LayerDims& d, int T, Workspace& ws, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
@@ -361,6 +454,13 @@ cudaError_t launch_routing(const LayerDims& d, int T, Workspace& ws, cudaStream_
   if (nblocks == 1) {
     const cudaError_t e_ = launch_k(routing_one_block_kernel, dim3(1), dim3(kTok),
                                     sizeof(uint32_t) * kWarpsPerBlock * d.E, s, ws.topk_idx, T, d.k, d.E, d.S, bn,
+                                    ws.counts, ws.offsets, ws.tile_base, ws.perm, ws.pos, ws.gu_done, ws.err);
+    if (e_ != cudaSuccess) return e_;
+    return cudaGetLastError();
+  }
+  if (T <= kFusedMaxTok) {
+    const cudaError_t e_ = launch_k(routing_fused_kernel, dim3(nblocks), dim3(kTok),
+                                    sizeof(uint32_t) * kWarpsPerBlock * d.E * 3, s, ws.topk_idx, T, d.k, d.E, d.S, bn,
                                     ws.counts, ws.offsets, ws.tile_base, ws.perm, ws.pos, ws.gu_done, ws.err);
     if (e_ != cudaSuccess) return e_;
     return cudaGetLastError();

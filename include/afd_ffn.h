@@ -254,8 +254,8 @@ int afd_ffn_profile_end(afd_ffn_t h, double* ms_per_kernel, int* n_forwards);
 
 /* Number of kernel launches one afd_ffn_forward of T > 0 tokens enqueues
  * (it depends on T: for bf16/fp8 layers small batches route in one launch and
- * larger ones in two; the routing tables take one launch up to 256 tokens and two
- * above).
+ * larger ones in two; the routing tables take one launch up to 2048 tokens and
+ * two above).
  * Returns AFD_EINVAL for a NULL handle or T < 1. */
 int afd_ffn_launches_per_forward(afd_ffn_t h, int T);
 

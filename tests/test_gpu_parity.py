@@ -64,7 +64,7 @@ def test_tensor_core_router_tiles_per_source(dtype):
     c = _small(dtype=dtype, E=128, k=8, H=256, I=128)
     counts = [300, 0, 129, 1, 77]
     layer, srcs, outs, r, ref = run_case(c, counts)
-    assert layer.launches_per_forward(sum(counts)) == 8  # two router launches: not the small path
+    assert layer.launches_per_forward(sum(counts)) == 7  # two router launches: not the small path
     assert_routing_exact(c, r, ref, sum(counts))
     assert_close(c, out_to_f64(outs), ref_to_f64(c, ref["out"]))
 
@@ -232,27 +232,30 @@ def test_device_checks_report_and_the_handle_recovers(kind, text):
 
 def test_launches_per_forward_by_batch():
     """One router launch for small batches (up to 224 tokens with 128 experts), two
-    (tensor-core logits, select) for larger ones; routing tables in one launch up to 256
-    tokens (a warp or a single block) and two above; then pack, 2 GEMMs, combine."""
+    (tensor-core logits, select) for larger ones; routing tables in one launch up to 2048
+    tokens (a warp, a block, or blocks that each count the whole batch) and two above;
+    then pack, 2 GEMMs, combine."""
     c = synth.CONFIGS["qwen3_bf16"]
     w = synth.make_weights(c, "cuda")
     layer = make_layer(c, w, max_tokens=4096, max_sources=8)
     assert layer.launches_per_forward(6) == 6
     assert layer.launches_per_forward(224) == 6   # last batch of the single-launch router
     assert layer.launches_per_forward(232) == 7   # two router launches, one routing launch
-    assert layer.launches_per_forward(257) == 8   # and two routing launches above 256 tokens
+    assert layer.launches_per_forward(2048) == 7
+    assert layer.launches_per_forward(2049) == 8  # two routing launches above 2048 tokens
     assert layer.launches_per_forward(3160) == 8
     with pytest.raises(afd.AfdError):
         layer.launches_per_forward(0)
 
 
-@pytest.mark.parametrize("counts", [[1], [31, 1], [32, 1], [255, 1], [256, 1], [1000, 24], [1024, 1],
-                                    [20000, 20001]])
+@pytest.mark.parametrize("counts", [[1], [31, 1], [32, 1], [255, 1], [256, 1], [1000, 24], [2000, 48],
+                                    [2048, 1], [20000, 20001]])
 def test_routing_tables_edges(counts):
     """Routing tables at the boundaries of their forms: one warp up to 32 tokens, one block
-    of 256 threads up to 256, one block of 1024 threads up to 1024, two launches above
-    (32/33, 256/257, 1024/1025 tokens, and 40001 tokens in 157 blocks).  Tables bit-exact
-    against the oracle, and identical on several forwards in a row."""
+    up to 256, one launch of blocks that each count the whole batch up to 2048, two
+    launches above (32/33, 256/257, 1024, 2048/2049 tokens, and 40001 tokens in 157
+    blocks).  Tables bit-exact against the oracle, and identical on several forwards in a
+    row."""
     c = _small(E=16, k=4, H=256, I=128, S=1)
     layer, srcs, outs, r, ref = run_case(c, counts)
     T = sum(counts)
@@ -286,7 +289,7 @@ def test_forward_captured_in_a_cuda_graph_replays_like_eager(dtype, n_micro, E):
     w = synth.make_weights(c, "cuda")
     layer = make_layer(c, w, max_tokens=600, max_sources=4)
     router = 2 if E == 128 else 1  # tensor-core logits + select, or the small-batch kernel
-    assert layer.launches_per_forward(550) == router + 2 + 1 + 2 + 1  # routing, pack, GEMMs, combine
+    assert layer.launches_per_forward(550) == router + 1 + 1 + 2 + 1  # routing, pack, GEMMs, combine
     static_in = synth.make_sources(c, "cuda", seed=1, counts=counts)
     static_out = [torch.empty_like(x) for x in static_in]
     side = torch.cuda.Stream()
