@@ -170,16 +170,21 @@ def test_forward_host_equals_device():
         layer.forward_host(hs, ho3, n_micro=0)
 
 
-@pytest.mark.parametrize("n_micro", [[1] * 5, [3] * 5, [1, 3, 1, 1, 2]])
-def test_forward_host_async_stream_of_batches(n_micro):
+@pytest.mark.parametrize("n_micro,E", [([1] * 5, 16), ([3] * 5, 16), ([1, 3, 1, 1, 2], 16), ([1] * 5, 128),
+                                       ([1, 2, 1, 1, 3], 128)])
+def test_forward_host_async_stream_of_batches(n_micro, E):
     """Consecutive asynchronous host-buffer calls (staging slots reused every other
     call, single-pass calls alternating compute streams and workspaces, batch sizes
     and micro-batch counts changing) give, call by call, the device forward's outputs;
-    afterwards the routing read-out is the last call's."""
-    c = _small(E=16, k=4, H=256, I=256, S=1)
+    afterwards the routing read-out is the last call's.  With 128 experts the larger
+    batches take the tensor-core router, whose source tensor maps then follow the
+    staging slots from call to call."""
+    c = _small(E=E, k=4, H=256, I=256, S=1)
     w = synth.make_weights(c, "cuda")
-    layer = make_layer(c, w, max_tokens=96, max_sources=4)
-    batches = [[20, 9], [33, 0, 40], [5], [48, 48], [1, 2, 3]]
+    big = E == 128
+    layer = make_layer(c, w, max_tokens=320 if big else 96, max_sources=4)
+    batches = ([[300, 9], [33, 200, 40], [5], [160, 160], [1, 250, 3]] if big else
+               [[20, 9], [33, 0, 40], [5], [48, 48], [1, 2, 3]])
     expect, hin, hout = [], [], []
     for i, counts in enumerate(batches):
         srcs = synth.make_sources(c, "cuda", seed=10 + i, counts=counts)
