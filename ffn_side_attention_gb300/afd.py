@@ -296,20 +296,23 @@ class MoELayer:
                                                                     "logits")])
         return r
 
-    def operands(self, T, stream=None):
+    def operands(self, T, stream=None, with_P=True):
         """Expert-GEMM operands of the last forward (of its first micro-batch when it was
         micro-batched): packed token rows P [R, H] and SwiGLU rows h [R, I], R = T*(k+S),
         in the layer's operand format (uint8 e4m3 codes for fp8, with scales
-        [H/128, R] and [I/128, R])."""
+        [H/128, R] and [I/128, R]).  with_P=False skips P (a bf16 forward of at most 8
+        tokens writes none, and the library rejects the request)."""
         torch = self.torch
         dev = torch.device("cuda")
         R = T * (self.k + self.S)
         et = {"fp32": torch.float32, "bf16": torch.bfloat16, "fp8": torch.uint8}[self.dtype]
-        r = {"P": torch.empty(R, self.H, dtype=et, device=dev), "h": torch.empty(R, self.I, dtype=et, device=dev)}
+        r = {"h": torch.empty(R, self.I, dtype=et, device=dev)}
+        if with_P:
+            r["P"] = torch.empty(R, self.H, dtype=et, device=dev)
         if self.dtype == "fp8":
             r["P_scale"] = torch.empty(self.H // 128, R, dtype=torch.float32, device=dev)
             r["h_scale"] = torch.empty(self.I // 128, R, dtype=torch.float32, device=dev)
-        afd_ffn_debug_operands(self.handle, self._stream(stream), r["P"].data_ptr(),
+        afd_ffn_debug_operands(self.handle, self._stream(stream), r["P"].data_ptr() if with_P else None,
                                r["P_scale"].data_ptr() if "P_scale" in r else None, r["h"].data_ptr(),
                                r["h_scale"].data_ptr() if "h_scale" in r else None)
         return r

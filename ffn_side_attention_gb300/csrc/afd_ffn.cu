@@ -51,6 +51,11 @@ struct afd_ffn {
   afd::SrcMaps src_maps[AFD_MAX_MICRO];
   const void* map_src[AFD_MAX_MICRO][AFD_MAX_SOURCES] = {};
   int map_rows[AFD_MAX_MICRO][AFD_MAX_SOURCES] = {};
+  // the same with one-row boxes, for the gate/up GEMM's direct form (bf16 batches of at
+  // most kDirectMaxTok tokens), with the sources' first rows
+  afd::DirectSrc direct_src[AFD_MAX_MICRO];
+  const void* map1_src[AFD_MAX_MICRO][AFD_MAX_SOURCES] = {};
+  int map1_rows[AFD_MAX_MICRO][AFD_MAX_SOURCES] = {};
   cudaStream_t mstream[AFD_MAX_MICRO] = {};
   cudaEvent_t ev_fork = nullptr;
   cudaEvent_t ev_join[AFD_MAX_MICRO] = {};
@@ -267,19 +272,22 @@ struct NvtxRange {
   NvtxRange& operator=(const NvtxRange&) = delete;
 };
 
-// Tensor maps of the sources of st for workspace wi (bf16 [rows, H], 128-row boxes),
-// encoded again only where a pointer or row count changed since the last forward.
-int update_src_maps(afd_ffn* h, int wi, const SrcTable& st) {
+// Tensor maps of the sources of st (bf16 [rows, H], box_rows-row boxes), encoded again
+// only where a pointer or row count changed since the last forward on that cache.
+int update_src_maps(afd_ffn* h, const SrcTable& st, afd::SrcMaps& maps, const void** cached_src, int* cached_rows,
+                    uint32_t box_rows) {
   for (int m = 0; m < st.M; ++m) {
     const int rows = st.row0[m + 1] - st.row0[m];
-    if (rows == 0 || (h->map_src[wi][m] == st.src[m] && h->map_rows[wi][m] == rows)) continue;
-    if (!make_map(&h->src_maps[wi].m[m], const_cast<void*>(st.src[m]), false, h->cfg.H, rows, 128))
+    if (rows == 0 || (cached_src[m] == st.src[m] && cached_rows[m] == rows)) continue;
+    if (!make_map(&maps.m[m], const_cast<void*>(st.src[m]), false, h->cfg.H, rows, box_rows))
       return fail(h, AFD_ECUDA, "cuTensorMapEncodeTiled failed for source %d", m);
-    h->map_src[wi][m] = st.src[m];
-    h->map_rows[wi][m] = rows;
+    cached_src[m] = st.src[m];
+    cached_rows[m] = rows;
   }
   return AFD_OK;
 }
+
+bool direct_form(const afd::LayerDims& d, int T) { return d.dtype == AFD_BF16 && T <= afd::kDirectMaxTok; }
 
 int run_layer(afd_ffn* h, const SrcTable& st, Workspace& ws, cudaStream_t s) {
   const LayerDims& d = h->dims;
@@ -289,6 +297,15 @@ int run_layer(afd_ffn* h, const SrcTable& st, Workspace& ws, cudaStream_t s) {
   NvtxRange range_layer("afd.forward");
   int rc;
   afd::TcWeights w{&h->tm_wg, &h->tm_wu, &h->tm_wd, h->sgT, h->suT, h->sdT};
+  const int wi = (int)(&ws - h->ws);
+  const bool direct = direct_form(d, T);
+  ws.direct = direct;
+  afd::DirectSrc* ds = direct ? &h->direct_src[wi] : nullptr;
+  if (direct) {
+    if ((rc = update_src_maps(h, st, ds->maps, h->map1_src[wi], h->map1_rows[wi], 1))) return rc;
+    for (int m = 0; m <= st.M; ++m) ds->row0[m] = st.row0[m];
+    ds->M = st.M;
+  }
   if ((rc = prof_mark(h, 0, s))) return rc;
   {
     NvtxRange r("afd.router");
@@ -296,8 +313,9 @@ int run_layer(afd_ffn* h, const SrcTable& st, Workspace& ws, cudaStream_t s) {
       CUDA_TRY(h, afd::launch_router(st, h->wrT, h->bias, d, ws, s));
     else
     {
-      const int wi = (int)(&ws - h->ws);
-      if (afd::router_tc_launches(d, T, h->num_sms) > 1 && (rc = update_src_maps(h, wi, st))) return rc;
+      if (afd::router_tc_launches(d, T, h->num_sms) > 1 &&
+          (rc = update_src_maps(h, st, h->src_maps[wi], h->map_src[wi], h->map_rows[wi], 128)))
+        return rc;
       CUDA_TRY(h, afd::launch_router_tc(st, h->src_maps[wi], h->wrT, h->bias, h->wnorm, &h->tm_wr, d, ws,
                                         h->num_sms, s));
     }
@@ -308,7 +326,7 @@ int run_layer(afd_ffn* h, const SrcTable& st, Workspace& ws, cudaStream_t s) {
     CUDA_TRY(h, afd::launch_routing(d, T, ws, s));
   }
   if ((rc = prof_mark(h, 2, s))) return rc;
-  {
+  if (!direct) {  // the direct form's gate/up reads the sources itself
     NvtxRange r("afd.pack");
     CUDA_TRY(h, afd::launch_pack(st, d, T, ws, h->num_sms, s));
   }
@@ -320,7 +338,7 @@ int run_layer(afd_ffn* h, const SrcTable& st, Workspace& ws, cudaStream_t s) {
     else if (d.dtype == AFD_FP8_E4M3)
       CUDA_TRY(h, afd::launch_gemm_fp8(d, T, w, ws, h->num_sms, s, which));
     else
-      CUDA_TRY(h, afd::launch_gemm_tc(d, T, w, ws, h->num_sms, s, which));
+      CUDA_TRY(h, afd::launch_gemm_tc(d, T, w, ws, h->num_sms, s, which, which == 0 ? ds : nullptr));
     if ((rc = prof_mark(h, 4 + which, s))) return rc;
   }
   {
@@ -676,6 +694,8 @@ int afd_ffn_debug_operands(afd_ffn_t h, void* stream, void* P, float* P_scale, v
   const size_t R = (size_t)ws.last_T * (h->cfg.k + h->cfg.n_shared);
   if (R == 0) return AFD_OK;
   const size_t H = h->cfg.H, I = h->cfg.I, eb = fp8 ? 1 : act_bytes(h->cfg);
+  if (P && ws.direct)
+    return fail(h, AFD_EINVAL, "P is not written for bf16 batches of at most %d tokens", afd::kDirectMaxTok);
   if (P) CUDA_TRY(h, cudaMemcpyAsync(P, ws.P, R * H * eb, cudaMemcpyDeviceToDevice, s));
   if (Hmid) CUDA_TRY(h, cudaMemcpyAsync(Hmid, ws.Hb, R * I * eb, cudaMemcpyDeviceToDevice, s));
   // scales are stored K-block major with row stride scale_ld: copy the first R of each block
@@ -757,12 +777,13 @@ int afd_ffn_profile_end(afd_ffn_t h, double* ms_per_kernel, int* n_forwards) {
 
 // router (one kernel for fp32 and small bf16/fp8 batches; tensor-core logits and
 // select otherwise), the routing tables (one launch up to 2048 tokens, two above),
-// pack, two GEMMs, combine
+// pack (none for bf16 batches of at most kDirectMaxTok = 8 tokens), two GEMMs, combine
 int afd_ffn_launches_per_forward(afd_ffn_t h, int T) {
   if (!h || T < 1) return AFD_EINVAL;
   const afd::LayerDims& d = h->dims;
   const int router = d.dtype == AFD_FP32 ? 1 : afd::router_tc_launches(d, T, h->num_sms);
-  return router + afd::routing_launches(T) + 1 /* pack */ + 2 /* GEMMs */ + 1 /* combine */;
+  const int pack = direct_form(d, T) ? 0 : 1;
+  return router + afd::routing_launches(T) + pack + 2 /* GEMMs */ + 1 /* combine */;
 }
 
 const char* afd_ffn_last_error(afd_ffn_t h) { return h ? h->err.c_str() : "handle is NULL"; }

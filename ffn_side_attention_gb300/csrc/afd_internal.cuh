@@ -76,6 +76,7 @@ struct Workspace {
   void* stage = nullptr;        // forward_host staging: [maxT, H] in + [maxT, H] out
   float* rpart = nullptr;       // [kRouterMaxSplits][maxT][E] router logit partials
   int last_T = 0;
+  bool direct = false;          // the last forward's gate/up read its tokens from the sources (P unwritten)
   CUtensorMap tm_P, tm_H;       // B operands of the two GEMMs
   bool ready = false;
 };
@@ -132,6 +133,20 @@ struct SrcMaps {
   CUtensorMap m[AFD_MAX_SOURCES];
 };
 
+// bf16 layers, batches of at most kDirectMaxTok tokens: no pack runs, and the gate/up GEMM
+// loads each packed row's token straight from its source through one-row tensor maps
+// (every group then holds at most kDirectMaxTok rows; the token producer takes up to 32,
+// one per lane).  The limit is where the two forms cross (qwen3 shapes, ms per step, pack
+// then direct: 6 tokens 0.2333 / 0.2322, 8 tokens 0.3004 / 0.2968, 12 tokens 0.3896 /
+// 0.3913, 32 tokens 0.5770 / 0.6218): one copy per row and K block, against one 32-row box
+// from P, costs more as the groups grow.
+constexpr int kDirectMaxTok = 8;
+struct DirectSrc {
+  SrcMaps maps;                    // one-row boxes: 64 columns x 1 row, 128-byte swizzle
+  int row0[AFD_MAX_SOURCES + 1];  // as SrcTable::row0
+  int M;
+};
+
 // ---------------------------------------------------------------- launchers
 struct LayerDims {
   int H, I, E, k, S, dtype;  // dtype: afd_dtype
@@ -164,8 +179,10 @@ struct TcWeights {
   const float* su;
   const float* sd;           // fp8: [(E+S), H/128, I/128]
 };
+// which: 0 gate/up + SwiGLU, 1 down.  direct (gate/up of a batch of at most kDirectMaxTok
+// tokens only): the token rows come from the sources instead of P.
 cudaError_t launch_gemm_tc(const LayerDims& d, int T, const TcWeights& w, Workspace& ws, int num_sms,
-                           cudaStream_t s, int which);  // which: 0 gate/up + SwiGLU, 1 down
+                           cudaStream_t s, int which, const DirectSrc* direct = nullptr);
 cudaError_t gemm_tc_setup();  // opt-in shared memory sizes (once per process)
 int bf16_tile_tokens(const LayerDims& d, int T);  // token-tile width of the bf16 GEMMs for a batch of T
 cudaError_t launch_gemm_fp8(const LayerDims& d, int T, const TcWeights& w, Workspace& ws, int num_sms,

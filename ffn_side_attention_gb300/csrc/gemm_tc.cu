@@ -45,7 +45,17 @@
 // on a timeout the CTA raises its abort flag and the device error word, every
 // role stops, issued copies and MMAs are drained, TMEM is freed and the kernel
 // returns.
+//
+// Direct form (gate/up of a batch of at most kDirectMaxTok = 8 tokens): no pack
+// runs.  The token producer's lanes copy the tile's rows (one lane per row) from
+// the tokens' own source buffers, one 128-byte row of K per copy through
+// one-row tensor maps whose 128-byte swizzle follows the shared-memory
+// address, so the rows land as a 32-row box would place them.  The kernel
+// then follows the routing tables directly, and the weight stream starts as
+// soon as they are final instead of after a pack launch.
 #include <cuda_bf16.h>
+
+#include <type_traits>
 
 #include "afd_internal.cuh"
 
@@ -97,7 +107,13 @@ struct TcArgs {
   // whole gate/up grid.  Null: mode 1 waits for the previous grid.
   int32_t* done;
   int done_mt;           // gate/up items per token tile (I / 128)
+  const int32_t* perm;   // packed row -> token (read by the direct token producer)
 };
+
+// Kernel parameter of the direct form (sources' one-row maps) or an empty stand-in.
+struct NoSrc {};
+template <bool DIRECT>
+using SrcParam = typename std::conditional<DIRECT, DirectSrc, NoSrc>::type;
 
 struct Item {
   int g, mt, row0, nrows;
@@ -149,15 +165,20 @@ __device__ __forceinline__ uint16_t f2bf(float v) {
   return *reinterpret_cast<uint16_t*>(&b);
 }
 
-template <int BN>
+template <int BN, bool DIRECT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
-                     const __grid_constant__ CUtensorMap tmB, const TcArgs args) {
+                     const __grid_constant__ CUtensorMap tmB, const TcArgs args,
+                     const __grid_constant__ SrcParam<DIRECT> ds) {
   // Dependent launch: this kernel starts only after the previous one (the pack,
   // or the gate/up GEMM) has passed its own wait, so the routing tables are final
   // and the weights are constant: the weight producer streams at once, and only
   // the token producer waits for the previous kernel's output (P or h).  The
   // epilogue writes (h, Y) are read by nothing that can still be running.
+  // Direct form (no pack): the previous kernel builds the routing tables, so every
+  // thread waits for it first, and the down launch, which reads the tables at its
+  // start, may launch only after that wait.
+  if constexpr (DIRECT) pdl_wait();
   pdl_trigger();
   constexpr int kWS = TileCfg<BN>::kWStages, kXS = TileCfg<BN>::kXStages, kBTile = TileCfg<BN>::kBTile;
   constexpr uint32_t kAbuf = TileCfg<BN>::kAbuf;
@@ -223,7 +244,63 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int first = (int)blockIdx.x < nact ? (int)blockIdx.x : total;  // idle CTAs take none
   volatile int* abort = &s_abort;
 
-  if (warp == 0 || warp == kTokWarp) {
+  if (DIRECT && warp == kTokWarp) {
+    if constexpr (DIRECT) {
+      // ---------------- token producer, direct form: lane r copies row r of the item's
+      // tile from its token's source, one 128-byte row of K per copy (a group holds at
+      // most kDirectMaxTok rows, and the warp takes up to 32).  Rows past nrows keep stale
+      // contents: they feed only accumulator columns that no epilogue thread stores.
+      const uint64_t pol = l2_policy_evict_last();
+      int s = 0;
+      uint32_t ph = 0, filled = 0, fill_ph = 0;
+      bool ok = true;
+      for (int item = first; ok && item < total; item += nact) {
+        const Item it = decode_item<BN>(item, args.MT, G, s_tb, s_off, s_cnt);
+        if (it.nrows > 32) {  // not reachable from a batch of at most kDirectMaxTok tokens
+          if (lane == 0) {
+            *abort = 1;
+            atomicOr(args.err, kErrRange);
+          }
+          ok = false;
+          break;
+        }
+        const CUtensorMap* map = nullptr;
+        int row = 0;
+        if (lane < it.nrows) {
+          const int t = args.perm[it.row0 + lane];
+          int lo = 0, hi = ds.M - 1;  // last source m with row0[m] <= t
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (ds.row0[mid] <= t) lo = mid; else hi = mid - 1;
+          }
+          map = &ds.maps.m[lo];
+          row = t - ds.row0[lo];
+        }
+        for (int kb = 0; kb < args.num_kb; ++kb) {
+          int go = 1;
+          if (lane == 0) {
+            go = mbar_wait(&xempty[s], ph ^ 1u, abort, args.err);
+            if (go) mbar_arrive_expect_tx(&xfull[s], (uint32_t)(it.nrows * kRowBytes));
+          }
+          if (!__shfl_sync(0xffffffffu, go, 0)) {
+            ok = false;
+            break;
+          }
+          if (lane < it.nrows)
+            tma_load_2d_hint(xsm + s * kBTile + lane * kRowBytes, map, &xfull[s], kb * 64, row, pol);
+          filled |= 1u << s;
+          fill_ph = (fill_ph & ~(1u << s)) | (ph << s);
+          if (++s == kXS) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (!ok && lane == 0)  // let the copies already issued land before the CTA exits
+        for (int q = 0; q < kXS; ++q)
+          if ((filled >> q) & 1u) mbar_wait_cycles(&xfull[q], (fill_ph >> q) & 1u, kDrainCycles);
+    }
+  } else if (warp == 0 || warp == kTokWarp) {
     if (lane == 0) {
       // ---------------- TMA producers: warp 0 weights, warp kTokWarp tokens
       const bool wprod = warp == 0;
@@ -426,16 +503,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t gemm_tc_setup() {
-  cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        TileCfg<128>::kDynSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_bf16_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             TileCfg<128>::kDynSmem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(gemm_bf16_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(gemm_bf16_kernel<256, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               TileCfg<256>::kDynSmem);
 }
 
 template <int BN>
 static cudaError_t launch_bn(const LayerDims& d, int T, const TcWeights& w, Workspace& ws, int num_sms,
-                             cudaStream_t s, int which) {
+                             cudaStream_t s, int which, const DirectSrc* direct) {
   const int G = d.E + d.S;
   const long rows = (long)T * (d.k + d.S);
   const long tiles_ub = rows / BN + G + 1;
@@ -456,6 +536,7 @@ static cudaError_t launch_bn(const LayerDims& d, int T, const TcWeights& w, Work
     a.ld_out = d.I;
     a.mode = 0;
     a.done = ws.gu_done;
+    a.perm = ws.perm;
     m0 = w.tm_wg;
     m1 = w.tm_wu;
     mb = &ws.tm_P;
@@ -476,11 +557,20 @@ static cudaError_t launch_bn(const LayerDims& d, int T, const TcWeights& w, Work
   }
   const long items_ub = tiles_ub * a.MT;
   const int grid = (int)(items_ub < num_sms ? items_ub : num_sms);
-  {
-    const cudaError_t e_ = launch_k(gemm_bf16_kernel<BN>, dim3(grid), dim3(kThreads), TileCfg<BN>::kDynSmem, s,
-                                    *m0, *m1, *mb, a);
-    if (e_ != cudaSuccess) return e_;
+  cudaError_t e_;
+  if constexpr (BN == 128) {
+    if (direct)
+      e_ = launch_k(gemm_bf16_kernel<128, true>, dim3(grid), dim3(kThreads), TileCfg<128>::kDynSmem, s, *m0, *m1,
+                    *mb, a, *direct);
+    else
+      e_ = launch_k(gemm_bf16_kernel<128, false>, dim3(grid), dim3(kThreads), TileCfg<128>::kDynSmem, s, *m0,
+                    *m1, *mb, a, NoSrc{});
+  } else {
+    if (direct) return cudaErrorInvalidValue;
+    e_ = launch_k(gemm_bf16_kernel<BN, false>, dim3(grid), dim3(kThreads), TileCfg<BN>::kDynSmem, s, *m0, *m1, *mb,
+                  a, NoSrc{});
   }
+  if (e_ != cudaSuccess) return e_;
   return cudaGetLastError();
 }
 
@@ -490,11 +580,12 @@ int bf16_tile_tokens(const LayerDims& d, int T) {
 }
 
 cudaError_t launch_gemm_tc(const LayerDims& d, int T, const TcWeights& w, Workspace& ws, int num_sms,
-                           cudaStream_t s, int which) {
+                           cudaStream_t s, int which, const DirectSrc* direct) {
   if (T == 0) return cudaSuccess;
   if (d.dtype != AFD_BF16) return cudaErrorNotSupported;
-  return bf16_tile_tokens(d, T) == 256 ? launch_bn<256>(d, T, w, ws, num_sms, s, which)
-                                       : launch_bn<128>(d, T, w, ws, num_sms, s, which);
+  if (direct && (which != 0 || T > kDirectMaxTok)) return cudaErrorInvalidValue;
+  return bf16_tile_tokens(d, T) == 256 ? launch_bn<256>(d, T, w, ws, num_sms, s, which, direct)
+                                       : launch_bn<128>(d, T, w, ws, num_sms, s, which, direct);
 }
 
 }  // namespace afd

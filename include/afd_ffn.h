@@ -214,7 +214,9 @@ int afd_ffn_debug_routing(afd_ffn_t h, void* stream, int* topk_idx, float* topk_
  * activations) with the per-token-per-128-channel rule of the fp8 layer:
  * scale = amax/448, code = e4m3(x / scale), nearest even, saturating; an
  * all-zero block has scale 1 and zero codes.  Scales are rejected (AFD_EINVAL)
- * for layers other than AFD_FP8_E4M3.  Enqueued on `stream`. */
+ * for layers other than AFD_FP8_E4M3.  A bf16 forward of at most 8 tokens
+ * writes no P (its gate/up GEMM reads the token rows from the sources), so P
+ * is then rejected (AFD_EINVAL) too.  Enqueued on `stream`. */
 int afd_ffn_debug_operands(afd_ffn_t h, void* stream, void* P, float* P_scale, void* Hmid, float* H_scale);
 
 /* Synchronise `stream`, then read and clear the device error word of every
@@ -255,7 +257,7 @@ int afd_ffn_profile_end(afd_ffn_t h, double* ms_per_kernel, int* n_forwards);
 /* Number of kernel launches one afd_ffn_forward of T > 0 tokens enqueues
  * (it depends on T: for bf16/fp8 layers small batches route in one launch and
  * larger ones in two; the routing tables take one launch up to 2048 tokens and
- * two above).
+ * two above; a bf16 layer packs no rows for at most 8 tokens).
  * Returns AFD_EINVAL for a NULL handle or T < 1. */
 int afd_ffn_launches_per_forward(afd_ffn_t h, int T);
 

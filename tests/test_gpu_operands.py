@@ -193,11 +193,42 @@ def test_bf16_operands_qwen3():
     layer.close()
 
 
+def test_bf16_small_batch_writes_no_P_and_h_follows_the_oracle():
+    """A bf16 forward of at most 8 tokens packs no rows (its gate/up GEMM copies the token
+    rows from the sources): P is rejected, and h, computed from those rows, is still the
+    nearest-even bf16 of the oracle's SwiGLU value up to boundary cases (qwen3 shapes, 6
+    tokens)."""
+    from ffn_side_attention_gb300 import afd
+
+    c = synth.CONFIGS["qwen3_bf16"].with_batch(6, 1)
+    T = c.T
+    srcs = synth.make_sources(c, "cuda", counts=[T])
+    w = synth.make_weights(c, "cuda")
+    layer = make_layer(c, w, max_tokens=T, max_sources=1)
+    layer.forward(srcs)
+    torch.cuda.synchronize()
+    layer.check()
+    r = layer.routing(T)
+    ops = layer.operands(T, with_P=False)
+    torch.cuda.synchronize()
+    with pytest.raises(afd.AfdError) as e:
+        layer.operands(T)
+    assert e.value.code == afd.AFD_EINVAL
+    tokens, experts = _row_tokens_experts(c, r, T)
+    xb = synth.to_numpy_bits(torch.cat(srcs))
+    hf = oracle.expert_hidden(cfg_dict(c), synth.weights_numpy(w), xb[tokens], experts)
+    got = ops["h"].view(torch.int16).cpu().numpy().view(np.uint16)
+    frac = _check_bf16_rounding(got, hf, c.name)
+    print(f"qwen3_bf16 T=6 h values differing: {frac:.2e}")
+    assert frac <= 1e-2
+    layer.close()
+
+
 def test_operand_scales_rejected_for_bf16():
     from ffn_side_attention_gb300 import afd
 
     c = synth.LayerConfig("small_bf16", H=256, I=256, E=8, k=2, S=0, dtype="bf16", B=0, M=0)
-    layer, w, x, r, ops = _forward(c, [9])
+    layer, w, x, r, ops = _forward(c, [9])  # above 8 tokens: P is written
     dummy = torch.empty(16, dtype=torch.float32, device="cuda")
     with pytest.raises(afd.AfdError) as e:
         afd.afd_ffn_debug_operands(layer.handle, None, None, dummy.data_ptr(), None, None)

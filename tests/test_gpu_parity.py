@@ -239,11 +239,14 @@ def test_launches_per_forward_by_batch():
     """One router launch for small batches (up to 152 tokens with 128 experts), two
     (tensor-core logits, select) for larger ones; routing tables in one launch up to 2048
     tokens (a warp, a block, or blocks that each count the whole batch) and two above;
-    then pack, 2 GEMMs, combine."""
+    then pack (none up to 8 tokens: the gate/up GEMM reads the sources), 2 GEMMs,
+    combine."""
     c = synth.CONFIGS["qwen3_bf16"]
     w = synth.make_weights(c, "cuda")
     layer = make_layer(c, w, max_tokens=4096, max_sources=8)
-    assert layer.launches_per_forward(6) == 6
+    assert layer.launches_per_forward(6) == 5
+    assert layer.launches_per_forward(8) == 5     # last batch without a pack launch
+    assert layer.launches_per_forward(9) == 6
     assert layer.launches_per_forward(152) == 6   # last batch of the single-launch router
     assert layer.launches_per_forward(160) == 7   # two router launches, one routing launch
     assert layer.launches_per_forward(2048) == 7
@@ -251,6 +254,23 @@ def test_launches_per_forward_by_batch():
     assert layer.launches_per_forward(3160) == 8
     with pytest.raises(afd.AfdError):
         layer.launches_per_forward(0)
+
+
+@pytest.mark.parametrize("counts", [[1] * 8, [0, 3, 1, 0, 4], [2] * 4 + [1], [8]])
+def test_bf16_gateup_reads_the_sources_up_to_8_tokens(counts):
+    """bf16 batches of at most 8 tokens run no pack: the gate/up GEMM's token producer copies
+    each packed row from its token's own source buffer (one lane per row, one-row tensor
+    maps).  Covered: 8 one-token sources, ragged sources with empty ones, 9 tokens (the
+    packed form, just past the limit), and one source whose 8 tokens all reach the shared
+    expert and, with 4 experts and k = 4, every routed one (every group at the limit).
+    Routing bit-exact and the full output against the oracle."""
+    c = _small(E=4 if counts == [8] else 16, k=4, H=512, I=256, S=1)
+    T = sum(counts)
+    layer, srcs, outs, r, ref = run_case(c, counts, max_sources=64)
+    assert layer.launches_per_forward(T) == (5 if T <= 8 else 6)
+    assert_routing_exact(c, r, ref, T)
+    assert_close(c, out_to_f64(outs), ref_to_f64(c, ref["out"]))
+    layer.close()
 
 
 @pytest.mark.parametrize("counts", [[1], [31, 1], [32, 1], [255, 1], [256, 1], [1000, 24], [2000, 48],
@@ -277,24 +297,28 @@ def test_routing_tables_edges(counts):
             assert torch.equal(x, y)
 
 
-@pytest.mark.parametrize("dtype,n_micro,E", [("bf16", 1, 16), ("fp8", 1, 16), ("bf16", 3, 16), ("bf16", 1, 128),
-                                             ("fp8", 1, 128)])
-def test_forward_captured_in_a_cuda_graph_replays_like_eager(dtype, n_micro, E):
+@pytest.mark.parametrize("dtype,n_micro,E,counts", [
+    ("bf16", 1, 16, [300, 0, 250]), ("fp8", 1, 16, [300, 0, 250]), ("bf16", 3, 16, [300, 0, 250]),
+    ("bf16", 1, 128, [300, 0, 250]), ("fp8", 1, 128, [300, 0, 250]),
+    ("bf16", 1, 16, [5, 0, 3]), ("bf16", 3, 128, [5, 0, 3])])  # no pack: the GEMM reads the sources
+def test_forward_captured_in_a_cuda_graph_replays_like_eager(dtype, n_micro, E, counts):
     """afd_ffn_forward enqueues no host synchronisation and keeps no per-launch host state
     on the device path, so a serving loop can capture it in a CUDA graph: replaying the
     graph over new contents of the captured source buffers gives, each time, the eager
-    forward's outputs bit for bit (550 tokens: the two-launch routing tables).  With
-    micro-batches the capture spans the library's own streams, forked from and joined
-    back to the capturing stream with events.  With 128 experts the router takes the
-    tensor-core path, whose source tensor maps are kernel parameters: the eager forwards
-    in between run on other buffers (the library encodes their maps), and each replay
-    still reads the captured buffers."""
+    forward's outputs bit for bit (550 tokens: the one-launch routing tables for more than
+    256 tokens; 8 tokens: no pack).  With micro-batches the capture spans the library's own
+    streams, forked from and joined back to the capturing stream with events.  With 128
+    experts at 550 tokens the router takes the tensor-core path, and at 8 bf16 tokens the
+    gate/up GEMM reads the sources: both through source tensor maps passed as kernel
+    parameters.  The eager forwards in between run on other buffers (the library encodes
+    their maps), and each replay still reads the captured buffers."""
     c = _small(dtype=dtype, E=E, k=4, H=256, I=256, S=1)
-    counts = [300, 0, 250]
+    T = sum(counts)
     w = synth.make_weights(c, "cuda")
     layer = make_layer(c, w, max_tokens=600, max_sources=4)
-    router = 2 if E == 128 else 1  # tensor-core logits + select, or the small-batch kernel
-    assert layer.launches_per_forward(550) == router + 1 + 1 + 2 + 1  # routing, pack, GEMMs, combine
+    router = 2 if E == 128 and T > 152 else 1  # tensor-core logits + select, or the small-batch kernel
+    pack = 0 if dtype == "bf16" and T <= 8 else 1
+    assert layer.launches_per_forward(T) == router + 1 + pack + 2 + 1  # routing, pack, GEMMs, combine
     static_in = synth.make_sources(c, "cuda", seed=1, counts=counts)
     static_out = [torch.empty_like(x) for x in static_in]
     side = torch.cuda.Stream()
