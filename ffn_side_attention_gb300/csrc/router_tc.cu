@@ -630,7 +630,6 @@ __global__ void __launch_bounds__(32 * kSelWarps, 1)
     router_small_kernel(const SrcTable st, const uint16_t* __restrict__ wrT, const float* __restrict__ bias, int H,
                         int E, int k, float* __restrict__ logits, int32_t* __restrict__ topk_idx,
                         float* __restrict__ topk_w, int32_t* __restrict__ ticket, int* err) {
-  pdl_begin();
   extern __shared__ __align__(16) uint4 s_w[];  // [kOct][H/8] router rows, then [8][H/8] token rows
   __shared__ __align__(8) uint64_t bar;
   __shared__ int s_abort;
@@ -639,6 +638,8 @@ __global__ void __launch_bounds__(32 * kSelWarps, 1)
   const int oct = blockIdx.x % noct;
   const int e0 = oct * kOct, ne = min(kOct, E - e0);
   const int nc = H >> 3;
+  // the router rows are weights: their copy starts before the wait on the previous kernel,
+  // the token rows' after it (a caller may feed one layer's outputs back as the sources)
   if (threadIdx.x == 0) {
     s_abort = 0;
     mbar_init(&bar, 1);
@@ -646,6 +647,10 @@ __global__ void __launch_bounds__(32 * kSelWarps, 1)
     const int tok0 = (blockIdx.x / noct) * kSelWarps, ntok = min(kSelWarps, st.T - tok0);
     mbar_arrive_expect_tx(&bar, (uint32_t)((ne + ntok) * nc * 16));
     bulk_load(s_w, reinterpret_cast<const uint4*>(wrT) + (size_t)e0 * nc, (uint32_t)(ne * nc * 16), &bar);
+  }
+  pdl_begin();
+  if (threadIdx.x == 0) {
+    const int tok0 = (blockIdx.x / noct) * kSelWarps, ntok = min(kSelWarps, st.T - tok0);
     for (int w = 0; w < ntok; ++w) {
       const int tw = tok0 + w, m = src_of_token(st, tw);
       bulk_load(s_w + (size_t)(kOct + w) * nc, reinterpret_cast<const uint4*>(st.src[m]) + (size_t)(tw - st.row0[m]) * nc,
