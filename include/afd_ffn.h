@@ -8,7 +8,8 @@
  *   histogram / exclusive prefix sum / stable expert-contiguous order ->
  *   pack (optionally e4m3 quantisation) -> grouped gate/up GEMM + SwiGLU ->
  *   grouped down GEMM x routing weight -> weighted combine back into the M
- *   output buffers.
+ *   output buffers.  (A bf16 batch of at most 8 tokens skips the pack: its
+ *   gate/up GEMM reads the token rows from the source buffers.)
  *
  * Sources for the operation:
  *   - "大模型推理的内存与计算解耦：AFD 架构解析与性能验证" (FastAFD blog),
@@ -246,7 +247,8 @@ const char* afd_ffn_last_error(afd_ffn_t h);
 /* Per-kernel timing (benchmark aid).  afd_ffn_profile_begin() makes every
  * following forward record CUDA events on its stream around each of its
  * AFD_NUM_KERNELS kernels (router, routing tables, pack, gate/up GEMM, down
- * GEMM, combine).  afd_ffn_profile_end() synchronises the device, writes the
+ * GEMM, combine; a forward without a pack launch records ~0 for it).
+ * afd_ffn_profile_end() synchronises the device, writes the
  * summed milliseconds per kernel over the recorded forwards into
  * ms_per_kernel[AFD_NUM_KERNELS] and their number into *n_forwards, and turns
  * recording off.  Recording adds one event per kernel launch. */
