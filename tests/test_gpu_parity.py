@@ -127,6 +127,25 @@ def test_pipelined_equals_single_and_deterministic():
     layer.check()
 
 
+@pytest.mark.parametrize("counts,n_micro", [([9, 0, 8], 2), ([4, 21], 3), ([33], 4)])
+def test_pipelined_mixes_packed_and_direct_micro_batches(counts, n_micro):
+    """Micro-batches on both sides of the pack-free limit (8 bf16 tokens) in one forward:
+    17 tokens in 9 + 8, 25 in 9 + 8 + 8, 33 in 9 + 8 + 8 + 8.  The first micro-batch's
+    gate/up reads the packed rows, the others' read the sources; the outputs equal the
+    single pass bit for bit, and the oracle within the bf16 tolerance."""
+    c = _small(E=16, k=4, S=1, H=512, I=256)
+    layer, srcs, outs, r, ref = run_case(c, counts)
+    assert_close(c, out_to_f64(outs), ref_to_f64(c, ref["out"]))
+    single = [o.clone() for o in outs]
+    for _ in range(2):
+        p = layer.forward(srcs, n_micro=n_micro)
+        torch.cuda.synchronize()
+        for x, y in zip(single, p):
+            assert torch.equal(x, y), f"n_micro={n_micro} differs from the single pass"
+    layer.check()
+    layer.close()
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "fp8"])
 def test_outputs_follow_their_tokens(dtype):
     """Per-token independence on the GPU: permuting tokens within and across the source
