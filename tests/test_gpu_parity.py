@@ -127,6 +127,25 @@ def test_pipelined_equals_single_and_deterministic():
     layer.check()
 
 
+def test_fp8_pipelined_equals_single_pass():
+    """The fp8 layer micro-batched in 2, 3 and 4 parts gives the single pass bit for bit:
+    activations are quantised per token, every MMA row is one token's, the promotion scale
+    and the re-quantisation of h are per token, and the combine sums each token's slots in
+    order, so how tokens share tiles changes nothing.  The single pass matches the oracle."""
+    c = _small(dtype="fp8", E=16, k=4, S=1, H=512, I=256)
+    counts = [50, 0, 77, 12]
+    layer, srcs, outs, r, ref = run_case(c, counts)
+    assert_close(c, out_to_f64(outs), ref_to_f64(c, ref["out"]))
+    single = [o.clone() for o in outs]
+    for n in (2, 3, 4):
+        p = layer.forward(srcs, n_micro=n)
+        torch.cuda.synchronize()
+        for x, y in zip(single, p):
+            assert torch.equal(x, y), f"fp8 n_micro={n} differs from the single pass"
+    layer.check()
+    layer.close()
+
+
 @pytest.mark.parametrize("counts,n_micro", [([9, 0, 8], 2), ([4, 21], 3), ([33], 4)])
 def test_pipelined_mixes_packed_and_direct_micro_batches(counts, n_micro):
     """Micro-batches on both sides of the pack-free limit (8 bf16 tokens) in one forward:
@@ -189,16 +208,17 @@ def test_forward_host_equals_device():
         layer.forward_host(hs, ho3, n_micro=0)
 
 
-@pytest.mark.parametrize("n_micro,E", [([1] * 5, 16), ([3] * 5, 16), ([1, 3, 1, 1, 2], 16), ([1] * 5, 128),
-                                       ([1, 2, 1, 1, 3], 128)])
-def test_forward_host_async_stream_of_batches(n_micro, E):
+@pytest.mark.parametrize("n_micro,E,dtype", [([1] * 5, 16, "bf16"), ([3] * 5, 16, "bf16"),
+                                             ([1, 3, 1, 1, 2], 16, "bf16"), ([1] * 5, 128, "bf16"),
+                                             ([1, 2, 1, 1, 3], 128, "bf16"), ([1, 3, 1, 1, 2], 16, "fp8")])
+def test_forward_host_async_stream_of_batches(n_micro, E, dtype):
     """Consecutive asynchronous host-buffer calls (staging slots reused every other
     call, single-pass calls alternating compute streams and workspaces, batch sizes
     and micro-batch counts changing) give, call by call, the device forward's outputs;
     afterwards the routing read-out is the last call's.  With 128 experts the larger
     batches take the tensor-core router, whose source tensor maps then follow the
-    staging slots from call to call."""
-    c = _small(E=E, k=4, H=256, I=256, S=1)
+    staging slots from call to call.  One case runs the fp8 layer (quantising pack)."""
+    c = _small(dtype=dtype, E=E, k=4, H=256, I=256, S=1)
     w = synth.make_weights(c, "cuda")
     big = E == 128
     layer = make_layer(c, w, max_tokens=320 if big else 96, max_sources=4)
