@@ -305,6 +305,11 @@ int run_layer(afd_ffn* h, const SrcTable& st, Workspace& ws, cudaStream_t s) {
     if ((rc = update_src_maps(h, st, ds->maps, h->map1_src[wi], h->map1_rows[wi], 1))) return rc;
     for (int m = 0; m <= st.M; ++m) ds->row0[m] = st.row0[m];
     ds->M = st.M;
+    ds->topk_idx = ws.topk_idx;
+    ds->T = T;
+    ds->k = d.k;
+    ds->E = d.E;
+    ds->S = d.S;
   }
   if ((rc = prof_mark(h, 0, s))) return rc;
   {

@@ -51,8 +51,9 @@
 // the tokens' own source buffers, one 128-byte row of K per copy through
 // one-row tensor maps whose 128-byte swizzle follows the shared-memory
 // address, so the rows land as a 32-row box would place them.  The kernel
-// then follows the routing tables directly, and the weight stream starts as
-// soon as they are final instead of after a pack launch.
+// builds its work list from the router's top-k itself (a bit per token per
+// group), so the weight stream starts while the routing kernel still runs; it
+// lets the down launch start only after that kernel has completed.
 #include <cuda_bf16.h>
 
 #include <type_traits>
@@ -107,7 +108,6 @@ struct TcArgs {
   // whole gate/up grid.  Null: mode 1 waits for the previous grid.
   int32_t* done;
   int done_mt;           // gate/up items per token tile (I / 128)
-  const int32_t* perm;   // packed row -> token (read by the direct token producer)
 };
 
 // Kernel parameter of the direct form (sources' one-row maps) or an empty stand-in.
@@ -175,11 +175,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // and the weights are constant: the weight producer streams at once, and only
   // the token producer waits for the previous kernel's output (P or h).  The
   // epilogue writes (h, Y) are read by nothing that can still be running.
-  // Direct form (no pack): the previous kernel builds the routing tables, so every
-  // thread waits for it first, and the down launch, which reads the tables at its
-  // start, may launch only after that wait.
-  if constexpr (DIRECT) pdl_wait();
-  pdl_trigger();
+  // Direct form (no pack): the previous kernel is the routing kernel, which started
+  // once the router had completed; this kernel reads only the router's top-k and the
+  // sources before its wait on that kernel (below).
+  if constexpr (!DIRECT) pdl_trigger();
   constexpr int kWS = TileCfg<BN>::kWStages, kXS = TileCfg<BN>::kXStages, kBTile = TileCfg<BN>::kBTile;
   constexpr uint32_t kAbuf = TileCfg<BN>::kAbuf;
   extern __shared__ uint8_t dyn_smem[];
@@ -191,6 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_tb[kMaxExperts + 1], s_off[kMaxExperts + 1], s_cnt[kMaxExperts];
+  __shared__ uint32_t s_mask[DIRECT ? kMaxExperts : 1];  // direct form: each group's tokens
   uint64_t* wfull = bars;
   uint64_t* wempty = bars + kWS;
   uint64_t* xfull = bars + 2 * kWS;
@@ -201,10 +201,61 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = args.G;
-  for (int g = threadIdx.x; g <= G; g += kThreads) {
-    s_tb[g] = args.tile_base[g];
-    s_off[g] = args.offsets[g];
-    if (g < G) s_cnt[g] = args.counts[g];
+  if constexpr (DIRECT) {
+    // The routing tables of this batch, built from the router's top-k (complete: the
+    // routing kernel that launched this grid waited for it), as the routing kernel builds
+    // them: per group a bit per token, counts, offsets and tile bases by a warp scan.
+    for (int g = threadIdx.x; g < G; g += kThreads) s_mask[g] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < ds.T * ds.k; i += kThreads) {
+      const int e = ds.topk_idx[i];
+      if (e >= 0 && e < ds.E) atomicOr(&s_mask[e], 1u << (i / ds.k));
+    }
+    if (ds.S && threadIdx.x == 0) s_mask[ds.E] = ds.T >= 32 ? ~0u : (1u << ds.T) - 1u;
+    __syncthreads();
+    if (warp == 0) {
+      const int c = (G + 31) / 32;
+      int rows = 0, tiles = 0;
+      for (int i = 0; i < c; ++i) {
+        const int g = lane * c + i;
+        if (g < G) {
+          const int n = __popc(s_mask[g]);
+          rows += n;
+          tiles += (n + BN - 1) / BN;
+        }
+      }
+      int ir = rows, it = tiles;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, ir, o), b = __shfl_up_sync(0xffffffffu, it, o);
+        if (lane >= o) {
+          ir += a;
+          it += b;
+        }
+      }
+      int row = ir - rows, tile = it - tiles;
+      for (int i = 0; i < c; ++i) {
+        const int g = lane * c + i;
+        if (g < G) {
+          const int n = __popc(s_mask[g]);
+          s_off[g] = row;
+          s_tb[g] = tile;
+          s_cnt[g] = n;
+          row += n;
+          tile += (n + BN - 1) / BN;
+        }
+      }
+      if (lane == 31) {
+        s_off[G] = row;
+        s_tb[G] = tile;
+      }
+    }
+  } else {
+    for (int g = threadIdx.x; g <= G; g += kThreads) {
+      s_tb[g] = args.tile_base[g];
+      s_off[g] = args.offsets[g];
+      if (g < G) s_cnt[g] = args.counts[g];
+    }
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWS; ++s) {
@@ -243,6 +294,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nact = rounds <= kEvenRounds ? (total + rounds - 1) / rounds : (int)gridDim.x;
   const int first = (int)blockIdx.x < nact ? (int)blockIdx.x : total;  // idle CTAs take none
   volatile int* abort = &s_abort;
+  // Direct form: the down launch reads the routing kernel's tables as it starts, so this
+  // grid lets it launch only once that kernel has completed: every thread waits for it and
+  // then triggers; the two producers do so once their first stages are issued.
+  if constexpr (DIRECT)
+    if (!(warp == 0 && lane == 0) && warp != kTokWarp) {
+      pdl_wait();
+      pdl_trigger();
+    }
 
   if (DIRECT && warp == kTokWarp) {
     if constexpr (DIRECT) {
@@ -251,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // most kDirectMaxTok rows, and the warp takes up to 32).  Rows past nrows keep stale
       // contents: they feed only accumulator columns that no epilogue thread stores.
       const uint64_t pol = l2_policy_evict_last();
-      int s = 0;
+      int s = 0, issued = 0;
       uint32_t ph = 0, filled = 0, fill_ph = 0;
       bool ok = true;
       for (int item = first; ok && item < total; item += nact) {
@@ -267,7 +326,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* map = nullptr;
         int row = 0;
         if (lane < it.nrows) {
-          const int t = args.perm[it.row0 + lane];
+          uint32_t m = s_mask[it.g];  // the group's rows are its tokens in ascending order
+          for (int j = it.row0 - s_off[it.g] + lane; j > 0; --j) m &= m - 1u;
+          const int t = __ffs(m) - 1;
           int lo = 0, hi = ds.M - 1;  // last source m with row0[m] <= t
           while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
@@ -294,7 +355,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             s = 0;
             ph ^= 1u;
           }
+          if (++issued == kXS) {
+            pdl_wait();
+            pdl_trigger();
+          }
         }
+      }
+      if (issued < kXS) {
+        pdl_wait();
+        pdl_trigger();
       }
       if (!ok && lane == 0)  // let the copies already issued land before the CTA exits
         for (int q = 0; q < kXS; ++q)
@@ -357,6 +426,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(&fb[s], bytes);
+          if (DIRECT && wprod && ld_n + 1 == kWS) {
+            pdl_wait();
+            pdl_trigger();
+          }
           if (wprod) {
             uint8_t* st = wsm + s * kWTileBytes;
             tma_load_2d_hint(st, &tmA0, &fb[s], 0, (rb0 * args.num_kb + kb) * 128, pol);
@@ -373,6 +446,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ph ^= 1u;
           }
         }
+      }
+      if (DIRECT && wprod && ld_n < kWS) {  // fewer loads than the first ring: wait now
+        pdl_wait();
+        pdl_trigger();
       }
       if (!ok)  // let the copies already issued land before the CTA exits
         for (int q = 0; q < nst; ++q)
@@ -536,7 +613,6 @@ static cudaError_t launch_bn(const LayerDims& d, int T, const TcWeights& w, Work
     a.ld_out = d.I;
     a.mode = 0;
     a.done = ws.gu_done;
-    a.perm = ws.perm;
     m0 = w.tm_wg;
     m1 = w.tm_wu;
     mb = &ws.tm_P;
