@@ -3,7 +3,8 @@
 // Host side only: argument validation, weight re-layout at create time,
 // workspace ownership, TMA descriptor set-up and the launch sequence of one
 // forward (router -> routing tables -> pack -> gate/up GEMM -> down GEMM ->
-// combine), all enqueued on the caller's stream with no host synchronisation.
+// combine; no pack for bf16 batches of at most 8 tokens), all enqueued on the
+// caller's stream with no host synchronisation.
 // The batch shape (src_counts) is the control-plane metadata of the FastAFD
 // blog's transport (section 3); the M device pointers are its data plane.
 #include <cudaTypedefs.h>

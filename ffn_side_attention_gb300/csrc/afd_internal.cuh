@@ -136,10 +136,11 @@ struct SrcMaps {
 // bf16 layers, batches of at most kDirectMaxTok tokens: no pack runs, and the gate/up GEMM
 // loads each packed row's token straight from its source through one-row tensor maps
 // (every group then holds at most kDirectMaxTok rows; the token producer takes up to 32,
-// one per lane), with a work list it builds from the router's top-k.  The limit is where the two forms cross (qwen3 shapes, ms per step, pack
-// then direct: 6 tokens 0.2333 / 0.2322, 8 tokens 0.3004 / 0.2968, 12 tokens 0.3896 /
-// 0.3913, 32 tokens 0.5770 / 0.6218): one copy per row and K block, against one 32-row box
-// from P, costs more as the groups grow.
+// one per lane), with a work list it builds from the router's top-k.  The limit is where
+// the two forms cross (qwen3 shapes, ms per step, pack then direct: 6 tokens 0.2333 /
+// 0.2322, 8 tokens 0.3004 / 0.2968, 12 tokens 0.3896 / 0.3913, 32 tokens 0.5770 /
+// 0.6218): one copy per row and K block, against one 32-row box from P, costs more as
+// the groups grow.
 constexpr int kDirectMaxTok = 8;
 struct DirectSrc {
   SrcMaps maps;                    // one-row boxes: 64 columns x 1 row, 128-byte swizzle
